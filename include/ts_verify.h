@@ -1,0 +1,191 @@
+/*
+ * ts_verify.h - C ABI of libtsverify.so: the speculative-decoding verify-and-sample
+ * step on one GB300 (sm_103a) GPU.
+ *
+ * What the step computes is defined by three public pages:
+ *   [TS-FI]  TokenSpeed, runtime/sampling/backends/flashinfer.py,
+ *            FlashInferSamplingBackend.verify() / .sample();
+ *   [TS-DP]  TokenSpeed, runtime/distributed/dp_sampling_comm.py (output layout);
+ *   [TRT-IF] TensorRT-LLM, _torch/speculative/interface.py,
+ *            rejection_sampling_one_model(), SpecWorkerBase._sample_sharded_temperature().
+ *
+ * Conventions for every call
+ * --------------------------
+ *  - Pointers named *_host are host memory; every other pointer is CUDA device memory
+ *    owned by the caller. The library never allocates, frees or synchronises: each
+ *    call enqueues its kernels on `stream` and returns.
+ *  - Rows: a [batch, R, vocab] tensor is rows b*R + j of a row-major matrix whose rows
+ *    are `ld` elements apart (ld >= vocab). R = D + 1 for verification.
+ *  - Token ids are int32; seeds and offsets int64; probabilities fp32. Logits are fp32
+ *    or bf16 (TS_F32 / TS_BF16); bf16 is widened to fp32 exactly.
+ *  - Knobs: temperature < TS_GREEDY_T (or NaN) means greedy (one-hot at the argmax);
+ *    top_k <= 0 or >= vocab means no top-k; top_p >= 1 means no top-p. A NULL knob
+ *    array means "off" (temperature 1).
+ *  - Ties: the argmax and top-k keep the lowest token id among equal values.
+ *  - Workspace: calls that need scratch take `workspace`/`ws_bytes`, a caller-owned
+ *    device buffer of at least ts_workspace_size(...) bytes that must be zero-filled
+ *    once before its first use (ts_workspace_init does that). Every call leaves it
+ *    zero again, so it can be reused by later calls on the same stream without
+ *    clearing. Calls that overlap on the GPU must not share a workspace.
+ *  - Errors: arguments are validated on the host before any launch; an invalid call
+ *    returns TS_ERR_INVALID_ARG / TS_ERR_UNSUPPORTED_DTYPE and enqueues nothing. A
+ *    failed launch returns TS_ERR_CUDA. ts_last_error_message() (thread-local) gives
+ *    the reason for the last failure of the calling thread.
+ *  - Limits: 1 <= vocab <= TS_MAX_VOCAB, 0 <= D <= TS_MAX_DRAFT, batch >= 1.
+ *  - Inputs with NaN are outside the contract (no fault; results unspecified).
+ */
+#ifndef TS_VERIFY_H
+#define TS_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TS_OK = 0,
+  TS_ERR_INVALID_ARG = 1,
+  TS_ERR_UNSUPPORTED_DTYPE = 2,
+  TS_ERR_CUDA = 3,
+  TS_ERR_TIMEOUT = 4 /* a bounded device-side wait gave up (see ts_device_error) */
+} ts_status;
+
+typedef enum { TS_F32 = 0, TS_BF16 = 1 } ts_dtype;
+
+#define TS_GREEDY_T 1e-5f
+#define TS_MAX_DRAFT 64
+#define TS_MAX_VOCAB (1 << 22)
+
+/* Bytes of workspace any call below needs for `batch` requests of `rows_per_req` rows
+ * over `vocab` tokens (rows_per_req = D + 1 for verification, n_per_req for
+ * ts_gumbel_max_sample, 1 for per-row calls with batch = rows). */
+size_t ts_workspace_size(int64_t batch, int32_t rows_per_req, int64_t vocab);
+
+/* Zero-fills a workspace on `stream` (cudaMemsetAsync). */
+ts_status ts_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* The reason for the calling thread's last non-OK status ("" if none). */
+const char* ts_last_error_message(void);
+
+/* Synchronises the current device and reads (then, if clear != 0, clears) the
+ * library's device error word: 0 if no bounded wait ever gave up. Returns
+ * TS_ERR_TIMEOUT if a wait gave up, TS_ERR_CUDA if the read failed. A diagnostic,
+ * not part of the hot path. */
+ts_status ts_device_error(uint32_t* word_host, int clear);
+
+/* Temperature softmax [TS-FI verify(): softmax(logits, temperature)].
+ * probs_out[r, i] = exp((x_ri - M_r)/T_r) / sum_k exp((x_rk - M_r)/T_r), M_r the row max;
+ * one-hot at the row argmax when T_r < TS_GREEDY_T. temperature: [rows] or NULL (= 1).
+ * logits: [rows, ld] of `dt`; probs_out: [rows, vocab] fp32, contiguous, must not alias
+ * logits. */
+ts_status ts_softmax_temp(const void* logits, ts_dtype dt, int64_t rows, int64_t vocab,
+                          int64_t ld, const float* temperature, float* probs_out,
+                          cudaStream_t stream);
+
+/* Top-k then top-p renormalisation of probability rows, fused [TS-FI verify():
+ * fused_topk_topp_renorm, the replacement for top_k_renorm_prob followed by
+ * top_p_renorm_prob]. Top-k keeps the k largest probabilities (exactly k; lowest ids
+ * first among equals); top-p then keeps, in the same order, each token whose
+ * preceding kept mass is below top_p times the kept mass (the first token always).
+ * The result is renormalised; dropped tokens are 0.
+ * probs: [rows, ld] fp32 (non-negative); top_k: [rows] or NULL; top_p: [rows] or NULL;
+ * probs_out: [rows, vocab] fp32 contiguous; may equal probs when ld == vocab. */
+ts_status ts_topk_topp_renorm(const float* probs, int64_t rows, int64_t vocab, int64_t ld,
+                              const int32_t* top_k, const float* top_p, float* probs_out,
+                              cudaStream_t stream);
+
+/* Greedy chain verification [TS-FI verify(): sampling_argmax then verify_chain_greedy;
+ * TRT-IF strict acceptance]. Draft j of request b is accepted while it equals the
+ * argmax of target row (b, j); the argmax of the first mismatching row (or of row D,
+ * the bonus) follows.
+ * target_logits: [batch*(D+1), ld] of `dt`; draft_tokens: [batch, D].
+ * Out: accepted_tokens [batch, D+1] (accepted drafts, the target token, then -1),
+ * accept_length [batch] in [1, D+1] (tokens emitted), accept_index [batch, D+1]
+ * (b*(D+1)+j for emitted positions, else -1; NULL = skip), logprobs [batch, D+1]
+ * (log-softmax at temperature 1 of the raw logits at each emitted token, 0 after;
+ * NULL = skip). */
+ts_status ts_verify_chain_greedy(const void* target_logits, ts_dtype dt, int64_t batch,
+                                 int32_t D, int64_t vocab, int64_t ld,
+                                 const int32_t* draft_tokens, int32_t* accepted_tokens,
+                                 int32_t* accept_length, int32_t* accept_index,
+                                 float* logprobs, void* workspace, size_t ws_bytes,
+                                 cudaStream_t stream);
+
+/* Arguments of ts_chain_spec_sampling. Layouts as in the comments; NULL where allowed. */
+typedef struct ts_chain_args {
+  const void* target;        /* [batch*(D+1), ld]: logits (target_is_logits = 1, dtype
+                                target_dtype) or fp32 probabilities (target_is_logits = 0) */
+  int32_t target_dtype;      /* ts_dtype; must be TS_F32 for probabilities */
+  int32_t target_is_logits;
+  int64_t batch;
+  int32_t D;
+  int32_t reserved0;
+  int64_t vocab;
+  int64_t ld;
+  const float* temperature;  /* [batch] or NULL; logits only */
+  const int32_t* top_k;      /* [batch] or NULL; logits only */
+  const float* top_p;        /* [batch] or NULL; logits only */
+  const float* draft_probs;  /* [batch*D, ld_draft] fp32, or NULL: target-only (the draft
+                                is a point mass on the drafted token) */
+  int64_t ld_draft;
+  const int32_t* draft_tokens; /* [batch, D]; ids outside [0, vocab) are never accepted */
+  const int64_t* seed;       /* [batch] Philox key (two's-complement bits) */
+  const int64_t* offset;     /* [batch] Philox counter base */
+  const float* uniforms;     /* [batch, D+1] explicit coins in (0, 1) replacing Philox:
+                                u_j for the test at j < D, u_D for the final draw; or NULL */
+  int32_t* accepted_tokens;  /* [batch, D+1] out */
+  int32_t* accept_length;    /* [batch] out */
+  int32_t* accept_index;     /* [batch, D+1] out, or NULL */
+  float* logprobs;           /* [batch, D+1] out, or NULL: logits: log-softmax at T = 1 of
+                                the raw row; probabilities: ln p(token); 0 after the last
+                                emitted token */
+} ts_chain_args;
+
+/* Chain speculative sampling [TRT-IF rejection_sampling_one_model; TS-FI verify():
+ * softmax + fused top-k/top-p renorm + chain_speculative_sampling_target_only].
+ * p_j is the target distribution of row (b, j): softmax(logits/T) renormalised by top-k
+ * and top-p (logits), or the given row (probabilities). For j = 0..D-1 with draft x_j:
+ *   with draft probs q: accept iff u_j * q_j(x_j) < p_j(x_j)  (accept w.p. min(1, p/q));
+ *   target-only:        accept iff u_j < p_j(x_j).
+ * At the first rejection j*, the token is drawn from norm(max(p_j* - q_j*, 0))
+ * (target-only: p_j* with x_j* removed); if all D drafts are accepted, the bonus is
+ * drawn from p_D. The draw uses u_D: the smallest token id whose inclusive prefix mass,
+ * in token-id order, exceeds u_D times the total mass. With explicit probabilities the
+ * accept test is evaluated in fp32 (one rounded product); the residual max(p - q, 0) is
+ * formed elementwise in fp32.
+ * Coins: uniforms if given, else Philox4x32-10 keyed by seed[b] with counter
+ * (j, 0xFFFFFFFF, lo32(offset[b]), hi32(offset[b])), word 0 mapped to
+ * (2*(w >> 9) + 1) * 2^-24.
+ * Outputs as ts_verify_chain_greedy. */
+ts_status ts_chain_spec_sampling(const ts_chain_args* args, void* workspace,
+                                 size_t ws_bytes, cudaStream_t stream);
+
+/* Temperature-only sampling by Gumbel-max [TRT-IF _sample_sharded_temperature: the
+ * argmax of x/T plus Gumbel noise is an exact sample of softmax(x/T); rows below the
+ * greedy threshold stay greedy]. rows = batch * n_per_req; row r belongs to request
+ * r / n_per_req as its row n = r % n_per_req. tokens_out[r] = argmax_i (x_ri/T_r + G_ri),
+ * G = -ln(-ln u), u from Philox4x32-10 keyed by seed[b], counter (i >> 2, n,
+ * lo32(offset[b]), hi32(offset[b])), word i & 3, mapped as for the coins. Tokens with
+ * logit -inf never win. temperature: [rows]; seed, offset: [batch]. */
+ts_status ts_gumbel_max_sample(const void* logits, ts_dtype dt, int64_t batch,
+                               int32_t n_per_req, int64_t vocab, int64_t ld,
+                               const float* temperature, const int64_t* seed,
+                               const int64_t* offset, int32_t* tokens_out, void* workspace,
+                               size_t ws_bytes, cudaStream_t stream);
+
+/* Chosen-token logprobs [TS-FI gather_token_logprobs_torch]:
+ * out[r] = log_softmax(x[r, :])[tokens[r]] at temperature 1 (is_probs = 0) or
+ * ln x[r, tokens[r]] (is_probs = 1, fp32 only); a token outside [0, vocab) gives 0.
+ * x: [rows, ld]; tokens: [rows]; out: [rows] fp32. */
+ts_status ts_gather_logprobs(const void* x, ts_dtype dt, int32_t is_probs, int64_t rows,
+                             int64_t vocab, int64_t ld, const int32_t* tokens, float* out,
+                             void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TS_VERIFY_H */

@@ -1,0 +1,341 @@
+// The C ABI of libtsverify.so: argument validation, workspace carve-up, launch geometry
+// and dispatch to the kernels. Host code only; every step of the computation runs in
+// the kernels of ts_stream.cu and ts_staged.cu.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <cuda_runtime.h>
+
+#include "../../include/ts_verify.h"
+#include "ts_internal.h"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+ts_status fail(ts_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+ts_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(TS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool aligned16(const void* p, int64_t ld, int esize) {
+  return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((ld * esize) % 16 == 0);
+}
+
+// Splits of a row so that about 8 CTAs per SM are in flight, each streaming >= min_len.
+void choose_splits(int64_t units, int64_t V, int64_t min_len, int32_t* splits, int64_t* len) {
+  const int64_t target = (int64_t)sm_count() * 8;
+  int64_t s = (target + units - 1) / units;
+  s = s < 1 ? 1 : (s > tsv::kMaxSplits ? tsv::kMaxSplits : s);
+  const int64_t smax = (V + min_len - 1) / min_len;
+  if (s > smax) s = smax < 1 ? 1 : smax;
+  int64_t l = ((V + s - 1) / s + 7) & ~(int64_t)7;
+  *len = l;
+  *splits = (int32_t)((V + l - 1) / l);
+}
+
+ts_status check_common(int64_t rows, int64_t V, int64_t ld) {
+  if (rows < 1) return fail(TS_ERR_INVALID_ARG, "rows/batch must be >= 1 (got %lld)", (long long)rows);
+  if (V < 1 || V > TS_MAX_VOCAB)
+    return fail(TS_ERR_INVALID_ARG, "vocab must be in [1, %d] (got %lld)", TS_MAX_VOCAB, (long long)V);
+  if (ld < V) return fail(TS_ERR_INVALID_ARG, "ld (%lld) must be >= vocab (%lld)", (long long)ld, (long long)V);
+  if (rows > (int64_t)1 << 30) return fail(TS_ERR_INVALID_ARG, "too many rows");
+  return TS_OK;
+}
+
+ts_status check_dtype(int dt) {
+  if (dt != TS_F32 && dt != TS_BF16) return fail(TS_ERR_UNSUPPORTED_DTYPE, "unsupported dtype %d", dt);
+  return TS_OK;
+}
+
+ts_status take_workspace(int64_t batch, int32_t R, void* ws, size_t ws_bytes, tsv::Workspace* out) {
+  const size_t need = tsv::workspace_layout(batch, R, ws, out);
+  if (ws == nullptr) return fail(TS_ERR_INVALID_ARG, "workspace is NULL (need %zu bytes)", need);
+  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0)
+    return fail(TS_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (ws_bytes < need)
+    return fail(TS_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  return TS_OK;
+}
+
+ts_status launched(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  g_msg[0] = 0;
+  return TS_OK;
+}
+
+}  // namespace
+
+namespace tsv {
+
+size_t workspace_layout(int64_t batch, int32_t R, void* base, Workspace* ws) {
+  const size_t rows = (size_t)batch * (size_t)R;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align256(off + bytes);
+    return base ? static_cast<unsigned char*>(base) + at : nullptr;
+  };
+  Workspace w{};
+  w.rowcnt = reinterpret_cast<uint32_t*>(take(rows * 4));
+  w.reqcnt = reinterpret_cast<uint32_t*>(take((size_t)batch * 4));
+  w.part = reinterpret_cast<Part*>(take(rows * kMaxSplits * sizeof(Part)));
+  w.rowres = reinterpret_cast<RowRes*>(take(rows * sizeof(RowRes)));
+  w.dpart = reinterpret_cast<DrawPart*>(take((size_t)batch * kMaxSplits * sizeof(DrawPart)));
+  w.bytes = off;
+  if (ws) *ws = w;
+  return off;
+}
+
+}  // namespace tsv
+
+extern "C" {
+
+size_t ts_workspace_size(int64_t batch, int32_t rows_per_req, int64_t vocab) {
+  (void)vocab;
+  if (batch < 1 || rows_per_req < 1) return 0;
+  return tsv::workspace_layout(batch, rows_per_req, nullptr, nullptr);
+}
+
+ts_status ts_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (!workspace) return fail(TS_ERR_INVALID_ARG, "workspace is NULL");
+  return launched(cudaMemsetAsync(workspace, 0, ws_bytes, stream), "cudaMemsetAsync");
+}
+
+const char* ts_last_error_message(void) { return g_msg; }
+
+ts_status ts_device_error(uint32_t* word_host, int clear) {
+  if (!word_host) return fail(TS_ERR_INVALID_ARG, "word_host is NULL");
+  uint32_t w = 0;
+  cudaError_t e = tsv::staged_read_error(&w, clear);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  *word_host = w;
+  if (w) return fail(TS_ERR_TIMEOUT, "a bounded device wait gave up (word 0x%x)", w);
+  g_msg[0] = 0;
+  return TS_OK;
+}
+
+ts_status ts_softmax_temp(const void* logits, ts_dtype dt, int64_t rows, int64_t vocab,
+                          int64_t ld, const float* temperature, float* probs_out,
+                          cudaStream_t stream) {
+  ts_status st;
+  if ((st = check_dtype(dt)) != TS_OK) return st;
+  if ((st = check_common(rows, vocab, ld)) != TS_OK) return st;
+  if (!logits || !probs_out) return fail(TS_ERR_INVALID_ARG, "logits and probs_out are required");
+  if (vocab > tsv::staged_max_vocab(dt == TS_BF16))
+    return fail(TS_ERR_INVALID_ARG, "vocab %lld above the staged limit %d", (long long)vocab,
+                tsv::staged_max_vocab(dt == TS_BF16));
+  tsv::StagedArgs a{};
+  a.mode = tsv::kSoftmax;
+  a.x = logits;
+  a.bf16 = (dt == TS_BF16);
+  a.ld = ld;
+  a.V = vocab;
+  a.rows = rows;
+  a.R = 1;
+  a.temperature = temperature;
+  a.out = probs_out;
+  const char* why = "launch";
+  return launched(tsv::launch_staged(a, stream, &why), why);
+}
+
+ts_status ts_topk_topp_renorm(const float* probs, int64_t rows, int64_t vocab, int64_t ld,
+                              const int32_t* top_k, const float* top_p, float* probs_out,
+                              cudaStream_t stream) {
+  ts_status st;
+  if ((st = check_common(rows, vocab, ld)) != TS_OK) return st;
+  if (!probs || !probs_out) return fail(TS_ERR_INVALID_ARG, "probs and probs_out are required");
+  if (probs_out == probs && ld != vocab)
+    return fail(TS_ERR_INVALID_ARG, "in-place renorm needs ld == vocab");
+  if (vocab > tsv::staged_max_vocab(0))
+    return fail(TS_ERR_INVALID_ARG, "vocab %lld above the staged limit %d", (long long)vocab,
+                tsv::staged_max_vocab(0));
+  tsv::StagedArgs a{};
+  a.mode = tsv::kRenorm;
+  a.x = probs;
+  a.bf16 = 0;
+  a.ld = ld;
+  a.V = vocab;
+  a.rows = rows;
+  a.R = 1;
+  a.top_k = top_k;
+  a.top_p = top_p;
+  a.out = probs_out;
+  const char* why = "launch";
+  return launched(tsv::launch_staged(a, stream, &why), why);
+}
+
+ts_status ts_verify_chain_greedy(const void* target_logits, ts_dtype dt, int64_t batch,
+                                 int32_t D, int64_t vocab, int64_t ld,
+                                 const int32_t* draft_tokens, int32_t* accepted_tokens,
+                                 int32_t* accept_length, int32_t* accept_index,
+                                 float* logprobs, void* workspace, size_t ws_bytes,
+                                 cudaStream_t stream) {
+  ts_status st;
+  if ((st = check_dtype(dt)) != TS_OK) return st;
+  if (D < 0 || D > TS_MAX_DRAFT) return fail(TS_ERR_INVALID_ARG, "D must be in [0, %d]", TS_MAX_DRAFT);
+  if ((st = check_common(batch, vocab, ld)) != TS_OK) return st;
+  if (!target_logits || !accepted_tokens || !accept_length || (D > 0 && !draft_tokens))
+    return fail(TS_ERR_INVALID_ARG, "target_logits, draft_tokens, accepted_tokens and accept_length are required");
+  tsv::RowStatArgs a{};
+  if ((st = take_workspace(batch, D + 1, workspace, ws_bytes, &a.ws)) != TS_OK) return st;
+  a.x = target_logits;
+  a.ld = ld;
+  a.V = vocab;
+  a.rows = batch * (D + 1);
+  choose_splits(a.rows, vocab, 2048, &a.splits, &a.split_len);
+  a.vec = aligned16(target_logits, ld, dt == TS_BF16 ? 2 : 4);
+  a.want_lse = logprobs != nullptr;
+  a.kind = 0;
+  a.D = D;
+  a.draft_tokens = draft_tokens;
+  a.accepted_tokens = accepted_tokens;
+  a.accept_length = accept_length;
+  a.accept_index = accept_index;
+  a.logprobs = logprobs;
+  return launched(tsv::launch_rowstat(a, dt == TS_BF16, stream), "greedy verify launch");
+}
+
+ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t ws_bytes,
+                                 cudaStream_t stream) {
+  if (!p) return fail(TS_ERR_INVALID_ARG, "args is NULL");
+  ts_status st;
+  if ((st = check_dtype(p->target_dtype)) != TS_OK) return st;
+  if (p->D < 0 || p->D > TS_MAX_DRAFT) return fail(TS_ERR_INVALID_ARG, "D must be in [0, %d]", TS_MAX_DRAFT);
+  if ((st = check_common(p->batch, p->vocab, p->ld)) != TS_OK) return st;
+  if (!p->target || !p->accepted_tokens || !p->accept_length || (p->D > 0 && !p->draft_tokens))
+    return fail(TS_ERR_INVALID_ARG, "target, draft_tokens, accepted_tokens and accept_length are required");
+  if (!p->uniforms && (!p->seed || !p->offset))
+    return fail(TS_ERR_INVALID_ARG, "seed and offset are required when uniforms is NULL");
+  if (p->draft_probs && p->ld_draft < p->vocab)
+    return fail(TS_ERR_INVALID_ARG, "ld_draft must be >= vocab");
+  const int32_t R = p->D + 1;
+  if (!p->target_is_logits) {
+    if (p->target_dtype != TS_F32)
+      return fail(TS_ERR_UNSUPPORTED_DTYPE, "probability targets must be fp32");
+    tsv::DrawArgs a{};
+    if ((st = take_workspace(p->batch, R, workspace, ws_bytes, &a.ws)) != TS_OK) return st;
+    a.p = static_cast<const float*>(p->target);
+    a.ld = p->ld;
+    a.V = p->vocab;
+    a.B = p->batch;
+    a.D = p->D;
+    a.q = p->draft_probs;
+    a.ld_q = p->ld_draft;
+    a.drafts = p->draft_tokens;
+    a.seed = p->seed;
+    a.offset = p->offset;
+    a.uniforms = p->uniforms;
+    choose_splits(p->batch, p->vocab, 4096, &a.splits, &a.split_len);
+    a.vec = aligned16(p->target, p->ld, 4) && (!p->draft_probs || aligned16(p->draft_probs, p->ld_draft, 4));
+    a.accepted_tokens = p->accepted_tokens;
+    a.accept_length = p->accept_length;
+    a.accept_index = p->accept_index;
+    a.logprobs = p->logprobs;
+    return launched(tsv::launch_draw_probs(a, stream), "probability-row chain launch");
+  }
+  if (p->draft_probs)
+    return fail(TS_ERR_INVALID_ARG,
+                "logit targets with explicit draft probabilities are not supported by this build");
+  if (p->vocab > tsv::staged_max_vocab(p->target_dtype == TS_BF16))
+    return fail(TS_ERR_INVALID_ARG, "vocab %lld above the staged limit %d", (long long)p->vocab,
+                tsv::staged_max_vocab(p->target_dtype == TS_BF16));
+  tsv::StagedArgs a{};
+  if ((st = take_workspace(p->batch, R, workspace, ws_bytes, &a.ws)) != TS_OK) return st;
+  a.mode = tsv::kChain;
+  a.x = p->target;
+  a.bf16 = (p->target_dtype == TS_BF16);
+  a.ld = p->ld;
+  a.V = p->vocab;
+  a.rows = p->batch * R;
+  a.R = R;
+  a.D = p->D;
+  a.temperature = p->temperature;
+  a.top_k = p->top_k;
+  a.top_p = p->top_p;
+  a.draft_tokens = p->draft_tokens;
+  a.seed = p->seed;
+  a.offset = p->offset;
+  a.uniforms = p->uniforms;
+  a.accepted_tokens = p->accepted_tokens;
+  a.accept_length = p->accept_length;
+  a.accept_index = p->accept_index;
+  a.logprobs = p->logprobs;
+  const char* why = "target-only chain launch";
+  return launched(tsv::launch_staged(a, stream, &why), why);
+}
+
+ts_status ts_gumbel_max_sample(const void* logits, ts_dtype dt, int64_t batch,
+                               int32_t n_per_req, int64_t vocab, int64_t ld,
+                               const float* temperature, const int64_t* seed,
+                               const int64_t* offset, int32_t* tokens_out, void* workspace,
+                               size_t ws_bytes, cudaStream_t stream) {
+  ts_status st;
+  if ((st = check_dtype(dt)) != TS_OK) return st;
+  if (n_per_req < 1) return fail(TS_ERR_INVALID_ARG, "n_per_req must be >= 1");
+  if ((st = check_common(batch * (int64_t)n_per_req, vocab, ld)) != TS_OK) return st;
+  if (!logits || !temperature || !seed || !offset || !tokens_out)
+    return fail(TS_ERR_INVALID_ARG, "logits, temperature, seed, offset and tokens_out are required");
+  tsv::RowStatArgs a{};
+  if ((st = take_workspace(batch, n_per_req, workspace, ws_bytes, &a.ws)) != TS_OK) return st;
+  a.x = logits;
+  a.ld = ld;
+  a.V = vocab;
+  a.rows = batch * n_per_req;
+  choose_splits(a.rows, vocab, 2048, &a.splits, &a.split_len);
+  a.vec = aligned16(logits, ld, dt == TS_BF16 ? 2 : 4);
+  a.kind = 2;
+  a.temperature = temperature;
+  a.seed = seed;
+  a.offset = offset;
+  a.n_per_req = n_per_req;
+  a.tokens_out = tokens_out;
+  return launched(tsv::launch_rowstat(a, dt == TS_BF16, stream), "Gumbel launch");
+}
+
+ts_status ts_gather_logprobs(const void* x, ts_dtype dt, int32_t is_probs, int64_t rows,
+                             int64_t vocab, int64_t ld, const int32_t* tokens, float* out,
+                             void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  ts_status st;
+  if ((st = check_dtype(dt)) != TS_OK) return st;
+  if ((st = check_common(rows, vocab, ld)) != TS_OK) return st;
+  if (!x || !tokens || !out) return fail(TS_ERR_INVALID_ARG, "x, tokens and out are required");
+  if (is_probs) {
+    if (dt != TS_F32) return fail(TS_ERR_UNSUPPORTED_DTYPE, "probabilities must be fp32");
+    return launched(tsv::launch_logprobs_probs(static_cast<const float*>(x), ld, vocab, rows,
+                                               tokens, out, stream),
+                    "logprobs launch");
+  }
+  tsv::RowStatArgs a{};
+  if ((st = take_workspace(rows, 1, workspace, ws_bytes, &a.ws)) != TS_OK) return st;
+  a.x = x;
+  a.ld = ld;
+  a.V = vocab;
+  a.rows = rows;
+  choose_splits(rows, vocab, 2048, &a.splits, &a.split_len);
+  a.vec = aligned16(x, ld, dt == TS_BF16 ? 2 : 4);
+  a.want_lse = 1;
+  a.kind = 1;
+  a.lp_tokens = tokens;
+  a.lp_out = out;
+  return launched(tsv::launch_rowstat(a, dt == TS_BF16, stream), "logprobs launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,135 @@
+// Internal interface between the C ABI (ts_abi.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace tsv {
+
+constexpr int kMaxSplits = 64;  // row splits of the streaming kernels
+
+// Per-(row, split) partial of the streaming row statistics: argmax (v, i) and the
+// log-sum-exp state s * exp(m) of the raw row.
+struct alignas(16) Part {
+  float v;
+  int32_t i;
+  float m;
+  float s;
+};
+
+// Per-row result handed from the row kernels to the request-level chain writer.
+struct alignas(32) RowRes {
+  float M;       // row maximum (raw logits)
+  int32_t am;    // row argmax
+  float S;       // sum exp(x - M) at temperature 1 (logprobs), or 0
+  int32_t tok;   // drawn token of this row (residual or bonus draw), -1 if none
+  int32_t acc;   // 1 if the draft of this row was accepted
+  int32_t pad[3];
+};
+
+// Per-request partial of the streaming draw: residual mass and base mass.
+struct alignas(8) DrawPart {
+  float w;
+  float b;
+};
+
+// Workspace carve-up for `batch` requests of `R` rows each.
+struct Workspace {
+  uint32_t* rowcnt;   // [rows]
+  uint32_t* reqcnt;   // [batch]
+  Part* part;         // [rows * kMaxSplits]
+  RowRes* rowres;     // [rows]
+  DrawPart* dpart;    // [batch * kMaxSplits]
+  size_t bytes;
+};
+
+size_t workspace_layout(int64_t batch, int32_t R, void* base, Workspace* ws);
+
+// ---- streaming kernels (ts_stream.cu) ------------------------------------------
+
+struct RowStatArgs {
+  const void* x;
+  int64_t ld, V, rows;
+  int32_t splits;
+  int64_t split_len;  // elements per split, a multiple of 8
+  int32_t vec;        // rows are 16-byte aligned
+  int32_t want_lse;
+  int32_t kind;       // 0: greedy verify, 1: gather logprobs (logits), 2: Gumbel-max
+  // Gumbel
+  const float* temperature;
+  const int64_t* seed;
+  const int64_t* offset;
+  int32_t n_per_req;
+  int32_t* tokens_out;
+  // greedy verify
+  int32_t D;
+  const int32_t* draft_tokens;
+  int32_t* accepted_tokens;
+  int32_t* accept_length;
+  int32_t* accept_index;
+  float* logprobs;
+  // gather logprobs
+  const int32_t* lp_tokens;
+  float* lp_out;
+  Workspace ws;
+};
+
+cudaError_t launch_rowstat(const RowStatArgs& a, int bf16, cudaStream_t s);
+
+struct DrawArgs {
+  const float* p;
+  int64_t ld, V, B;
+  int32_t D;
+  const float* q;
+  int64_t ld_q;
+  const int32_t* drafts;
+  const int64_t* seed;
+  const int64_t* offset;
+  const float* uniforms;
+  int32_t splits;
+  int64_t split_len;
+  int32_t vec;
+  int32_t* accepted_tokens;
+  int32_t* accept_length;
+  int32_t* accept_index;
+  float* logprobs;
+  Workspace ws;
+};
+
+cudaError_t launch_draw_probs(const DrawArgs& a, cudaStream_t s);
+
+cudaError_t launch_logprobs_probs(const float* p, int64_t ld, int64_t V, int64_t rows,
+                                  const int32_t* tokens, float* out, cudaStream_t s);
+
+// ---- cluster-staged row kernels (ts_staged.cu) -----------------------------------
+
+enum StagedMode { kSoftmax = 0, kRenorm = 1, kChain = 2 };
+
+struct StagedArgs {
+  int32_t mode;
+  const void* x;
+  int32_t bf16;
+  int64_t ld, V, rows;
+  int32_t R, D;  // chain: rows per request and drafts
+  const float* temperature;  // softmax: per row; chain: per request
+  const int32_t* top_k;      // renorm: per row; chain: per request
+  const float* top_p;
+  float* out;  // softmax / renorm output, [rows, V]
+  // chain (target-only, logits)
+  const int32_t* draft_tokens;
+  const int64_t* seed;
+  const int64_t* offset;
+  const float* uniforms;
+  int32_t* accepted_tokens;
+  int32_t* accept_length;
+  int32_t* accept_index;
+  float* logprobs;
+  Workspace ws;
+};
+
+cudaError_t launch_staged(const StagedArgs& a, cudaStream_t s, const char** why);
+cudaError_t staged_read_error(uint32_t* word, int clear);
+int staged_max_vocab(int bf16);
+
+}  // namespace tsv

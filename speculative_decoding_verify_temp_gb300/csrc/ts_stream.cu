@@ -1,0 +1,570 @@
+// Streaming row kernels: one pass over each needed row, split across CTAs, combined by
+// the last CTA to finish (an atomic arrival counter in the workspace; no waiting).
+//
+//  k_rowstat<E, GUMBEL>  row argmax (lowest id on ties) and the temperature-1 log-sum-exp,
+//                        then per kind: greedy chain verification (TokenSpeed
+//                        flashinfer.py verify(): sampling_argmax + verify_chain_greedy),
+//                        chosen-token logprobs (gather_token_logprobs_torch), or the
+//                        temperature-only Gumbel-max draw (TensorRT-LLM interface.py,
+//                        _sample_sharded_temperature).
+//  k_draw_probs          chain speculative sampling on probability rows (TensorRT-LLM
+//                        interface.py, rejection_sampling_one_model): the accept tests,
+//                        then one streamed pass over the single row that the final
+//                        (residual or bonus) draw needs.
+#include <stdint.h>
+
+#include "ts_common.cuh"
+#include "ts_internal.h"
+
+namespace tsv {
+
+constexpr int kStreamThreads = 256;
+constexpr float kGumbelCap = 17.0f;  // > the largest noise -ln(-ln(1 - 2^-24)) = 16.64
+
+template <typename E>
+struct Vec;
+template <>
+struct Vec<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void unpack(const uint4& r, float* x) {
+    x[0] = __uint_as_float(r.x);
+    x[1] = __uint_as_float(r.y);
+    x[2] = __uint_as_float(r.z);
+    x[3] = __uint_as_float(r.w);
+  }
+  __device__ __forceinline__ static float scalar(const float* p, int64_t i) { return p[i]; }
+};
+template <>
+struct Vec<uint16_t> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void unpack(const uint4& r, float* x) {
+    x[0] = __uint_as_float(r.x << 16);
+    x[1] = __uint_as_float(r.x & 0xFFFF0000u);
+    x[2] = __uint_as_float(r.y << 16);
+    x[3] = __uint_as_float(r.y & 0xFFFF0000u);
+    x[4] = __uint_as_float(r.z << 16);
+    x[5] = __uint_as_float(r.z & 0xFFFF0000u);
+    x[6] = __uint_as_float(r.w << 16);
+    x[7] = __uint_as_float(r.w & 0xFFFF0000u);
+  }
+  __device__ __forceinline__ static float scalar(const uint16_t* p, int64_t i) {
+    return bf16_bits_to_f32(p[i]);
+  }
+};
+
+// Block-wide reduction of (argmax, lse) into thread 0; returns true on thread 0.
+__device__ __forceinline__ void block_reduce_stat(float& bv, int32_t& bi, float& lm, float& ls) {
+  __shared__ float s_v[32], s_m[32], s_s[32];
+  __shared__ int32_t s_i[32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  warp_argmax(bv, bi);
+  warp_lse(lm, ls);
+  if (lane == 0) {
+    s_v[w] = bv;
+    s_i[w] = bi;
+    s_m[w] = lm;
+    s_s[w] = ls;
+  }
+  __syncthreads();
+  if (w == 0) {
+    bv = lane < nw ? s_v[lane] : -INFINITY;
+    bi = lane < nw ? s_i[lane] : INT32_MAX;
+    lm = lane < nw ? s_m[lane] : -INFINITY;
+    ls = lane < nw ? s_s[lane] : 0.f;
+    warp_argmax(bv, bi);
+    warp_lse(lm, ls);
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// Row statistics: argmax + log-sum-exp, or the Gumbel-max argmax.
+
+template <typename E, bool GUMBEL>
+__global__ void __launch_bounds__(kStreamThreads) k_rowstat(RowStatArgs a) {
+  constexpr int N = Vec<E>::N;
+  const int64_t row = blockIdx.x / a.splits;
+  const int split = (int)(blockIdx.x % a.splits);
+  const int64_t lo = (int64_t)split * a.split_len;
+  const int64_t hi = min(a.V, lo + a.split_len);
+  const E* xr = reinterpret_cast<const E*>(a.x) + row * a.ld;
+
+  // Gumbel noise stream of this row
+  bool noise = false;
+  float invT = 1.f;
+  uint32_t k0 = 0, k1 = 0, c1 = 0, c2 = 0, c3 = 0;
+  if (GUMBEL) {
+    const float T = a.temperature[row];
+    noise = (T >= kGreedyT);
+    invT = noise ? __frcp_rn(T) : 1.f;
+    const int64_t b = row / a.n_per_req;
+    const uint64_t seed = (uint64_t)a.seed[b], off = (uint64_t)a.offset[b];
+    k0 = (uint32_t)seed;
+    k1 = (uint32_t)(seed >> 32);
+    c1 = (uint32_t)(row % a.n_per_req);
+    c2 = (uint32_t)off;
+    c3 = (uint32_t)(off >> 32);
+  }
+
+  float bv = -INFINITY;
+  int32_t bi = INT32_MAX;
+  float lm = -INFINITY, ls = 0.f, lc = 0.f;
+  const bool lse = !GUMBEL && a.want_lse;
+
+  // Elements x[0..n) with indices base.. base+n-1, n a multiple of 4 for the vector path.
+  auto visit = [&](const float* x, int n, int64_t base) {
+    if (GUMBEL && noise) {
+      for (int g = 0; g < n; g += 4) {
+        const float gm = fmaxf(fmaxf(x[g], x[g + 1]), fmaxf(x[g + 2], x[g + 3]));
+        if (gm * invT + kGumbelCap >= bv) {
+          const uint32_t gi = (uint32_t)((base + g) >> 2);
+          const uint4 r = philox4x32_10(make_uint4(gi, c1, c2, c3), k0, k1);
+          const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (x[g + k] == -INFINITY) continue;
+            const float e = -logf(u01(wv[k]));
+            const float s = x[g + k] * invT - __logf(e);
+            if (s > bv) {
+              bv = s;
+              bi = (int32_t)(base + g + k);
+            }
+          }
+        }
+      }
+      return;
+    }
+    float vm = x[0];
+    for (int k = 1; k < n; ++k) vm = fmaxf(vm, x[k]);
+    if (vm > bv) {
+      for (int k = 0; k < n; ++k)
+        if (x[k] == vm) {
+          bi = (int32_t)(base + k);
+          break;
+        }
+      bv = vm;
+    }
+    if (lse && vm > -INFINITY) {
+      const float nm = fmaxf(lm, vm);
+      const float f = ex2((lm - nm) * kLog2e);
+      ls *= f;
+      lc *= f;
+      lm = nm;
+      float vs = 0.f;
+      for (int k = 0; k < n; ++k) vs += ex2((x[k] - nm) * kLog2e);
+      kahan_add(ls, lc, vs);
+    }
+  };
+
+  if (a.vec) {
+    const int64_t nv = (hi - lo) / N;
+    const uint4* vp = reinterpret_cast<const uint4*>(xr + lo);
+    int64_t vi = threadIdx.x;
+    constexpr int U = 4;
+    for (; vi + (U - 1) * kStreamThreads < nv; vi += U * kStreamThreads) {
+      uint4 r[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) r[u] = ldg_stream(vp + vi + u * kStreamThreads);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        float x[N];
+        Vec<E>::unpack(r[u], x);
+        visit(x, N, lo + (vi + u * kStreamThreads) * N);
+      }
+    }
+    for (; vi < nv; vi += kStreamThreads) {
+      float x[N];
+      Vec<E>::unpack(ldg_stream(vp + vi), x);
+      visit(x, N, lo + vi * N);
+    }
+    // ragged tail: fewer than N elements, padded with -inf to a multiple of 4
+    const int64_t t0 = lo + nv * N;
+    if (threadIdx.x == 0 && t0 < hi) {
+      float x[8];
+      int n = (int)(hi - t0);
+      for (int k = 0; k < 8; ++k) x[k] = k < n ? Vec<E>::scalar(xr, t0 + k) : -INFINITY;
+      visit(x, (n + 3) & ~3, t0);
+    }
+  } else {
+    for (int64_t g = lo + 4 * (int64_t)threadIdx.x; g < hi; g += 4 * kStreamThreads) {
+      float x[4];
+      for (int k = 0; k < 4; ++k) x[k] = (g + k < hi) ? Vec<E>::scalar(xr, g + k) : -INFINITY;
+      visit(x, 4, g);
+    }
+  }
+  ls += lc;  // fold the compensation in before combining
+
+  block_reduce_stat(bv, bi, lm, ls);
+
+  __shared__ int s_last;
+  if (threadIdx.x == 0) {
+    a.ws.part[row * kMaxSplits + split] = Part{bv, bi, lm, ls};
+    __threadfence();
+    const uint32_t prev = atomicAdd(&a.ws.rowcnt[row], 1u);
+    s_last = (prev == (uint32_t)a.splits - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // Last CTA of the row: combine the splits in order.
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float v = -INFINITY, m = -INFINITY, s = 0.f;
+    int32_t i = INT32_MAX;
+    for (int k = lane; k < a.splits; k += 32) {
+      const Part* pp = &a.ws.part[row * kMaxSplits + k];
+      const float v2 = __ldcg(&pp->v), m2 = __ldcg(&pp->m), s2 = __ldcg(&pp->s);
+      const int32_t i2 = __ldcg(&pp->i);
+      argmax_merge(v, i, v2, i2);
+      lse_merge(m, s, m2, s2);
+    }
+    warp_argmax(v, i);
+    warp_lse(m, s);
+    if (lane == 0) {
+      a.ws.rowcnt[row] = 0;
+      const int32_t am = (i == INT32_MAX) ? 0 : i;
+      if (a.kind == 2) {
+        a.tokens_out[row] = am;
+      } else if (a.kind == 1) {
+        const int32_t t = a.lp_tokens[row];
+        float lp = 0.f;
+        if (t >= 0 && (int64_t)t < a.V) lp = (Vec<E>::scalar(xr, t) - m) - logf(s);
+        a.lp_out[row] = lp;
+      } else {
+        // greedy chain verification: publish the row, the last row of the request writes
+        a.ws.rowres[row] = RowRes{m, am, s, -1, 0, {0, 0, 0}};
+        __threadfence();
+        const int32_t R = a.D + 1;
+        const int64_t b = row / R;
+        const uint32_t prev = atomicAdd(&a.ws.reqcnt[b], 1u);
+        if (prev == (uint32_t)R - 1) {
+          __threadfence();
+          a.ws.reqcnt[b] = 0;
+          int32_t js = a.D;
+          for (int32_t j = 0; j < a.D; ++j) {
+            if (a.draft_tokens[b * a.D + j] != __ldcg(&a.ws.rowres[b * R + j].am)) {
+              js = j;
+              break;
+            }
+          }
+          for (int32_t j = 0; j < R; ++j) {
+            const int64_t rj = b * R + j;
+            int32_t tok = -1;
+            if (j < js) tok = a.draft_tokens[b * a.D + j];
+            else if (j == js) tok = __ldcg(&a.ws.rowres[rj].am);
+            a.accepted_tokens[rj] = tok;
+            if (a.accept_index) a.accept_index[rj] = (j <= js) ? (int32_t)rj : -1;
+            if (a.logprobs) {
+              float lp = 0.f;
+              if (j <= js) {
+                const E* xj = reinterpret_cast<const E*>(a.x) + rj * a.ld;
+                lp = (Vec<E>::scalar(xj, tok) - __ldcg(&a.ws.rowres[rj].M)) -
+                     logf(__ldcg(&a.ws.rowres[rj].S));
+              }
+              a.logprobs[rj] = lp;
+            }
+          }
+          a.accept_length[b] = js + 1;
+        }
+      }
+    }
+  }
+}
+
+cudaError_t launch_rowstat(const RowStatArgs& a, int bf16, cudaStream_t s) {
+  const dim3 grid((unsigned)(a.rows * a.splits));
+  if (a.kind == 2) {
+    if (bf16) k_rowstat<uint16_t, true><<<grid, kStreamThreads, 0, s>>>(a);
+    else k_rowstat<float, true><<<grid, kStreamThreads, 0, s>>>(a);
+  } else {
+    if (bf16) k_rowstat<uint16_t, false><<<grid, kStreamThreads, 0, s>>>(a);
+    else k_rowstat<float, false><<<grid, kStreamThreads, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------
+// Chain speculative sampling on probability rows.
+
+// Inclusive block scan of a float (fixed order: lanes, then warps).
+__device__ __forceinline__ float block_incl_scan(float v, float* s_w, float& total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  if (lane == 31) s_w[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    float t = lane < nw ? s_w[lane] : 0.f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    if (lane < nw) s_w[lane] = t;
+  }
+  __syncthreads();
+  const float excl_w = (w > 0) ? s_w[w - 1] : 0.f;
+  total = s_w[nw - 1];
+  __syncthreads();
+  return v + excl_w;
+}
+
+__global__ void __launch_bounds__(kStreamThreads) k_draw_probs(DrawArgs a) {
+  const int64_t b = blockIdx.x / a.splits;
+  const int split = (int)(blockIdx.x % a.splits);
+  const int32_t R = a.D + 1;
+  __shared__ int32_t s_js, s_x;
+  __shared__ float s_uD;
+
+  // 1. the accept tests (every CTA of the request repeats them: D scalar pairs)
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const uint64_t seed = a.seed ? (uint64_t)a.seed[b] : 0, off = a.offset ? (uint64_t)a.offset[b] : 0;
+    int32_t js = a.D;
+    for (int32_t j0 = 0; j0 < a.D; j0 += 32) {
+      const int32_t j = j0 + lane;
+      bool fail = false;
+      if (j < a.D) {
+        const int32_t x = a.drafts[b * a.D + j];
+        const bool valid = x >= 0 && (int64_t)x < a.V;
+        const float u = a.uniforms ? a.uniforms[b * R + j] : verify_coin(seed, off, (uint32_t)j);
+        const float px = valid ? a.p[(b * R + j) * a.ld + x] : 0.f;
+        if (a.q) {
+          const float qx = valid ? a.q[(b * a.D + j) * a.ld_q + x] : 0.f;
+          fail = !(__fmul_rn(u, qx) < px);
+        } else {
+          fail = !(u < px);
+        }
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, fail);
+      if (m) {
+        js = j0 + __ffs(m) - 1;
+        break;
+      }
+    }
+    if (lane == 0) {
+      s_js = js;
+      s_x = (js < a.D) ? a.drafts[b * a.D + js] : -1;
+      s_uD = a.uniforms ? a.uniforms[b * R + a.D] : verify_coin(seed, off, (uint32_t)a.D);
+    }
+  }
+  __syncthreads();
+  const int32_t js = s_js, x = s_x;
+  const bool resid_q = (js < a.D) && a.q != nullptr;
+  const int64_t r = b * R + js;
+  const float* pr = a.p + r * a.ld;
+  const float* qr = resid_q ? a.q + (b * a.D + js) * a.ld_q : nullptr;
+
+  // w_i: the residual max(p - q, 0) formed in fp32, or p with the draft removed, or p.
+  auto weight = [&](float p, float q, int64_t i) -> float {
+    if (resid_q) {
+      const float d = __fsub_rn(p, q);
+      return d > 0.f ? d : 0.f;
+    }
+    return (i == (int64_t)x) ? 0.f : p;
+  };
+
+  // 2. mass of this split (residual and base)
+  const int64_t lo = (int64_t)split * a.split_len;
+  const int64_t hi = min(a.V, lo + a.split_len);
+  float ws = 0.f, wc = 0.f, bs = 0.f, bc = 0.f;
+  if (a.vec) {
+    const int64_t nv = (hi - lo) / 4;
+    const uint4* pv = reinterpret_cast<const uint4*>(pr + lo);
+    const uint4* qv = resid_q ? reinterpret_cast<const uint4*>(qr + lo) : nullptr;
+    for (int64_t vi = threadIdx.x; vi < nv; vi += kStreamThreads) {
+      float p[4], q[4] = {0.f, 0.f, 0.f, 0.f};
+      Vec<float>::unpack(ldg_stream(pv + vi), p);
+      if (resid_q) Vec<float>::unpack(ldg_stream(qv + vi), q);
+      const int64_t i0 = lo + vi * 4;
+      float w4 = 0.f, b4 = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        w4 += weight(p[k], q[k], i0 + k);
+        b4 += p[k];
+      }
+      kahan_add(ws, wc, w4);
+      kahan_add(bs, bc, b4);
+    }
+    for (int64_t i = lo + nv * 4 + threadIdx.x; i < hi; i += kStreamThreads) {
+      const float p = pr[i], q = resid_q ? qr[i] : 0.f;
+      kahan_add(ws, wc, weight(p, q, i));
+      kahan_add(bs, bc, p);
+    }
+  } else {
+    for (int64_t i = lo + threadIdx.x; i < hi; i += kStreamThreads) {
+      const float p = pr[i], q = resid_q ? qr[i] : 0.f;
+      kahan_add(ws, wc, weight(p, q, i));
+      kahan_add(bs, bc, p);
+    }
+  }
+  ws += wc;
+  bs += bc;
+  __shared__ float s_red[2][32];
+  {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ws += __shfl_xor_sync(0xffffffffu, ws, o);
+      bs += __shfl_xor_sync(0xffffffffu, bs, o);
+    }
+    if (lane == 0) {
+      s_red[0][w] = ws;
+      s_red[1][w] = bs;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float t0 = 0.f, t1 = 0.f;
+      for (int k = 0; k < (int)(blockDim.x >> 5); ++k) {
+        t0 += s_red[0][k];
+        t1 += s_red[1][k];
+      }
+      ws = t0;
+      bs = t1;
+    }
+  }
+
+  __shared__ int s_last;
+  if (threadIdx.x == 0) {
+    a.ws.dpart[b * kMaxSplits + split] = DrawPart{ws, bs};
+    __threadfence();
+    const uint32_t prev = atomicAdd(&a.ws.reqcnt[b], 1u);
+    s_last = (prev == (uint32_t)a.splits - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // 3. last CTA of the request: locate the split, then the token, in token-id order
+  __shared__ int s_split, s_fallback;
+  __shared__ float s_t;
+  if (threadIdx.x == 0) {
+    float Z = 0.f, Zb = 0.f;
+    for (int k = 0; k < a.splits; ++k) {
+      Z += __ldcg(&a.ws.dpart[b * kMaxSplits + k].w);
+      Zb += __ldcg(&a.ws.dpart[b * kMaxSplits + k].b);
+    }
+    const int fb = !(Z > 0.f);  // zero residual: draw from p itself
+    if (fb) Z = Zb;
+    float t = __fmul_rn(s_uD, Z);
+    int sp = -1, last_nz = 0;
+    float acc = 0.f;
+    for (int k = 0; k < a.splits; ++k) {
+      const float pk = fb ? __ldcg(&a.ws.dpart[b * kMaxSplits + k].b)
+                          : __ldcg(&a.ws.dpart[b * kMaxSplits + k].w);
+      if (pk > 0.f) last_nz = k;
+      if (sp < 0 && acc + pk > t) {
+        sp = k;
+        t -= acc;
+      }
+      acc += pk;
+    }
+    if (sp < 0) {  // rounding put t past the total: take the last token with mass
+      sp = last_nz;
+      t = INFINITY;
+    }
+    s_split = sp;
+    s_t = t;
+    s_fallback = fb;
+    a.ws.reqcnt[b] = 0;
+  }
+  __syncthreads();
+  const int fb = s_fallback;
+  const int64_t slo = (int64_t)s_split * a.split_len;
+  const int64_t shi = min(a.V, slo + a.split_len);
+  float t = s_t;
+  __shared__ float s_w[32];
+  __shared__ int32_t s_tok, s_lastnz;
+  if (threadIdx.x == 0) {
+    s_tok = -1;
+    s_lastnz = -1;
+  }
+  __syncthreads();
+  // tiles of 4 consecutive tokens per thread, scanned in order
+  for (int64_t t0 = slo; t0 < shi; t0 += 4 * kStreamThreads) {
+    const int64_t i0 = t0 + 4 * (int64_t)threadIdx.x;
+    float w[4];
+    int32_t my_last = -1;
+    float sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t i = i0 + k;
+      float wk = 0.f;
+      if (i < shi) {
+        const float p = pr[i];
+        wk = fb ? p : weight(p, resid_q ? qr[i] : 0.f, i);
+      }
+      w[k] = wk;
+      sum += wk;
+      if (wk > 0.f) my_last = (int32_t)i;
+    }
+    float total;
+    const float incl = block_incl_scan(sum, s_w, total);
+    const float excl = incl - sum;
+    if (excl <= t && t < incl) {  // exactly one thread: the prefix is nondecreasing
+      float acc = excl;
+      int32_t tok = my_last;
+      for (int k = 0; k < 4; ++k) {
+        if (w[k] > 0.f && acc + w[k] > t) {
+          tok = (int32_t)(i0 + k);
+          break;
+        }
+        acc += w[k];
+      }
+      s_tok = tok;
+    }
+    if (my_last >= 0) atomicMax(&s_lastnz, my_last);
+    __syncthreads();
+    if (s_tok >= 0) break;
+    t -= total;
+    __syncthreads();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int32_t tok = s_tok >= 0 ? s_tok : s_lastnz;
+    if (tok < 0) tok = (x >= 0) ? x : 0;  // no mass anywhere in the split (degenerate input)
+    for (int32_t j = 0; j < R; ++j) {
+      const int64_t rj = b * R + j;
+      int32_t tj = -1;
+      if (j < js) tj = a.drafts[b * a.D + j];
+      else if (j == js) tj = tok;
+      a.accepted_tokens[rj] = tj;
+      if (a.accept_index) a.accept_index[rj] = (j <= js) ? (int32_t)rj : -1;
+      if (a.logprobs) {
+        float lp = 0.f;
+        if (j <= js && tj >= 0 && (int64_t)tj < a.V) lp = logf(a.p[rj * a.ld + tj]);
+        a.logprobs[rj] = lp;
+      }
+    }
+    a.accept_length[b] = js + 1;
+  }
+}
+
+cudaError_t launch_draw_probs(const DrawArgs& a, cudaStream_t s) {
+  const dim3 grid((unsigned)(a.B * a.splits));
+  k_draw_probs<<<grid, kStreamThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------
+// ln p[r, tokens[r]] for probability rows.
+
+__global__ void k_logprobs_probs(const float* p, int64_t ld, int64_t V, int64_t rows,
+                                 const int32_t* tokens, float* out) {
+  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= rows) return;
+  const int32_t t = tokens[r];
+  out[r] = (t >= 0 && (int64_t)t < V) ? logf(p[r * ld + t]) : 0.f;
+}
+
+cudaError_t launch_logprobs_probs(const float* p, int64_t ld, int64_t V, int64_t rows,
+                                  const int32_t* tokens, float* out, cudaStream_t s) {
+  const int th = 256;
+  k_logprobs_probs<<<(unsigned)((rows + th - 1) / th), th, 0, s>>>(p, ld, V, rows, tokens, out);
+  return cudaGetLastError();
+}
+
+}  // namespace tsv

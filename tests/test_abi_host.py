@@ -1,0 +1,89 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads, it
+exports every call the header declares, the workspace size is consistent, and invalid
+arguments are rejected on the host before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ts_verify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verify_temp_gb300 import build, tsverify
+
+    build.build()
+    return tsverify.load()
+
+
+def declared_calls():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ts_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_six_calls():
+    names = declared_calls()
+    for n in ["ts_softmax_temp", "ts_topk_topp_renorm", "ts_verify_chain_greedy",
+              "ts_chain_spec_sampling", "ts_gumbel_max_sample", "ts_gather_logprobs"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(os.path.join(ROOT, "speculative_decoding_verify_temp_gb300",
+                                   "libtsverify.so"))
+    missing = [n for n in declared_calls() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_workspace_size(lib):
+    a = lib.ts_workspace_size(64, 4, 32000)
+    b = lib.ts_workspace_size(128, 4, 32000)
+    assert 0 < a < b
+    assert a % 256 == 0
+    assert lib.ts_workspace_size(0, 4, 100) == 0
+
+
+def _err(lib):
+    return lib.ts_last_error_message().decode()
+
+
+def test_invalid_arguments_are_rejected_before_launch(lib):
+    P = ctypes.c_void_p
+    fake = P(256)  # never dereferenced: validation fails first
+    # vocab = 0
+    st = lib.ts_verify_chain_greedy(fake, 0, 4, 3, 0, 0, fake, fake, fake, None, None, fake,
+                                    1 << 20, None)
+    assert st == 1 and "vocab" in _err(lib)
+    # D out of range
+    st = lib.ts_verify_chain_greedy(fake, 0, 4, 65, 100, 100, fake, fake, fake, None, None,
+                                    fake, 1 << 20, None)
+    assert st == 1 and "D must" in _err(lib)
+    # ld < vocab
+    st = lib.ts_softmax_temp(fake, 0, 4, 100, 99, None, fake, None)
+    assert st == 1 and "ld" in _err(lib)
+    # unknown dtype
+    st = lib.ts_softmax_temp(fake, 7, 4, 100, 100, None, fake, None)
+    assert st == 2
+    # workspace too small
+    st = lib.ts_gumbel_max_sample(fake, 0, 4, 2, 100, 100, fake, fake, fake, fake, P(512), 16,
+                                  None)
+    assert st == 1 and "workspace" in _err(lib)
+    # bf16 probabilities are not accepted
+    st = lib.ts_gather_logprobs(fake, 1, 1, 4, 100, 100, fake, fake, None, 0, None)
+    assert st == 2
+    # chain without coins
+    from speculative_decoding_verify_temp_gb300.tsverify import ChainArgs
+    a = ChainArgs()
+    a.target = 256
+    a.target_dtype = 0
+    a.target_is_logits = 1
+    a.batch, a.D, a.vocab, a.ld = 2, 1, 10, 10
+    a.draft_tokens = 256
+    a.accepted_tokens = 256
+    a.accept_length = 256
+    st = lib.ts_chain_spec_sampling(ctypes.byref(a), P(512), 1 << 20, None)
+    assert st == 1 and "seed" in _err(lib)

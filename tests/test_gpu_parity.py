@@ -1,0 +1,291 @@
+"""GPU parity: every C-ABI call against the oracle on the same seeded inputs.
+
+Sizes span several tiles, clusters of 1 to 8 CTAs and ragged tails; the workloads of
+the benchmark configurations are covered at full size in test_gpu_fullsize.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_verify_temp_gb300 import synth
+from speculative_decoding_verify_temp_gb300 import tsverify as tv
+from tests.gpu_util import TOL, BOUNDARY, compare_chain, dev, dev_logits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    oracle.build()
+    yield
+    assert tv.device_error() == 0
+
+
+def _rand_logits(rng, rows, V, dtype, sigma=3.0, zipf=True):
+    x = rng.standard_normal((rows, V), dtype=np.float32) * np.float32(sigma)
+    if zipf:
+        x += synth.zipf_bias(V)[None, :]
+    if dtype == "bf16":
+        bits = synth.bf16_bits_from_f32(x)
+        return dict(dtype="bf16", logits_bits=bits, logits=synth.f32_from_bf16_bits(bits))
+    return dict(dtype="f32", logits=x)
+
+
+# ---- greedy chain verification ------------------------------------------------------------
+
+@pytest.mark.parametrize("B,D,V,dtype", [(4, 3, 1024, "f32"), (64, 3, 32000, "bf16"),
+                                         (7, 0, 1000, "f32"), (5, 6, 129, "bf16"),
+                                         (3, 2, 7, "f32"), (2, 1, 1, "f32"),
+                                         (16, 4, 50007, "bf16")])
+def test_greedy_verify(B, D, V, dtype):
+    rng = np.random.default_rng(B * 1000 + V)
+    d = _rand_logits(rng, B * (D + 1), V, dtype)
+    am = d["logits"].reshape(B, D + 1, V)[:, :D].argmax(-1)
+    drafts = np.where(rng.random((B, D)) < 0.7, am, rng.integers(0, V, (B, D))).astype(np.int32)
+    g = tv.verify_chain_greedy(dev_logits(d), D, dev(drafts))
+    ref = oracle.verify_chain_greedy(d["logits"], D, drafts)
+    compare_chain(g, ref, dtype)
+
+
+def test_greedy_verify_ties_neginf_and_padded_rows():
+    B, D, V = 6, 3, 300
+    x = np.zeros((B * (D + 1), V), np.float32)
+    x[:, 250:] = -np.inf
+    x[0, [5, 9]] = 3.0  # tie: the lowest id wins
+    x[1, :] = -np.inf  # an all -inf row has argmax 0
+    x[2, 249] = -1.0  # below the zeros: the row argmax stays at id 0
+    drafts = np.array([[9, 0, 0], [0, 0, 0], [0, 1, 2], [3, 3, 3], [0, 0, 0], [1, 1, 1]], np.int32)
+    ld = 320  # padded rows: ld > V, 16-byte aligned
+    xp = np.full((B * (D + 1), ld), 7.0, np.float32)
+    xp[:, :V] = x
+    xt = torch.from_numpy(xp).cuda()[:, :V]
+    g = tv.verify_chain_greedy(xt, D, dev(drafts))
+    ref = oracle.verify_chain_greedy(x, D, drafts)
+    compare_chain(g, ref, "f32")
+    # a row stride that breaks 16-byte alignment takes the scalar path
+    ld2 = 301
+    xq = np.full((B * (D + 1), ld2), 7.0, np.float32)
+    xq[:, :V] = x
+    g = tv.verify_chain_greedy(torch.from_numpy(xq).cuda()[:, :V], D, dev(drafts))
+    compare_chain(g, ref, "f32")
+
+
+# ---- logprobs ------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,V,dtype", [(33, 1000, "f32"), (9, 128256, "bf16"), (5, 3, "f32")])
+def test_gather_logprobs(rows, V, dtype):
+    rng = np.random.default_rng(rows + V)
+    d = _rand_logits(rng, rows, V, dtype)
+    tok = rng.integers(-1, V, rows).astype(np.int32)
+    got = tv.gather_logprobs(dev_logits(d), dev(tok)).cpu().numpy()
+    np.testing.assert_allclose(got, oracle.gather_logprobs(d["logits"], False, tok), **TOL[dtype])
+    p = oracle.softmax_temp(d["logits"]).astype(np.float32)
+    got = tv.gather_logprobs(dev(p), dev(tok), is_probs=True).cpu().numpy()
+    np.testing.assert_allclose(got, oracle.gather_logprobs(p, True, tok), rtol=1e-6, atol=1e-6)
+
+
+# ---- softmax -------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,V,dtype", [(8, 1024, "f32"), (5, 40000, "f32"), (6, 128256, "bf16"),
+                                          (3, 201088, "bf16"), (4, 151936, "f32"), (3, 17, "bf16")])
+def test_softmax_temp(rows, V, dtype):
+    rng = np.random.default_rng(rows * 7 + V)
+    d = _rand_logits(rng, rows, V, dtype)
+    T = rng.uniform(0.3, 1.5, rows).astype(np.float32)
+    T[0] = 0.0  # greedy row
+    got = tv.softmax_temp(dev_logits(d), dev(T)).cpu().numpy()
+    ref = oracle.softmax_temp(d["logits"], T)
+    np.testing.assert_allclose(got, ref, **TOL[dtype])
+    np.testing.assert_allclose(got.sum(-1), 1.0, rtol=1e-5)
+
+
+# ---- top-k / top-p renorm --------------------------------------------------------------------
+
+def _check_renorm(got, ref, marg, probs):
+    ok = marg > BOUNDARY
+    assert (~ok).sum() <= max(1, len(ok) // 50)
+    np.testing.assert_array_equal(got[ok] > 0, ref[ok] > 0)
+    np.testing.assert_allclose(got[ok], ref[ok], rtol=1e-5, atol=1e-6)
+
+
+@pytest.mark.parametrize("rows,V", [(24, 1000), (12, 32000), (8, 151936), (10, 5)])
+def test_topk_topp_renorm(rows, V):
+    rng = np.random.default_rng(rows + 3 * V)
+    d = _rand_logits(rng, rows, V, "f32", sigma=2.5)
+    T = rng.uniform(0.5, 1.2, rows).astype(np.float32)
+    p = oracle.softmax_temp(d["logits"], T).astype(np.float32)
+    k = rng.choice(np.array([0, 1, 20, 50, 1000, V, -3], np.int32), rows).astype(np.int32)
+    tp = rng.choice(np.array([1.0, 0.95, 0.9, 0.5, 0.0], np.float32), rows).astype(np.float32)
+    got = tv.topk_topp_renorm(dev(p), dev(k), dev(tp)).cpu().numpy()
+    ref, marg = oracle.topk_topp_renorm(p, k, tp)
+    _check_renorm(got, ref, marg, p)
+    # knobs absent: pure renormalisation
+    got = tv.topk_topp_renorm(dev(p)).cpu().numpy()
+    ref, marg = oracle.topk_topp_renorm(p)
+    np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-6)
+
+
+def test_renorm_ties_exact_k():
+    # many equal probabilities around the k-th: exactly k survive, lowest ids first
+    V = 4096
+    p = np.full((3, V), 1.0 / V, np.float32)
+    p[1, ::3] = 2.0 / V
+    p[2, 100:200] = 5.0 / V
+    p /= p.sum(-1, keepdims=True)
+    k = np.array([10, 700, 150], np.int32)
+    got = tv.topk_topp_renorm(dev(p), dev(k)).cpu().numpy()
+    ref, _ = oracle.topk_topp_renorm(p, k)
+    np.testing.assert_array_equal(got > 0, ref > 0)
+    assert ((got > 0).sum(-1) == k).all()
+    np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-7)
+
+
+def test_renorm_in_place():
+    rng = np.random.default_rng(9)
+    p = oracle.softmax_temp(rng.standard_normal((4, 3000)).astype(np.float32)).astype(np.float32)
+    t = dev(p)
+    k = dev(np.array([5, 0, 100, 3000], np.int32))
+    tv.topk_topp_renorm(t, k, None, out=t)
+    ref, _ = oracle.topk_topp_renorm(p, np.array([5, 0, 100, 3000], np.int32))
+    np.testing.assert_allclose(t.cpu().numpy(), ref, rtol=1e-5, atol=1e-7)
+
+
+# ---- chain speculative sampling: probability rows ----------------------------------------------
+
+def test_rejection_tiny_config():
+    d = synth.tiny_verify()
+    B, D, V = d["B"], d["D"], d["V"]
+    p = oracle.softmax_temp(d["logits"]).astype(np.float32)
+    g = tv.chain_spec_sampling(dev(p), False, D, dev(d["draft_tokens"]),
+                               draft_probs=dev(d["draft_probs"]), seed=dev(d["seed"]),
+                               offset=dev(d["offset"]))
+    ref = oracle.chain_spec_sampling(p, False, D, d["draft_tokens"], draft_probs=d["draft_probs"],
+                                     seed=d["seed"], offset=d["offset"])
+    compare_chain(g, ref, "f32")
+
+
+@pytest.mark.parametrize("B,D,V,with_q", [(64, 3, 5000, True), (40, 7, 30011, True),
+                                          (50, 4, 2048, False), (16, 1, 3, True),
+                                          (8, 0, 100, False)])
+def test_rejection_probs(B, D, V, with_q):
+    rng = np.random.default_rng(B + D + V)
+    R = D + 1
+    tl = rng.standard_normal((B * R, V)).astype(np.float32) * 2.5
+    p = oracle.softmax_temp(tl).astype(np.float32)
+    q = oracle.softmax_temp(tl.reshape(B, R, V)[:, :D].reshape(B * D, V)
+                            + rng.standard_normal((B * D, V)).astype(np.float32) * 0.7)
+    q = q.astype(np.float32).reshape(B, D, V)
+    src = q if with_q else p.reshape(B, R, V)[:, :D]
+    drafts = np.array([[rng.choice(V, p=src[b, j].astype(np.float64) / src[b, j].sum())
+                        for j in range(D)] for b in range(B)], np.int32).reshape(B, D)
+    seed = synth.request_seeds(B)
+    off = np.arange(B, dtype=np.int64) * 3
+    kw = dict(draft_probs=dev(q) if with_q else None, seed=dev(seed), offset=dev(off))
+    g = tv.chain_spec_sampling(dev(p), False, D, dev(drafts), **kw)
+    ref = oracle.chain_spec_sampling(p, False, D, drafts, draft_probs=q if with_q else None,
+                                     seed=seed, offset=off)
+    compare_chain(g, ref, "f32")
+    # explicit uniforms replace Philox
+    uni = rng.uniform(0.0, 1.0, (B, R)).astype(np.float32)
+    uni = np.clip(uni, 1e-7, 1 - 1e-7).astype(np.float32)
+    g = tv.chain_spec_sampling(dev(p), False, D, dev(drafts), draft_probs=kw["draft_probs"],
+                               uniforms=dev(uni))
+    ref = oracle.chain_spec_sampling(p, False, D, drafts, draft_probs=q if with_q else None,
+                                     uniforms=uni)
+    compare_chain(g, ref, "f32")
+
+
+# ---- chain speculative sampling: target-only from logits ----------------------------------------
+
+@pytest.mark.parametrize("B,D,V,dtype", [(4, 3, 1024, "f32"), (48, 4, 32000, "bf16"),
+                                         (12, 4, 128256, "bf16"), (6, 3, 201088, "bf16"),
+                                         (10, 2, 40000, "f32"), (9, 0, 3000, "f32")])
+def test_target_only_from_logits(B, D, V, dtype):
+    rng = np.random.default_rng(B * 31 + V)
+    R = D + 1
+    d = _rand_logits(rng, B * R, V, dtype)
+    T = rng.uniform(0.3, 1.5, B).astype(np.float32)
+    T[rng.random(B) < 0.2] = 0.0
+    k = rng.choice(np.array(synth.TOPK_CHOICES, np.int32), B).astype(np.int32)
+    tp = rng.choice(np.array(synth.TOPP_CHOICES, np.float32), B).astype(np.float32)
+    lg = d["logits"].reshape(B, R, V)[:, :D]
+    am = lg.argmax(-1)
+    drafts = np.where(rng.random((B, D)) < 0.6, am, rng.integers(0, V, (B, D))).astype(np.int32)
+    seed = synth.request_seeds(B)
+    off = np.arange(B, dtype=np.int64)
+    g = tv.chain_spec_sampling(dev_logits(d), True, D, dev(drafts), temperature=dev(T),
+                               top_k=dev(k), top_p=dev(tp), seed=dev(seed), offset=dev(off))
+    ref = oracle.chain_spec_sampling(d["logits"], True, D, drafts, temperature=T, top_k=k,
+                                     top_p=tp, seed=seed, offset=off)
+    compare_chain(g, ref, dtype, max_boundary_frac=0.05)
+
+
+def test_target_only_explicit_uniforms_and_knobs_off():
+    rng = np.random.default_rng(77)
+    B, D, V = 40, 3, 5000
+    R = D + 1
+    d = _rand_logits(rng, B * R, V, "f32", sigma=1.0, zipf=False)
+    drafts = rng.integers(0, V, (B, D)).astype(np.int32)
+    uni = rng.uniform(0.001, 0.999, (B, R)).astype(np.float32)
+    g = tv.chain_spec_sampling(dev_logits(d), True, D, dev(drafts), uniforms=dev(uni))
+    ref = oracle.chain_spec_sampling(d["logits"], True, D, drafts, uniforms=uni)
+    compare_chain(g, ref, "f32")
+
+
+def test_determinism_bitwise():
+    rng = np.random.default_rng(5)
+    B, D, V = 32, 4, 128256
+    d = _rand_logits(rng, B * (D + 1), V, "bf16")
+    T = rng.uniform(0.5, 1.2, B).astype(np.float32)
+    k = rng.choice(np.array(synth.TOPK_CHOICES, np.int32), B).astype(np.int32)
+    tp = rng.choice(np.array(synth.TOPP_CHOICES, np.float32), B).astype(np.float32)
+    drafts = rng.integers(0, V, (B, D)).astype(np.int32)
+    args = (dev_logits(d), True, D, dev(drafts))
+    kw = dict(temperature=dev(T), top_k=dev(k), top_p=dev(tp),
+              seed=dev(synth.request_seeds(B)), offset=dev(np.arange(B)))
+    a = tv.chain_spec_sampling(*args, **kw)
+    b = tv.chain_spec_sampling(*args, **kw)
+    for key in ("accepted_tokens", "accept_length", "logprobs"):
+        assert torch.equal(a[key], b[key])
+
+
+# ---- Gumbel-max ------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,N,V,dtype", [(4, 4, 1024, "f32"), (16, 4, 32000, "bf16"),
+                                         (2, 4, 201088, "bf16"), (3, 2, 13, "f32")])
+def test_gumbel(B, N, V, dtype):
+    rng = np.random.default_rng(B + N + V)
+    d = _rand_logits(rng, B * N, V, dtype)
+    if V > 100:
+        d["logits"][:, V - 50:] = -np.inf
+        if dtype == "bf16":
+            d["logits_bits"][:, V - 50:] = 0xFF80
+    T = np.repeat(rng.uniform(0.3, 1.5, B), N).astype(np.float32)
+    T[:N] = 0.0
+    seed = synth.request_seeds(B)
+    off = np.arange(B, dtype=np.int64)
+    got = tv.gumbel_max_sample(dev_logits(d), N, dev(T), dev(seed), dev(off)).cpu().numpy()
+    ref, marg = oracle.gumbel_max_sample(d["logits"], N, T, seed, off)
+    ok = marg > BOUNDARY
+    assert (~ok).sum() <= 1
+    np.testing.assert_array_equal(got[ok], ref[ok])
+    assert (got < V - 50).all() or V <= 100
+
+
+# ---- argument validation through the ABI (no launch) --------------------------------------------
+
+def test_invalid_arguments_raise():
+    x = torch.zeros((4, 10), device="cuda")
+    with pytest.raises(tv.TsError):
+        tv.verify_chain_greedy(x, 65, torch.zeros((1, 65), dtype=torch.int32, device="cuda"))
+    with pytest.raises(tv.TsError):
+        tv.chain_spec_sampling(x, True, 1, torch.zeros((2, 1), dtype=torch.int32, device="cuda"))
+    with pytest.raises(tv.TsError):
+        tv.gather_logprobs(x.to(torch.bfloat16), torch.zeros(4, dtype=torch.int32, device="cuda"),
+                           is_probs=True)
