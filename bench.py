@@ -1,0 +1,465 @@
+#!/usr/bin/env python
+"""Benchmark of the verify-and-sample step on GB300.
+
+Default workload (the largest verify step): 512 requests x (D+1 = 4) target rows over a
+201088-token vocabulary (200019 real ids, -inf pads), bf16 logits ~ N(0, 3^2) + Zipf(1.1)
+bias, per-request temperature ~ U[0.3, 1.5] with 25% greedy requests, top_k in
+{0, 20, 50, 1000}, top_p in {1.0, 0.95, 0.9}, drafts drawn from the target row w.p. 0.6.
+One step = one ts_chain_spec_sampling call (target-only, from logits): softmax with
+temperature, fused top-k/top-p renorm, accept tests, chain scan and the corrected/bonus
+draw, for every row, in one launch. Inputs (824 MB) exceed the 129 MB L2, so no flush.
+
+Metric: verified rows/s = batch*(D+1) / step time (whole job over all GPUs), plus the
+achieved HBM bandwidth of the step (logit bytes read once) against the measured peak.
+Extra "legs" time the other calls on their workloads.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-legs]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified rows/sec (batch×(D+1)) and achieved HBM GB/s vs 8 TB/s peak"
+WORKLOAD = "verify step: target-only chain sampling from bf16 logits, B=512, D=3, V=201088"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-legs", action="store_true")
+    ap.add_argument("--cpu-sample", type=int, default=48, help="requests in the CPU baseline sample")
+    ap.add_argument("--batch", type=int, default=512,
+                    help="requests per step (512 = the benchmark workload; smaller for profiling)")
+    return ap.parse_args()
+
+
+# ---- distributed plumbing (replicas: no data-path collective) ---------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+
+    rank, local, world = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, local, world
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x over all ranks (the job is as slow as its slowest rank)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- measurement helpers ----------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch recorded from an ncu capture of this kernel and workload."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(f"{kernel}|{workload}")
+        return None if e is None else float(e["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[2]) or 0.0) for r in rows)}
+
+
+def time_device(fn, steps: int, warmup: int, device):
+    """Mean device time of one fn() call over `steps` timed calls (CUDA events on the
+    launching stream, barrier + synchronize on both sides, max over ranks)."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        fn()
+    e1.record(s)
+    torch.cuda.synchronize()
+    barrier()
+    ms = e0.elapsed_time(e1) / steps
+    return max_over_ranks(ms, device)
+
+
+# ---- the workload -----------------------------------------------------------------------
+
+def main_workload(batch: int = 512):
+    from speculative_decoding_verify_temp_gb300 import synth
+
+    return synth.verify_step(B=batch, D=3, V=201088, real_vocab=200019)
+
+
+def cpu_baseline(d, nreq: int):
+    """The oracle, as it stands, on the first nreq requests of the workload (1 core)."""
+    import oracle
+    from speculative_decoding_verify_temp_gb300 import synth
+
+    oracle.build()
+    B, D, V = d["B"], d["D"], d["V"]
+    R = D + 1
+    nreq = min(nreq, B)
+    x = synth.f32_from_bf16_bits(d["logits_bits"][: nreq * R])
+    t0 = time.perf_counter()
+    oracle.chain_spec_sampling(x, True, D, d["draft_tokens"][:nreq],
+                               temperature=d["temperature"][:nreq], top_k=d["top_k"][:nreq],
+                               top_p=d["top_p"][:nreq], seed=d["seed"][:nreq],
+                               offset=d["offset"][:nreq], logprobs=False)
+    dt = time.perf_counter() - t0
+    return {"value": nreq * R / dt, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {nreq} requests ({nreq * R} rows) of the workload, "
+                      f"{dt:.1f} s single-threaded C"}
+
+
+def run_reference(args):
+    """The oracle timed on the host cores: each step is a bounded sample of the workload."""
+    rank, _, world = dist_env()
+    if world > 1 and rank != 0:
+        return
+    import oracle
+    from speculative_decoding_verify_temp_gb300 import synth
+
+    oracle.build()
+    d = main_workload(args.batch)
+    D = d["D"]
+    R = D + 1
+    nreq = 8
+    x = synth.f32_from_bf16_bits(d["logits_bits"][: nreq * R])
+    kw = dict(temperature=d["temperature"][:nreq], top_k=d["top_k"][:nreq],
+              top_p=d["top_p"][:nreq], seed=d["seed"][:nreq], offset=d["offset"][:nreq],
+              logprobs=False)
+
+    def step():
+        oracle.chain_spec_sampling(x, True, D, d["draft_tokens"][:nreq], **kw)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    v = nreq * R / dt
+    sample = f"{nreq} requests ({nreq * R} rows) of the workload per step, single-threaded C"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "rows/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": d["B"], "D": D, "vocab": d["V"],
+                   "logits": "bf16", "sample_requests": nreq},
+        "cpu_baseline": {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_ours(args):
+    import torch
+
+    rank, local, world = dist_init("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import __graft_entry__
+    from speculative_decoding_verify_temp_gb300 import synth
+    from speculative_decoding_verify_temp_gb300 import tsverify as tv
+
+    __graft_entry__.build() if rank == 0 else None
+    barrier()
+    tv.load()
+    peak, peak_kind = measured_peaks()
+
+    d = main_workload(args.batch)
+    B, D, V = d["B"], d["D"], d["V"]
+    R = D + 1
+    rows = B * R
+    bits = np.ascontiguousarray(d["logits_bits"]).view(np.int16)
+    logits = torch.from_numpy(bits).to(device).view(torch.bfloat16)
+    drafts = torch.from_numpy(d["draft_tokens"]).to(device)
+    T = torch.from_numpy(d["temperature"]).to(device)
+    K = torch.from_numpy(d["top_k"]).to(device)
+    P = torch.from_numpy(d["top_p"]).to(device)
+    seed = torch.from_numpy(d["seed"]).to(device)
+    off = torch.from_numpy(d["offset"]).to(device)
+    ws = tv.make_workspace(B, R, V, device)
+    outs = tv._chain_outputs(B, R, device, False, False)
+    kw = dict(temperature=T, top_k=K, top_p=P, seed=seed, offset=off, workspace=ws, outputs=outs)
+
+    def step():
+        tv.chain_spec_sampling(logits, True, D, drafts, **kw)
+
+    alg_bytes = rows * V * 2  # the logits, read once
+    with ClockSampler(local) as clk:
+        ms = time_device(step, args.steps, args.warmup, device)
+    clocks = clk.summary()
+    value = world * rows / (ms / 1e3)
+    achieved = alg_bytes / (ms / 1e3) / 1e9
+
+    # end to end through the public API with host buffers
+    pin_logits = torch.from_numpy(bits).pin_memory()
+    pin_small = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+                 for a in (d["draft_tokens"], d["temperature"], d["top_k"], d["top_p"],
+                           d["seed"], d["offset"])]
+    dev_small = [drafts, T, K, P, seed, off]
+    host_acc = torch.empty((B, R), dtype=torch.int32).pin_memory()
+    host_len = torch.empty((B,), dtype=torch.int32).pin_memory()
+    h2d = pin_logits.numel() * 2 + sum(t.numel() * t.element_size() for t in pin_small)
+    d2h = host_acc.numel() * 4 + host_len.numel() * 4
+
+    def e2e_step():
+        logits.view(torch.int16).copy_(pin_logits, non_blocking=True)
+        for dst, src in zip(dev_small, pin_small):
+            dst.copy_(src, non_blocking=True)
+        r = tv.chain_spec_sampling(logits, True, D, drafts, **kw)
+        host_acc.copy_(r["accepted_tokens"], non_blocking=True)
+        host_len.copy_(r["accept_length"], non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    ms_e2e = time_device(e2e_step, e2e_steps, 2, device)
+    e2e = {"value": world * rows / (ms_e2e / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
+
+    legs = {}
+    if not args.no_legs:
+        legs = run_legs(args, d, logits, device, tv, synth, peak)
+
+    if rank != 0:
+        return
+    cpu = cpu_baseline(d, args.cpu_sample)
+    traffic = ncu_traffic("k_staged", "verify_step")
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD if B == 512 else WORKLOAD.replace("B=512", f"B={B}"),
+                   "batch": B, "D": D, "vocab": V, "real_vocab": 200019,
+                   "logits": "bf16", "greedy_requests": 0.25,
+                   "top_k": "uniform {0,20,50,1000}", "top_p": "uniform {1.0,0.95,0.9}",
+                   "temperature": "U[0.3,1.5]",
+                   "l2": f"inputs {alg_bytes / 1e6:.0f} MB vs 129 MB L2 (no flush)",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_gbs": achieved, "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": traffic, "kernel": "k_staged<bf16> (one launch per step)",
+                     "algorithmic_bytes_per_launch": alg_bytes},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "legs": legs,
+    }
+    print(json.dumps(line))
+
+
+def run_legs(args, d, logits, device, tv, synth, peak):
+    """The other calls, each on its own workload (mean device time per call)."""
+    import torch
+
+    legs = {}
+    steps, warm = max(5, args.steps), 3
+    B, D, V = d["B"], d["D"], d["V"]
+    R = D + 1
+    rows = B * R
+
+    def rec(name, ms, nrows, nbytes, launches=1):
+        legs[name] = {"ms": ms, "rows_per_s": nrows / (ms / 1e3),
+                      "hbm_gbs": nbytes / (ms / 1e3) / 1e9,
+                      "frac_of_peak": nbytes / (ms / 1e3) / 1e9 / peak, "launches": launches}
+
+    # greedy chain verification on the same logits (the greedy gate)
+    drafts = torch.from_numpy(d["draft_tokens"]).to(device)
+    ws = tv.make_workspace(B, R, V, device)
+    outs = tv._chain_outputs(B, R, device, False, False)
+    ms = time_device(lambda: tv.verify_chain_greedy(logits, D, drafts, ws, outputs=outs),
+                     steps, warm, device)
+    rec("greedy_verify_B512_D3_V201088_bf16", ms, rows, rows * V * 2)
+    # Gumbel-max on the same logits as 512 requests x 4 rows, greedy rows included
+    Trow = torch.from_numpy(np.repeat(d["temperature"], R)).to(device)
+    seed = torch.from_numpy(d["seed"]).to(device)
+    off = torch.from_numpy(d["offset"]).to(device)
+    wsg = tv.make_workspace(B, R, V, device)
+    tok = torch.empty(rows, dtype=torch.int32, device=device)
+    ms = time_device(lambda: tv.gumbel_max_sample(logits, R, Trow, seed, off, wsg, out=tok),
+                     steps, warm, device)
+    rec("gumbel_B512_N4_V201088_bf16", ms, rows, rows * V * 2)
+    # softmax with temperature, fp32 probabilities out
+    out = torch.empty((rows, V), dtype=torch.float32, device=device)
+    ms = time_device(lambda: tv.softmax_temp(logits, Trow, out=out), steps, warm, device)
+    rec("softmax_B512_R4_V201088_bf16", ms, rows, rows * V * 6)
+    del out
+    # greedy verification, small batch (latency-bound)
+    g = synth.greedy_verify()
+    gl = torch.from_numpy(np.ascontiguousarray(g["logits_bits"]).view(np.int16)).to(device).view(
+        torch.bfloat16)
+    gd = torch.from_numpy(g["draft_tokens"]).to(device)
+    gws = tv.make_workspace(g["B"], g["D"] + 1, g["V"], device)
+    gouts = tv._chain_outputs(g["B"], g["D"] + 1, device, False, False)
+    ms = time_device(lambda: tv.verify_chain_greedy(gl, g["D"], gd, gws, outputs=gouts),
+                     max(50, steps), 10, device)
+    grows = g["B"] * (g["D"] + 1)
+    rec("greedy_verify_B64_D3_V32000_bf16", ms, grows, grows * g["V"] * 2)
+    # target-only chain sampling, B=128 D=4 V=128256
+    c = synth.target_only()
+    cl = torch.from_numpy(np.ascontiguousarray(c["logits_bits"]).view(np.int16)).to(device).view(
+        torch.bfloat16)
+    ca = dict(temperature=torch.from_numpy(c["temperature"]).to(device),
+              top_k=torch.from_numpy(c["top_k"]).to(device),
+              top_p=torch.from_numpy(c["top_p"]).to(device),
+              seed=torch.from_numpy(c["seed"]).to(device),
+              offset=torch.from_numpy(c["offset"]).to(device),
+              workspace=tv.make_workspace(c["B"], c["D"] + 1, c["V"], device),
+              outputs=tv._chain_outputs(c["B"], c["D"] + 1, device, False, False))
+    cd = torch.from_numpy(c["draft_tokens"]).to(device)
+    ms = time_device(lambda: tv.chain_spec_sampling(cl, True, c["D"], cd, **ca), steps, warm, device)
+    crows = c["B"] * (c["D"] + 1)
+    rec("target_only_B128_D4_V128256_bf16", ms, crows, crows * c["V"] * 2)
+    del cl
+    # rejection sampling with draft probabilities, B=256 D=7 V=151936 (fp32 probs)
+    r = synth.rejection()
+    rp = torch.from_numpy(r["target_probs"]).to(device)
+    rq = torch.from_numpy(r["draft_probs"]).to(device)
+    ra = dict(draft_probs=rq, seed=torch.from_numpy(r["seed"]).to(device),
+              offset=torch.from_numpy(r["offset"]).to(device),
+              workspace=tv.make_workspace(r["B"], r["D"] + 1, r["V"], device),
+              outputs=tv._chain_outputs(r["B"], r["D"] + 1, device, False, True))
+    rd = torch.from_numpy(r["draft_tokens"]).to(device)
+    res = tv.chain_spec_sampling(rp, False, r["D"], rd, **ra)
+    alen = res["accept_length"].cpu().numpy()
+    rrows = r["B"] * (r["D"] + 1)
+    # algorithmic bytes: the row the draw needs (p, plus q for a rejection) and the
+    # accepted-prefix scalars
+    need = sum((2 if L <= r["D"] else 1) for L in alen) * r["V"] * 4
+    ms = time_device(lambda: tv.chain_spec_sampling(rp, False, r["D"], rd, **ra), steps, warm,
+                     device)
+    rec("rejection_B256_D7_V151936_f32", ms, rrows, need)
+    # top-k/top-p renorm of the same probabilities with the target-only knob mix
+    rng = np.random.default_rng(1)
+    kk = torch.from_numpy(rng.choice(np.array(synth.TOPK_CHOICES, np.int32), rrows)).to(device)
+    pp = torch.from_numpy(rng.choice(np.array(synth.TOPP_CHOICES, np.float32), rrows)).to(device)
+    ro = torch.empty_like(rp)
+    ms = time_device(lambda: tv.topk_topp_renorm(rp, kk, pp, out=ro), steps, warm, device)
+    rec("renorm_R2048_V151936_f32", ms, rrows, rrows * r["V"] * 8)
+    return legs
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

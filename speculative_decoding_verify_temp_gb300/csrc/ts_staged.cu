@@ -430,6 +430,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
         },
         [](float) { return (uint64_t)1; }, bf16 ? shk_h : shk_f, bf16 ? 5 : 7, (uint64_t)k, -1.f);
   }
+  // The k-th key was selected among the elements that pass the thread-maxima bound, and an
+  // early exit leaves the low digits of KK open: top-k membership needs both tests.
+  auto keptk = [&](uint64_t key) -> bool {
+    return !tk || (selected(KT, key) && selected(KK, key));
+  };
   // ---- 5. top-p on the top-k survivors ----------------------------------------------------
   RadixOut PP{0, 0, 0, 1};
   if (tpa) {
@@ -437,13 +442,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
         ctl, cluster, CL,
         [&](auto&& f) {
           slice_sweep([&](uint64_t key, float v) {
-            if (!tk || selected(KK, key)) f(binkey(v) | key, v);
+            if (keptk(key)) f(binkey(v) | key, v);
           });
         },
         wfn, bf16 ? shp_h : shp_f, bf16 ? 6 : 8, 0, tp);
   }
   auto kept = [&](uint64_t key, float v) -> bool {
-    if (tk && !selected(KK, key)) return false;
+    if (!keptk(key)) return false;
     if (tpa && !selected(PP, binkey(v) | key)) return false;
     return true;
   };

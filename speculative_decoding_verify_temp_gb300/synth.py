@@ -31,11 +31,10 @@ MASK64 = (1 << 64) - 1
 
 def bf16_bits_from_f32(x: np.ndarray) -> np.ndarray:
     """Round float32 to bfloat16 (nearest, ties to even); returns the uint16 bits."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    bits = rounded.astype(np.uint16)
-    # Infinities survive the rounding above; no NaNs are ever generated here.
-    return bits
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    # finite values and infinities stay below 0xFFFF8000, so the sum cannot wrap
+    rounded = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
+    return rounded.astype(np.uint16)
 
 
 def f32_from_bf16_bits(b: np.ndarray) -> np.ndarray:

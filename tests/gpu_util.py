@@ -20,17 +20,19 @@ def dev(a):
     return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def compare_chain(gpu: dict, ref: dict, dtype: str = "f32", max_boundary_frac: float = 0.01,
+def compare_chain(gpu: dict, ref: dict, dtype: str = "f32", max_boundary_frac: float = 0.05,
                   check_logprobs: bool = True):
     """Exact token/length/index parity on every request the oracle does not flag as a
     boundary case; logprobs within tolerance on the emitted positions. Returns the
-    number of boundary requests."""
+    number of boundary requests. A draw over a flat distribution of V tokens lands
+    within 1e-6 of a CDF edge with probability about 2e-6 * V, so the bound on the
+    count of boundary requests is a sanity bound, not part of the parity rule."""
     acc = gpu["accepted_tokens"].cpu().numpy()
     alen = gpu["accept_length"].cpu().numpy()
     margin = ref.get("margin")
     ok = np.ones(len(alen), bool) if margin is None else (margin > BOUNDARY)
     nb = int((~ok).sum())
-    assert nb <= max(1, int(max_boundary_frac * len(alen))), f"{nb} boundary requests"
+    assert nb <= max(3, int(max_boundary_frac * len(alen))), f"{nb} boundary requests"
     np.testing.assert_array_equal(alen[ok], ref["accept_length"][ok])
     np.testing.assert_array_equal(acc[ok], ref["accepted_tokens"][ok])
     # invariants hold everywhere, boundary cases included

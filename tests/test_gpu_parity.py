@@ -146,6 +146,19 @@ def test_renorm_ties_exact_k():
     np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-7)
 
 
+@pytest.mark.parametrize("V", [3000, 40000, 151936])
+def test_topk_only_flat_rows(V):
+    # top-k without top-p on flat rows: the k-th key is found among the elements that pass
+    # the thread-maxima bound, so membership must apply that bound too
+    rng = np.random.default_rng(V)
+    p = oracle.softmax_temp(rng.standard_normal((6, V)).astype(np.float32)).astype(np.float32)
+    k = np.array([1, 5, 17, 100, 1000, 4000], np.int32)
+    got = tv.topk_topp_renorm(dev(p), dev(k)).cpu().numpy()
+    ref, _ = oracle.topk_topp_renorm(p, k)
+    np.testing.assert_array_equal(got > 0, ref > 0)
+    np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-7)
+
+
 def test_renorm_in_place():
     rng = np.random.default_rng(9)
     p = oracle.softmax_temp(rng.standard_normal((4, 3000)).astype(np.float32)).astype(np.float32)
@@ -182,7 +195,8 @@ def test_rejection_probs(B, D, V, with_q):
                             + rng.standard_normal((B * D, V)).astype(np.float32) * 0.7)
     q = q.astype(np.float32).reshape(B, D, V)
     src = q if with_q else p.reshape(B, R, V)[:, :D]
-    drafts = np.array([[rng.choice(V, p=src[b, j].astype(np.float64) / src[b, j].sum())
+    src = src.astype(np.float64)
+    drafts = np.array([[rng.choice(V, p=src[b, j] / src[b, j].sum())
                         for j in range(D)] for b in range(B)], np.int32).reshape(B, D)
     seed = synth.request_seeds(B)
     off = np.arange(B, dtype=np.int64) * 3
