@@ -4,6 +4,8 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 #include "../../include/ts_verify.h"
@@ -339,3 +341,91 @@ ts_status ts_gather_logprobs(const void* x, ts_dtype dt, int32_t is_probs, int64
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------
+// Greedy chain verification without a caller workspace.
+//
+// Some callers cannot hand the library device memory: a host that binds the C ABI
+// without any device allocator of its own, or code that runs where cudaMalloc is not
+// allowed (inside stream capture, where it would break the capture, or under a fixed
+// memory budget owned by another allocator). For them this variant keeps its scratch
+// (arrival counters and per-split partials) in a file-scope device array that every GPU
+// loading the library holds until the process exits. Its size is fixed, so the number
+// of rows it can serve is capped.
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)4 << 20;  // 4 MiB per device
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kStaticMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kStaticMaxDevices];  // device address of g_static_scratch, per device
+
+// The device address of the scratch array on the current device, looked up once per
+// device. (In host code the array's name is only a host-side handle, never a device
+// pointer.)
+ts_status static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kStaticMaxDevices)
+    return fail(TS_ERR_INVALID_ARG, "device ordinal %d beyond %d", dev, kStaticMaxDevices);
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return TS_OK;
+}
+
+}  // namespace
+
+extern "C" ts_status ts_verify_chain_greedy_static(const void* target_logits, ts_dtype dt,
+                                                   int64_t batch, int32_t D, int64_t vocab,
+                                                   int64_t ld, const int32_t* draft_tokens,
+                                                   int32_t* accepted_tokens,
+                                                   int32_t* accept_length,
+                                                   int32_t* accept_index, float* logprobs,
+                                                   cudaStream_t stream) {
+  ts_status st;
+  if ((st = check_dtype(dt)) != TS_OK) return st;
+  if (D < 0 || D > TS_MAX_DRAFT) return fail(TS_ERR_INVALID_ARG, "D must be in [0, %d]", TS_MAX_DRAFT);
+  if ((st = check_common(batch, vocab, ld)) != TS_OK) return st;
+  if (!target_logits || !accepted_tokens || !accept_length || (D > 0 && !draft_tokens))
+    return fail(TS_ERR_INVALID_ARG, "target_logits, draft_tokens, accepted_tokens and accept_length are required");
+  const int64_t rows = batch * (D + 1);
+  if (rows > TS_STATIC_MAX_ROWS)
+    return fail(TS_ERR_INVALID_ARG,
+                "batch*(D+1) = %lld rows exceeds the static scratch limit of %d rows",
+                (long long)rows, TS_STATIC_MAX_ROWS);
+  if (tsv::workspace_layout(batch, D + 1, nullptr, nullptr) > kStaticScratchBytes)
+    return fail(TS_ERR_INVALID_ARG, "the call needs more than the %zu-byte static scratch",
+                kStaticScratchBytes);
+  void* base = nullptr;
+  if ((st = static_scratch(&base)) != TS_OK) return st;
+  tsv::RowStatArgs a{};
+  tsv::workspace_layout(batch, D + 1, base, &a.ws);
+  // The array keeps whatever the previous call left; the arrival counters must start at 0.
+  cudaError_t e = cudaMemsetAsync(a.ws.rowcnt, 0, (size_t)rows * sizeof(uint32_t), stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(a.ws.reqcnt, 0, (size_t)batch * sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch counters");
+  a.x = target_logits;
+  a.ld = ld;
+  a.V = vocab;
+  a.rows = rows;
+  choose_splits(a.rows, vocab, 2048, &a.splits, &a.split_len);
+  a.vec = aligned16(target_logits, ld, dt == TS_BF16 ? 2 : 4);
+  a.want_lse = logprobs != nullptr;
+  a.kind = 0;
+  a.D = D;
+  a.draft_tokens = draft_tokens;
+  a.accepted_tokens = accepted_tokens;
+  a.accept_length = accept_length;
+  a.accept_index = accept_index;
+  a.logprobs = logprobs;
+  return launched(tsv::launch_rowstat(a, dt == TS_BF16, stream), "greedy verify (static scratch) launch");
+}
