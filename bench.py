@@ -104,7 +104,9 @@ def ncu_traffic(kernel: str, workload: str):
         with open(path) as f:
             d = json.load(f)
         e = d.get(f"{kernel}|{workload}")
-        return None if e is None else float(e["bytes_per_launch"])
+        if e is None or e.get("bytes_per_launch") is None:
+            return None
+        return float(e["bytes_per_launch"])
     except Exception:
         return None
 

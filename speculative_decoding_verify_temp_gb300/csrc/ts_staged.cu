@@ -1,8 +1,7 @@
 // Cluster-staged row kernels: one thread-block cluster per row. Each CTA of the cluster
 // copies its slice of the row into shared memory with 1-D TMA bulk copies (one HBM read
-// of the row), then all later passes (the max, the top-k and top-p thresholds, the
-// normaliser, the draw) run over shared memory; cluster-wide sums and histograms are
-// exchanged through distributed shared memory (DSMEM).
+// of the row); every later pass runs over shared memory, and the CTAs exchange partial
+// results through distributed shared memory (DSMEM).
 //
 // Modes
 //  kSoftmax  probs = softmax(x / T) per row (TokenSpeed flashinfer.py verify(): softmax)
@@ -11,16 +10,28 @@
 //            top-p (verify(): softmax + fused renorm + chain_speculative_sampling_target_only):
 //            every row computes its filtered distribution p'', the accept test of its draft
 //            (u_j < p''_j(x_j)) and, speculatively, its final draw (the residual p''_j without
-//            x_j, or the bonus p''_D) from u_D; the last row of a request to finish writes the
-//            chain.
+//            x_j, or the bonus p''_D) with u_D; the last row of a request to finish writes
+//            the chain.
 //
-// Exactness. Weights are fixed-point integers w = floor(e * 2^40) of the fp32 weight e
-// (exp((x - M) / T) computed as 2^(-(M - x) * log2(e) / T)), so every sum is exact and the
-// thresholds and draws are deterministic: the same inputs give the same bits on every run.
-// The order "value descending, then token id ascending" is the order of 56-bit composite
-// keys (an order-preserving 32-bit image of the value, then 2^24 - 1 - id); top-k and top-p
-// are radix selections on these keys (8-bit digits, cluster-wide histograms), top-p with a
-// leading digit that buckets the weight in eighths of an octave.
+// Order and thresholds. "Value descending, then token id ascending" is the order of 56-bit
+// composite keys (an order-preserving image of the value above 2^24 - 1 - id). Top-k keeps
+// the k largest composites and top-p a prefix of them, so every filter ends as one
+// threshold: a token is kept iff its composite >= C. The thresholds are found without
+// sorting the row:
+//  - top-k: the k-th largest of the per-thread maxima (gathered over the cluster) bounds
+//    the k-th largest element from below; one sweep compacts the few elements above the
+//    bound, and every CTA sorts the gathered candidates (bitonic, in shared memory);
+//  - top-p without top-k: a 512-bucket histogram of the weights (sixteenths of an octave
+//    below the row maximum) locates the bucket where the ordered mass crosses top_p; only
+//    that bucket's elements are compacted and sorted.
+// If a candidate list would overflow, the row takes a general path: a cluster-wide radix
+// selection over the staged slice (slower, same result).
+//
+// Exactness. Weights are fixed-point integers w = floor(e * 2^40) of the fp32 weight e =
+// 2^(-(M - x) * log2(e) / T), so the masses that decide the thresholds are exact integer
+// sums and the result is deterministic. The draw walks token ids in order: each thread
+// owns a contiguous range, sums its weights in fp32 (a fixed order), and the thread
+// totals, taken to fixed point, are combined exactly.
 #include <stdint.h>
 
 #include "ts_common.cuh"
@@ -31,11 +42,16 @@ namespace tsv {
 static __device__ unsigned int g_staged_err;
 
 constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
 constexpr int kChunks = 4;
 constexpr int kMaxCluster = 8;
 constexpr uint32_t kWaitLimit = 1u << 26;
-constexpr int64_t kSliceTarget = 64 * 1024;   // bytes of row per CTA we aim for
-constexpr int64_t kSliceMax = 192 * 1024;     // bytes of row per CTA we accept
+constexpr int64_t kSliceTarget = 50 * 1024;  // bytes of row per CTA we aim for
+constexpr int64_t kSliceMax = 160 * 1024;    // bytes of row per CTA we accept
+constexpr int kGatherCap = 4096;             // candidates of a row (held by CTA 0)
+constexpr int kNBins = 512;                  // top-p weight buckets
+constexpr float kBinScale = 16.f;            // buckets per octave
+static_assert(kNBins == kThreads, "the bucket scan gives one bucket to each thread");
 
 struct RowCtl {
   // read by peer CTAs through DSMEM
@@ -44,26 +60,31 @@ struct RowCtl {
   float p_lm;
   float p_ls;
   uint64_t p_sum;
+  uint32_t gcount;  // CTA 0: candidates appended by the cluster
   int32_t p_tok;
-  int32_t pad0;
-  unsigned long long mass[2][256];
+  int32_t b_ok;     // written by CTA 0: the selection result
+  int32_t b_pad;
+  uint64_t b_C;
+  uint64_t b_Zk;
+  unsigned long long mass[2][256];  // radix histograms; the top-p buckets use all 512
   uint32_t cnt[2][256];
   // local
   unsigned long long tot_mass[256];
   uint32_t tot_cnt[256];
   uint64_t bar[kChunks];
-  uint64_t scan[kThreads / 32];
-  float red_f[3][kThreads / 32];
-  int32_t red_i[kThreads / 32];
-  // broadcast scalars
+  uint64_t scan[kWarps];
+  float red_f[3][kWarps];
+  int32_t red_i[kWarps];
   float M, S1;
   int32_t am;
   int32_t bin;
   int32_t bincnt;
-  int32_t keep_all;
+  int32_t found;
   uint64_t above;
   uint64_t target;
   uint64_t Z;
+  uint64_t C;
+  uint64_t aux;
   int32_t tok;
   int32_t round;
 };
@@ -72,21 +93,49 @@ template <typename E>
 struct SV;
 template <>
 struct SV<float> {
+  static constexpr int N = 4;  // elements per 16-byte vector
   __device__ __forceinline__ static float get(const float* s, int64_t i) { return s[i]; }
+  __device__ __forceinline__ static void vec(const float* s, int64_t i, float* x) {
+    const float4 r = *reinterpret_cast<const float4*>(s + i);
+    x[0] = r.x;
+    x[1] = r.y;
+    x[2] = r.z;
+    x[3] = r.w;
+  }
 };
 template <>
 struct SV<uint16_t> {
+  static constexpr int N = 8;
   __device__ __forceinline__ static float get(const uint16_t* s, int64_t i) {
     return bf16_bits_to_f32(s[i]);
   }
+  __device__ __forceinline__ static void vec(const uint16_t* s, int64_t i, float* x) {
+    const uint4 r = *reinterpret_cast<const uint4*>(s + i);
+    x[0] = __uint_as_float(r.x << 16);
+    x[1] = __uint_as_float(r.x & 0xFFFF0000u);
+    x[2] = __uint_as_float(r.y << 16);
+    x[3] = __uint_as_float(r.y & 0xFFFF0000u);
+    x[4] = __uint_as_float(r.z << 16);
+    x[5] = __uint_as_float(r.z & 0xFFFF0000u);
+    x[6] = __uint_as_float(r.w << 16);
+    x[7] = __uint_as_float(r.w & 0xFFFF0000u);
+  }
 };
+
+// inverse of fkey
+__device__ __forceinline__ float key_to_f32(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+__device__ __forceinline__ uint32_t comp_idx(uint64_t c) {
+  return kIdxMax - (uint32_t)(c & kIdxMax);
+}
 
 struct RadixOut {
   uint64_t prefix, mask, above;
   int keep_all;
 };
 
-// Cluster-wide radix selection over 64-bit composite keys.
+// Cluster-wide radix selection over 64-bit composite keys (the general path).
 //   count mode: finds the group of the `target`-th largest key;
 //   mass mode:  finds the element at which the mass, accumulated in descending key
 //               order, first reaches `target` (or ceil(top_p * total) when top_p >= 0).
@@ -203,7 +252,6 @@ __device__ __forceinline__ bool selected(const RadixOut& o, uint64_t key) {
 // writes the block total.
 __device__ __forceinline__ uint64_t block_excl_scan_u64(uint64_t v, RowCtl* ctl, uint64_t& total) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  constexpr int nw = kThreads / 32;
   uint64_t incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -213,19 +261,103 @@ __device__ __forceinline__ uint64_t block_excl_scan_u64(uint64_t v, RowCtl* ctl,
   if (lane == 31) ctl->scan[w] = incl;
   __syncthreads();
   if (w == 0) {
-    uint64_t t = lane < nw ? ctl->scan[lane] : 0;
+    uint64_t t = lane < kWarps ? ctl->scan[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint64_t y = __shfl_up_sync(0xffffffffu, t, o);
       if (lane >= o) t += y;
     }
-    if (lane < nw) ctl->scan[lane] = t;
+    if (lane < kWarps) ctl->scan[lane] = t;
   }
   __syncthreads();
   const uint64_t before = (w > 0) ? ctl->scan[w - 1] : 0;
-  total = ctl->scan[nw - 1];
+  total = ctl->scan[kWarps - 1];
   __syncthreads();
   return before + incl - v;
+}
+
+// The largest C made of whole top digits such that at least k of a[0..n) are >= C: a
+// lower bound for the k-th largest, exact in the digits examined. CTA-local.
+__device__ uint32_t cta_select_bound(const uint32_t* a, int n, uint32_t k, int ndig, RowCtl* ctl) {
+  uint32_t prefix = 0, mask = 0, above = 0;
+  const int tid = threadIdx.x;
+  for (int di = 0; di < ndig; ++di) {
+    const int sh = 24 - 8 * di;
+    if (tid < 256) ctl->cnt[0][tid] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kThreads) {
+      const uint32_t v = a[i];
+      if ((v & mask) == prefix) atomicAdd(&ctl->cnt[0][(v >> sh) & 255u], 1u);
+    }
+    __syncthreads();
+    if (tid < 32) {
+      const int lane = tid;
+      uint32_t lw = 0;
+      for (int q = 0; q < 8; ++q) lw += ctl->cnt[0][255 - 8 * lane - q];
+      uint32_t incl = lw;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      uint32_t acc = above + (incl - lw);
+      int found = -1;
+      uint32_t acc_at = 0;
+      for (int q = 0; q < 8; ++q) {
+        const int bin = 255 - 8 * lane - q;
+        const uint32_t c = ctl->cnt[0][bin];
+        if (c > 0 && acc + c >= k) {
+          found = bin;
+          acc_at = acc;
+          break;
+        }
+        acc += c;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, found >= 0);
+      if (m == 0) {
+        if (lane == 0) {  // fewer than k items remain: the bound keeps the whole group
+          ctl->bin = 0;
+          ctl->above = above;
+        }
+      } else if (lane == __ffs(m) - 1) {
+        ctl->bin = found;
+        ctl->above = acc_at;
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)ctl->bin << sh;
+    mask |= 255u << sh;
+    above = (uint32_t)ctl->above;
+    __syncthreads();
+  }
+  return prefix;
+}
+
+// Bitonic sort of a[0..n) in shared memory (n a power of two); less(x, y) = "x first".
+template <class Less>
+__device__ void bitonic_sort(uint64_t* a, int n, Less less) {
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        const int ixj = i ^ jj;
+        if (ixj > i) {
+          const uint64_t x = a[i], y = a[ixj];
+          const bool up = ((i & k) == 0);
+          if (up ? less(y, x) : less(x, y)) {
+            a[i] = y;
+            a[ixj] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__device__ __forceinline__ int next_pow2(int n) {
+  int p = 1;
+  while (p < n) p <<= 1;
+  return p;
 }
 
 template <typename E>
@@ -236,18 +368,27 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
   const uint32_t CL = cluster.num_blocks();
   const int tid = threadIdx.x;
   const int64_t row = blockIdx.x / CL;
+  constexpr int NV = SV<E>::N;
   E* sv = reinterpret_cast<E*>(smem);
   const int64_t sv_bytes = (slice_n * (int64_t)sizeof(E) + 127) & ~(int64_t)127;
   RowCtl* ctl = reinterpret_cast<RowCtl*>(smem + sv_bytes);
+  uint64_t* gbuf =
+      reinterpret_cast<uint64_t*>(smem + sv_bytes + ((sizeof(RowCtl) + 127) & ~(size_t)127));
+  uint32_t* tmk = reinterpret_cast<uint32_t*>(gbuf + kGatherCap);  // this CTA's thread maxima
+  uint32_t* tmall = tmk + kThreads;                                  // the cluster's
   const int64_t lo = (int64_t)crank * slice_n;
   const int64_t n = max((int64_t)0, min(slice_n, a.V - lo));
   const E* xr = reinterpret_cast<const E*>(a.x) + row * a.ld;
 
   // ---- 1. stage the slice ----------------------------------------------------------
-  if (tid == 0) ctl->round = 0;
+  if (tid == 0) {
+    ctl->round = 0;
+    ctl->gcount = 0;
+  }
+  for (int i = tid; i < kNBins; i += kThreads) (&ctl->mass[0][0])[i] = 0;
   if (vec) {
     const int64_t bulk = (n * (int64_t)sizeof(E)) & ~(int64_t)15;
-    int64_t cb = ((bulk / kChunks) + 15) & ~(int64_t)15;
+    const int64_t cb = ((bulk / kChunks) + 15) & ~(int64_t)15;
     if (tid == 0) {
       for (int c = 0; c < kChunks; ++c) mbar_init(&ctl->bar[c], 1);
       fence_mbar_init();
@@ -257,7 +398,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
         mbar_arrive_expect_tx(&ctl->bar[c], (uint32_t)len);
         if (len > 0)
           bulk_g2s(reinterpret_cast<unsigned char*>(sv) + off,
-                   reinterpret_cast<const unsigned char*>(xr + lo) + off, (uint32_t)len, &ctl->bar[c]);
+                   reinterpret_cast<const unsigned char*>(xr + lo) + off, (uint32_t)len,
+                   &ctl->bar[c]);
       }
     }
     const int64_t tail0 = bulk / (int64_t)sizeof(E);
@@ -275,22 +417,31 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
   } else {
     for (int64_t i = tid; i < n; i += kThreads) sv[i] = xr[lo + i];
   }
+  // pad the slice to whole vectors with -inf (never kept, zero weight)
+  const int64_t nvec = (n + NV - 1) / NV;
+  if (tid < NV) {
+    const int64_t i = n + tid;
+    if (i < nvec * NV) {
+      if (sizeof(E) == 2) reinterpret_cast<uint16_t*>(sv)[i] = 0xFF80u;
+      else reinterpret_cast<float*>(sv)[i] = -INFINITY;
+    }
+  }
   __syncthreads();
 
   // ---- 2. row maximum, argmax (lowest id), thread maxima, temperature-1 log-sum-exp ----
   const bool want_lse = (a.mode == kChain) && a.logprobs != nullptr;
   float bv = -INFINITY, lm = -INFINITY, ls = 0.f, lc = 0.f;
   int32_t bi = INT32_MAX;
-  for (int64_t g = (int64_t)tid * 8; g < n; g += (int64_t)kThreads * 8) {
-    float x[8];
-    const int m = (int)min((int64_t)8, n - g);
-    for (int k = 0; k < 8; ++k) x[k] = k < m ? SV<E>::get(sv, g + k) : -INFINITY;
+  for (int64_t vi = tid; vi < nvec; vi += kThreads) {
+    float x[NV];
+    SV<E>::vec(sv, vi * NV, x);
     float vm = x[0];
-    for (int k = 1; k < m; ++k) vm = fmaxf(vm, x[k]);
+#pragma unroll
+    for (int q = 1; q < NV; ++q) vm = fmaxf(vm, x[q]);
     if (vm > bv || bi == INT32_MAX) {
-      for (int k = 0; k < m; ++k)
-        if (x[k] == vm) {
-          bi = (int32_t)(lo + g + k);
+      for (int q = 0; q < NV; ++q)
+        if (x[q] == vm) {
+          bi = (int32_t)(lo + vi * NV + q);
           break;
         }
       bv = vm;
@@ -302,13 +453,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
       lc *= f;
       lm = nm;
       float vs = 0.f;
-      for (int k = 0; k < m; ++k) vs += ex2((x[k] - nm) * kLog2e);
+#pragma unroll
+      for (int q = 0; q < NV; ++q) vs += ex2((x[q] - nm) * kLog2e);
       kahan_add(ls, lc, vs);
     }
   }
   ls += lc;
-  // this thread's largest element as an order key (0 = the thread holds no element)
-  const uint64_t tmax = (bi == INT32_MAX) ? 0ull : comp_key(fkey(bv), (uint32_t)bi);
+  // a padding element can be a thread's maximum only if the thread holds nothing else
+  if (bi != INT32_MAX && (int64_t)bi >= lo + n) bi = INT32_MAX;
+  // this thread's largest value as an order key (0 = the thread holds no element)
+  tmk[tid] = (bi == INT32_MAX) ? 0u : fkey(bv);
   {
     float v = bv, m = lm, s = ls;
     int32_t i = bi;
@@ -323,11 +477,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
     }
     __syncthreads();
     if (w == 0) {
-      constexpr int nw = kThreads / 32;
-      v = lane < nw ? ctl->red_f[0][lane] : -INFINITY;
-      m = lane < nw ? ctl->red_f[1][lane] : -INFINITY;
-      s = lane < nw ? ctl->red_f[2][lane] : 0.f;
-      i = lane < nw ? ctl->red_i[lane] : INT32_MAX;
+      v = lane < kWarps ? ctl->red_f[0][lane] : -INFINITY;
+      m = lane < kWarps ? ctl->red_f[1][lane] : -INFINITY;
+      s = lane < kWarps ? ctl->red_f[2][lane] : 0.f;
+      i = lane < kWarps ? ctl->red_i[lane] : INT32_MAX;
       warp_argmax(v, i);
       warp_lse(m, s);
       if (lane == 0) {
@@ -338,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
       }
     }
   }
-  cluster.sync();
+  cluster.sync();  // (1) partial statistics and thread maxima are visible
   if (tid < 32) {
     const int lane = tid;
     float v = -INFINITY, m = -INFINITY, s = 0.f;
@@ -378,101 +531,308 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
   const bool tpa = !greedy && tp < 1.f;
   const float sl2 = is_logits ? __fdiv_rn(kLog2e, T) : 0.f;
   const uint32_t pmax_bits = __float_as_uint(fmaxf(M, 0.f));
+  const bool bf16 = sizeof(E) == 2;
 
-  // weight of a value: fixed point of exp((x - M)/T) (logits) or of the value (probs)
+  // The weight of a value: e = 2^(-(M - x) log2(e)/T) (logits) or the value (probabilities).
+  auto dfn = [&](float v) -> float { return (M - v) * sl2; };
   auto efn = [&](float v) -> float {
-    return is_logits ? ex2(-((M - v) * sl2)) : fminf(fmaxf(v, 0.f), 1.f);
+    return is_logits ? ex2(-dfn(v)) : fminf(fmaxf(v, 0.f), 1.f);
   };
   auto wfn = [&](float v) -> uint64_t { return fixw(efn(v)); };
-  // weight bucket, larger = heavier: eighths of an octave below the row maximum
+  // the top-p bucket of a value, 0 = heaviest (sixteenths of an octave below the maximum)
+  auto bin512 = [&](float v) -> int {
+    if (is_logits) {
+      const float t = __fadd_rd(fminf(dfn(v) * kBinScale, 1.0e6f), 8388608.f);
+      return (int)min(__float_as_uint(t) - 0x4B000000u, (uint32_t)(kNBins - 1));
+    }
+    const uint32_t vb = __float_as_uint(fmaxf(v, 0.f));
+    return (vb == 0u) ? (kNBins - 1) : (int)min((pmax_bits - vb) >> 19, (uint32_t)(kNBins - 1));
+  };
+
+  // Decided below, identically in every CTA of the cluster. fast: a token is kept iff its
+  // composite >= C (C = 0 keeps everything), and Zk is the exact mass of the kept set
+  // when a selection found it.
+  bool fast = true;
+  uint64_t C = 0;
+  uint64_t Zk = 0;
+
+  // Walking gbuf[0..cnt) in descending order from a mass `base`: the first index whose
+  // inclusive mass reaches `target` (cnt if none), and the inclusive mass there (the
+  // total if none).
+  auto crossing = [&](int cnt, uint64_t base, uint64_t target, uint64_t& incl_at) -> int {
+    const int per = (cnt + kThreads - 1) / kThreads;
+    const int r0 = min(cnt, tid * per), r1 = min(cnt, r0 + per);
+    uint64_t s = 0;
+    for (int i = r0; i < r1; ++i) s += wfn(key_to_f32((uint32_t)(gbuf[i] >> kIdxBits)));
+    uint64_t tot;
+    const uint64_t ex = block_excl_scan_u64(s, ctl, tot);
+    if (tid == 0) {
+      ctl->found = cnt;
+      ctl->aux = base + tot;
+    }
+    __syncthreads();
+    if (base + ex < target && base + ex + s >= target) {
+      uint64_t acc = base + ex;
+      for (int i = r0; i < r1; ++i) {
+        acc += wfn(key_to_f32((uint32_t)(gbuf[i] >> kIdxBits)));
+        if (acc >= target) {
+          ctl->found = i;
+          ctl->aux = acc;
+          break;
+        }
+      }
+    } else if (tid == 0 && base >= target && cnt > 0) {
+      ctl->found = 0;  // reached before the first element: the first element crosses
+      ctl->aux = base + wfn(key_to_f32((uint32_t)(gbuf[0] >> kIdxBits)));
+    }
+    __syncthreads();
+    const int f = ctl->found;
+    incl_at = ctl->aux;
+    __syncthreads();
+    return f;
+  };
+
+  // Every CTA appends its candidates to CTA 0's list; after a cluster barrier CTA 0 sorts
+  // them, finds the threshold and writes it to every CTA; a second barrier publishes it.
+  uint32_t* g0count = cluster.map_shared_rank(&ctl->gcount, 0);
+  uint64_t* g0buf = cluster.map_shared_rank(gbuf, 0);
+  auto append = [&](uint64_t cp) {
+    const uint32_t pos = atomicAdd(g0count, 1u);
+    if (pos < (uint32_t)kGatherCap) g0buf[pos] = cp;
+  };
+  // topk: the first k candidates are the top-k set, then top-p inside it; else the
+  // candidates are one weight bucket whose ordered mass starts at `base` and must reach P
+  auto select_and_broadcast = [&](bool topk, uint64_t base, uint64_t P) {
+    if (crank == 0) {
+      const uint32_t total = ctl->gcount;
+      const bool ok = total <= (uint32_t)kGatherCap && total > 0 && (!topk || total >= (uint32_t)k);
+      uint64_t Cb = 0, Zb = 0;
+      if (ok) {
+        const int n2 = next_pow2(max((int)total, 2));
+        for (int i = (int)total + tid; i < n2; i += kThreads) gbuf[i] = 0ull;
+        __syncthreads();
+        bitonic_sort(gbuf, n2, [](uint64_t p, uint64_t q) { return p > q; });
+        uint64_t incl = 0;
+        if (topk) {
+          int nk = k;
+          (void)crossing(k, 0, ~0ull, Zb);  // the exact mass of the top-k set
+          if (tpa) {
+            const double want = ceil((double)tp * (double)Zb);
+            const uint64_t Pk = (want > (double)Zb) ? Zb : (uint64_t)want;
+            const int f = crossing(k, 0, Pk, incl);
+            if (f < k) {
+              nk = f + 1;
+              Zb = incl;
+            }
+          }
+          Cb = gbuf[nk - 1];
+        } else {
+          int f = crossing((int)total, base, P, incl);
+          if (f >= (int)total) f = (int)total - 1;  // the bucket holds the crossing
+          Cb = gbuf[f];
+          Zb = incl;
+        }
+      }
+      if (tid < (int)CL) {
+        RowCtl* pc = cluster.map_shared_rank(ctl, (uint32_t)tid);
+        pc->b_ok = ok ? 1 : 0;
+        pc->b_C = Cb;
+        pc->b_Zk = Zb;
+      }
+    }
+    cluster.sync();  // the selection result is visible
+    fast = ctl->b_ok != 0;
+    C = ctl->b_C;
+    Zk = ctl->b_Zk;
+  };
+
+  if (!greedy && a.mode != kSoftmax && (tk || tpa)) {
+    if (tk && (int64_t)k <= (int64_t)CL * kThreads) {
+      // ---- 4a. top-k: bound from the gathered thread maxima, compaction, selection -----
+      for (int i = tid; i < (int)CL * kThreads; i += kThreads)
+        tmall[i] = cluster.map_shared_rank(tmk, (uint32_t)(i / kThreads))[i % kThreads];
+      __syncthreads();
+      const uint32_t tkey = cta_select_bound(tmall, (int)CL * kThreads, (uint32_t)k, bf16 ? 2 : 4, ctl);
+      for (int64_t vi = tid; vi < nvec; vi += kThreads) {
+        float xv[NV];
+        SV<E>::vec(sv, vi * NV, xv);
+        float vm = xv[0];
+#pragma unroll
+        for (int q = 1; q < NV; ++q) vm = fmaxf(vm, xv[q]);
+        if (fkey(vm) < tkey) continue;
+        for (int q = 0; q < NV; ++q) {
+          const int64_t li = vi * NV + q;
+          if (li >= n) break;
+          const uint32_t kq = fkey(xv[q]);
+          if (kq >= tkey) append(comp_key(kq, (uint32_t)(lo + li)));
+        }
+      }
+      __syncthreads();
+      cluster.sync();  // (2) the candidates are in CTA 0
+      select_and_broadcast(true, 0, 0);  // (3)
+    } else if (!tk) {
+      // ---- 4b. top-p over the whole row: bucket histogram, then the crossing bucket ------
+      uint64_t tail = 0;
+      unsigned long long* hist = &ctl->mass[0][0];
+      for (int64_t vi = tid; vi < nvec; vi += kThreads) {
+        float xv[NV];
+        SV<E>::vec(sv, vi * NV, xv);
+#pragma unroll
+        for (int q = 0; q < NV; ++q) {
+          const uint64_t w = wfn(xv[q]);
+          if (w == 0) continue;
+          const int b = bin512(xv[q]);
+          if (b < kNBins - 1) atomicAdd(&hist[b], (unsigned long long)w);
+          else tail += w;
+        }
+      }
+      tail = warp_sum_u64(tail);
+      if ((tid & 31) == 0 && tail) atomicAdd(&hist[kNBins - 1], (unsigned long long)tail);
+      __syncthreads();
+      cluster.sync();  // (2) bucket histograms are visible
+      // every CTA: the cluster histogram (one bucket per thread), the total, the crossing
+      uint64_t hb = 0;
+      for (uint32_t c = 0; c < CL; ++c) hb += cluster.map_shared_rank(&ctl->mass[0][0], c)[tid];
+      uint64_t Zt;
+      const uint64_t ex = block_excl_scan_u64(hb, ctl, Zt);  // heaviest bucket first
+      const double want = ceil((double)tp * (double)Zt);
+      const uint64_t P = (want > (double)Zt) ? Zt : (uint64_t)want;
+      if (tid == 0) ctl->bin = (P == 0) ? -2 : -1;
+      __syncthreads();
+      if (P > 0 && hb > 0 && ex < P && ex + hb >= P) {
+        ctl->bin = tid;
+        ctl->above = ex;
+      }
+      __syncthreads();
+      const int bstar = ctl->bin;
+      const uint64_t acc0 = (bstar >= 0) ? ctl->above : 0;
+      if (bstar == -2) {
+        // top_p <= 0 keeps the argmax alone
+        const float vam = (sizeof(E) == 2) ? bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(xr)[am])
+                                           : reinterpret_cast<const float*>(xr)[am];
+        C = comp_key(fkey(vam), (uint32_t)am);
+        Zk = wfn(vam);
+        cluster.sync();  // (3) every branch here passes the same barriers
+        cluster.sync();  // (4)
+      } else if (bstar < 0 || bstar == kNBins - 1) {
+        fast = false;  // the crossing lies in the tail bucket: general path
+        cluster.sync();  // (3)
+        cluster.sync();  // (4)
+      } else {
+        for (int64_t vi = tid; vi < nvec; vi += kThreads) {
+          float xv[NV];
+          SV<E>::vec(sv, vi * NV, xv);
+          float vm = xv[0];
+#pragma unroll
+          for (int q = 1; q < NV; ++q) vm = fmaxf(vm, xv[q]);
+          if (bin512(vm) > bstar) continue;  // even the heaviest element is lighter
+          for (int q = 0; q < NV; ++q) {
+            const int64_t li = vi * NV + q;
+            if (li >= n) break;
+            if (bin512(xv[q]) != bstar || wfn(xv[q]) == 0) continue;
+            append(comp_key(fkey(xv[q]), (uint32_t)(lo + li)));
+          }
+        }
+        __syncthreads();
+        cluster.sync();  // (3) the candidates are in CTA 0
+        select_and_broadcast(false, acc0, P);  // (4)
+      }
+    } else {
+      fast = false;  // k larger than the thread-maxima bound can serve
+    }
+  }
+
+  // ---- 5. general path (rare): cluster-wide radix selection over the staged slice -------
+  RadixOut KT{0, 0, 0, 1}, KK{0, 0, 0, 1}, PP{0, 0, 0, 1};
   auto binkey = [&](float v) -> uint64_t {
     uint32_t b;
     if (is_logits) {
-      const float d = (M - v) * sl2;
-      b = (uint32_t)fminf(d * 8.f, 255.f);
+      b = (uint32_t)fminf(dfn(v) * 8.f, 255.f);
     } else {
       const uint32_t vb = __float_as_uint(fmaxf(v, 0.f));
       b = (vb == 0u) ? 255u : min(255u, (pmax_bits - vb) >> 20);
     }
     return (uint64_t)(255u - b) << 56;
   };
-
-  const bool bf16 = sizeof(E) == 2;
-  const int shk_f[7] = {48, 40, 32, 24, 16, 8, 0};
-  const int shk_h[5] = {48, 40, 16, 8, 0};
-  const int shp_f[8] = {56, 48, 40, 32, 24, 16, 8, 0};
-  const int shp_h[6] = {56, 48, 40, 16, 8, 0};
-
-  auto slice_sweep = [&](auto&& f) {
-    for (int64_t i = tid; i < n; i += kThreads) {
-      const float v = SV<E>::get(sv, i);
-      f(comp_key(fkey(v), (uint32_t)(lo + i)), v);
-    }
-  };
-
-  // ---- 4. top-k: a bound from the thread maxima, then the exact k-th key -----------------
-  RadixOut KT{0, 0, 0, 1}, KK{0, 0, 0, 1};
-  if (tk) {
-    if ((int64_t)k <= (int64_t)CL * kThreads) {
-      KT = cluster_radix<false>(
+  if (!fast) {
+    const int gk_f[7] = {48, 40, 32, 24, 16, 8, 0};
+    const int gk_h[5] = {48, 40, 16, 8, 0};
+    const int gp_f[8] = {56, 48, 40, 32, 24, 16, 8, 0};
+    const int gp_h[6] = {56, 48, 40, 16, 8, 0};
+    auto slice_sweep = [&](auto&& f) {
+      for (int64_t i = tid; i < n; i += kThreads) {
+        const float v = SV<E>::get(sv, i);
+        f(comp_key(fkey(v), (uint32_t)(lo + i)), v);
+      }
+    };
+    if (tk) {
+      if ((int64_t)k <= (int64_t)CL * kThreads) {
+        // thread maxima as (value, lowest id) composites: a bound on the k-th element
+        const uint64_t tm = (tmk[tid] == 0u) ? 0ull : comp_key(tmk[tid], (uint32_t)bi);
+        KT = cluster_radix<false>(
+            ctl, cluster, CL,
+            [&](auto&& f) {
+              if (tm) f(tm, 0.f);
+            },
+            [](float) { return (uint64_t)1; }, bf16 ? gk_h : gk_f, bf16 ? 5 : 7, (uint64_t)k,
+            -1.f);
+      }
+      KK = cluster_radix<false>(
           ctl, cluster, CL,
           [&](auto&& f) {
-            if (tmax) f(tmax, 0.f);
+            slice_sweep([&](uint64_t key, float v) {
+              if (selected(KT, key)) f(key, v);
+            });
           },
-          [](float) { return (uint64_t)1; }, bf16 ? shk_h : shk_f, bf16 ? 5 : 7, (uint64_t)k, -1.f);
+          [](float) { return (uint64_t)1; }, bf16 ? gk_h : gk_f, bf16 ? 5 : 7, (uint64_t)k, -1.f);
     }
-    KK = cluster_radix<false>(
-        ctl, cluster, CL,
-        [&](auto&& f) {
-          slice_sweep([&](uint64_t key, float v) {
-            if (selected(KT, key)) f(key, v);
-          });
-        },
-        [](float) { return (uint64_t)1; }, bf16 ? shk_h : shk_f, bf16 ? 5 : 7, (uint64_t)k, -1.f);
+    if (tpa) {
+      PP = cluster_radix<true>(
+          ctl, cluster, CL,
+          [&](auto&& f) {
+            slice_sweep([&](uint64_t key, float v) {
+              if (!tk || (selected(KT, key) && selected(KK, key))) f(binkey(v) | key, v);
+            });
+          },
+          wfn, bf16 ? gp_h : gp_f, bf16 ? 6 : 8, 0, tp);
+    }
   }
-  // The k-th key was selected among the elements that pass the thread-maxima bound, and an
-  // early exit leaves the low digits of KK open: top-k membership needs both tests.
-  auto keptk = [&](uint64_t key) -> bool {
-    return !tk || (selected(KT, key) && selected(KK, key));
-  };
-  // ---- 5. top-p on the top-k survivors ----------------------------------------------------
-  RadixOut PP{0, 0, 0, 1};
-  if (tpa) {
-    PP = cluster_radix<true>(
-        ctl, cluster, CL,
-        [&](auto&& f) {
-          slice_sweep([&](uint64_t key, float v) {
-            if (keptk(key)) f(binkey(v) | key, v);
-          });
-        },
-        wfn, bf16 ? shp_h : shp_f, bf16 ? 6 : 8, 0, tp);
-  }
+  // the kept predicate on a composite (and its value, for the general path's buckets)
   auto kept = [&](uint64_t key, float v) -> bool {
-    if (!keptk(key)) return false;
+    if (fast) return key >= C;
+    if (tk && !(selected(KT, key) && selected(KK, key))) return false;
     if (tpa && !selected(PP, binkey(v) | key)) return false;
     return true;
   };
 
-  // ---- 6. outputs ----------------------------------------------------------------------
+  // ---- 6a. softmax and renorm outputs -----------------------------------------------------
   if (a.mode == kSoftmax || a.mode == kRenorm) {
-    uint64_t zt = 0;
-    if (!greedy) {
-      for (int64_t i = tid; i < n; i += kThreads) {
-        const float v = SV<E>::get(sv, i);
-        if (a.mode == kSoftmax || kept(comp_key(fkey(v), (uint32_t)(lo + i)), v)) zt += wfn(v);
+    uint64_t Z = Zk;
+    const bool have_z = fast && (tk || tpa) && Zk > 0;
+    if (!have_z) {
+      // the mass of the kept set by a sweep; thread sums of at most a few hundred
+      // weights <= 1 stay below 2^49 in fixed point
+      float s = 0.f;
+      if (!greedy) {
+        for (int64_t vi = tid; vi < nvec; vi += kThreads) {
+          float xv[NV];
+          SV<E>::vec(sv, vi * NV, xv);
+#pragma unroll
+          for (int q = 0; q < NV; ++q) {
+            const int64_t li = vi * NV + q;
+            if (a.mode == kSoftmax || kept(comp_key(fkey(xv[q]), (uint32_t)(lo + li)), xv[q]))
+              s += efn(xv[q]);
+          }
+        }
       }
-    }
-    uint64_t tot;
-    (void)block_excl_scan_u64(zt, ctl, tot);
-    if (tid == 0) ctl->p_sum = tot;
-    cluster.sync();
-    if (tid == 0) {
-      uint64_t Z = 0;
+      uint64_t tot;
+      (void)block_excl_scan_u64(fixw(s), ctl, tot);
+      if (tid == 0) ctl->p_sum = tot;
+      cluster.sync();
+      Z = 0;
       for (uint32_t c = 0; c < CL; ++c) Z += cluster.map_shared_rank(ctl, c)->p_sum;
-      ctl->Z = Z;
     }
-    __syncthreads();
-    const float scale = (ctl->Z > 0) ? __fdiv_rn(kFx, __ull2float_rn(ctl->Z)) : 0.f;
+    const float scale = (Z > 0) ? __fdiv_rn(kFx, __ull2float_rn(Z)) : 0.f;
     float* orow = a.out + row * a.V + lo;
     for (int64_t i = tid; i < n; i += kThreads) {
       const float v = SV<E>::get(sv, i);
@@ -486,84 +846,110 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
     return;
   }
 
-  // kChain: the accept test of this row's draft and this row's speculative draw
+  // ---- 6b. chain: the accept test of this row's draft and this row's speculative draw ---
   const int32_t D = a.D;
   const int32_t x = (j < D) ? a.draft_tokens[req * D + j] : -1;
   const bool xvalid = x >= 0 && (int64_t)x < a.V;
-  const uint64_t seed = a.seed ? (uint64_t)a.seed[req] : 0, off = a.offset ? (uint64_t)a.offset[req] : 0;
-  const float uj = (j < D) ? (a.uniforms ? a.uniforms[req * a.R + j] : verify_coin(seed, off, (uint32_t)j)) : 0.f;
-  const float uD = a.uniforms ? a.uniforms[req * a.R + D] : verify_coin(seed, off, (uint32_t)D);
+  if (tid == 0) {
+    const uint64_t seed = a.seed ? (uint64_t)a.seed[req] : 0;
+    const uint64_t off = a.offset ? (uint64_t)a.offset[req] : 0;
+    ctl->red_f[0][0] =
+        (j < D) ? (a.uniforms ? a.uniforms[req * a.R + j] : verify_coin(seed, off, (uint32_t)j)) : 0.f;
+    ctl->red_f[1][0] = a.uniforms ? a.uniforms[req * a.R + D] : verify_coin(seed, off, (uint32_t)D);
+    ctl->tok = -1;
+  }
+  __syncthreads();
+  const float uj = ctl->red_f[0][0], uD = ctl->red_f[1][0];
   int32_t acc = 0, tok = am;
   if (greedy) {
     acc = (j < D) && (x == am);
   } else {
-    // contiguous per-thread ranges, so that the draw can walk tokens in id order
-    const int64_t cpt = (n + kThreads - 1) / kThreads;
-    const int64_t r0 = min(n, (int64_t)tid * cpt), r1 = min(n, r0 + cpt);
-    uint64_t zt = 0;
-    for (int64_t i = r0; i < r1; ++i) {
-      const float v = SV<E>::get(sv, i);
-      const int64_t gi = lo + i;
-      if (gi != (int64_t)x && kept(comp_key(fkey(v), (uint32_t)gi), v)) zt += wfn(v);
-    }
-    uint64_t ctot;
-    const uint64_t texcl = block_excl_scan_u64(zt, ctl, ctot);
-    if (tid == 0) ctl->p_sum = ctot;
-    if (tid == 0) ctl->tok = -1;
-    cluster.sync();
-    // every CTA: the cluster totals, this CTA's prefix, the weight of the draft token
-    uint64_t Zr = 0, cpre = 0;
-    int last_nz = -1;
-    for (uint32_t c = 0; c < CL; ++c) {
-      const uint64_t pc = cluster.map_shared_rank(ctl, c)->p_sum;
-      if (c < crank) cpre += pc;
-      if (pc > 0) last_nz = (int)c;
-      Zr += pc;
-    }
+    // the draft token's weight
     uint64_t wx = 0;
     if (xvalid) {
       const float vx = (sizeof(E) == 2) ? bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(xr)[x])
                                          : reinterpret_cast<const float*>(xr)[x];
       if (kept(comp_key(fkey(vx), (uint32_t)x), vx)) wx = wfn(vx);
     }
-    const uint64_t Zf = Zr + wx;
-    if (j < D) acc = ((double)uj * (double)Zf < (double)wx) ? 1 : 0;
-    const uint64_t Zd = Zr;  // residual (x removed) or bonus (x = -1 removes nothing)
-    if (Zd == 0) {
-      tok = (wx > 0) ? x : am;  // all the mass sits on the draft token
-    } else {
-      const double tt = (double)uD * (double)Zd;
-      uint64_t t = (uint64_t)tt;
-      bool past = (t >= Zd);
-      // this CTA holds the crossing iff cpre <= t < cpre + ctot (or it is the last with mass)
-      const bool mine = past ? ((int)crank == last_nz) : (cpre <= t && t < cpre + ctot);
-      if (mine) {
-        const uint64_t tl = past ? ~0ull : t - cpre;
-        const bool hit = past ? (zt > 0 && texcl + zt == ctot) : (texcl <= tl && tl < texcl + zt);
-        if (hit) {
-          uint64_t accw = texcl;
-          int32_t found = -1, lastk = -1;
-          for (int64_t i = r0; i < r1; ++i) {
-            const float v = SV<E>::get(sv, i);
-            const int64_t gi = lo + i;
-            if (gi == (int64_t)x || !kept(comp_key(fkey(v), (uint32_t)gi), v)) continue;
-            const uint64_t w = wfn(v);
-            if (w == 0) continue;
-            lastk = (int32_t)gi;
-            if (!past && accw + w > tl) {
-              found = (int32_t)gi;
-              break;
+    {
+      // token-id order over the slice: contiguous per-thread ranges of whole vectors
+      const int64_t per = (nvec + kThreads - 1) / kThreads;
+      const int64_t v0 = min(nvec, (int64_t)tid * per), v1 = min(nvec, v0 + per);
+      auto wsum = [&](float v, int64_t gi) -> float {
+        if (gi == (int64_t)x) return 0.f;
+        if (!kept(comp_key(fkey(v), (uint32_t)gi), v)) return 0.f;
+        return efn(v);
+      };
+      const uint32_t ckey = (uint32_t)(C >> kIdxBits);
+      float s = 0.f;
+      for (int64_t vi = v0; vi < v1; ++vi) {
+        float xv[NV];
+        SV<E>::vec(sv, vi * NV, xv);
+        if (fast && C) {
+          float vm = xv[0];
+#pragma unroll
+          for (int q = 1; q < NV; ++q) vm = fmaxf(vm, xv[q]);
+          if (fkey(vm) < ckey) continue;  // no element of the vector is kept
+        }
+#pragma unroll
+        for (int q = 0; q < NV; ++q) s += wsum(xv[q], lo + vi * NV + q);
+      }
+      const uint64_t sfx = fixw(s);
+      uint64_t ctot;
+      const uint64_t texcl = block_excl_scan_u64(sfx, ctl, ctot);
+      if (tid == 0) ctl->p_sum = ctot;
+      cluster.sync();  // CTA masses are visible
+      uint64_t Zr = 0, cpre = 0;
+      int last_nz = -1;
+      for (uint32_t c = 0; c < CL; ++c) {
+        const uint64_t pc = cluster.map_shared_rank(ctl, c)->p_sum;
+        if (c < crank) cpre += pc;
+        if (pc > 0) last_nz = (int)c;
+        Zr += pc;
+      }
+      const uint64_t Zf = Zr + wx;
+      if (j < D) acc = ((double)uj * (double)Zf < (double)wx) ? 1 : 0;
+      if (Zr == 0) {
+        tok = (wx > 0) ? x : am;  // all the mass sits on the draft token
+      } else {
+        const uint64_t t = (uint64_t)((double)uD * (double)Zr);
+        const bool past = (t >= Zr);
+        const bool mine = past ? ((int)crank == last_nz) : (cpre <= t && t < cpre + ctot);
+        if (mine) {
+          const uint64_t tl = past ? 0 : t - cpre;
+          const bool hit = past ? (sfx > 0 && texcl + sfx == ctot) : (texcl <= tl && tl < texcl + sfx);
+          if (hit) {
+            const float tf = past ? INFINITY : (float)(tl - texcl) * (1.0f / kFx);
+            float accf = 0.f;
+            int32_t found = -1, lastk = -1;
+            for (int64_t vi = v0; vi < v1 && found < 0; ++vi) {
+              float xv[NV];
+              SV<E>::vec(sv, vi * NV, xv);
+              if (fast && C) {
+                float vm = xv[0];
+#pragma unroll
+                for (int q = 1; q < NV; ++q) vm = fmaxf(vm, xv[q]);
+                if (fkey(vm) < ckey) continue;
+              }
+              for (int q = 0; q < NV; ++q) {
+                const float w = wsum(xv[q], lo + vi * NV + q);
+                if (w == 0.f) continue;
+                lastk = (int32_t)(lo + vi * NV + q);
+                accf += w;
+                if (accf > tf) {
+                  found = lastk;
+                  break;
+                }
+              }
             }
-            accw += w;
+            if (found < 0) found = lastk;
+            *cluster.map_shared_rank(&ctl->tok, 0) = found;
           }
-          if (found < 0) found = lastk;
-          int32_t* dst = cluster.map_shared_rank(&ctl->tok, 0);
-          *dst = found;
         }
       }
     }
   }
-  cluster.sync();
+  cluster.sync();  // the drawn token has reached CTA 0
   if (crank == 0 && tid == 0) {
     if (!greedy && ctl->tok >= 0) tok = ctl->tok;
     a.ws.rowres[row] = RowRes{M, am, ctl->S1, tok, acc, {0, 0, 0}};
@@ -602,10 +988,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
   cluster.sync();
 }
 
+static size_t extra_smem() {
+  return ((sizeof(RowCtl) + 127) & ~(size_t)127) + sizeof(uint64_t) * (size_t)kGatherCap +
+         sizeof(uint32_t) * (size_t)(kThreads + kMaxCluster * kThreads);
+}
+
 static int64_t slice_elems(int64_t V, int esize, int* CL_out) {
-  int64_t bytes = V * esize;
-  int CL = (int)min((int64_t)kMaxCluster, max((int64_t)1, (bytes + kSliceTarget - 1) / kSliceTarget));
-  int64_t sl = ((V + CL - 1) / CL + 15) & ~(int64_t)15;
+  const int64_t bytes = V * esize;
+  const int CL = (int)min((int64_t)kMaxCluster, max((int64_t)1, (bytes + kSliceTarget - 1) / kSliceTarget));
+  // whole 16-element groups, so every slice starts 16-byte aligned and vectors never straddle
+  const int64_t sl = ((V + CL - 1) / CL + 15) & ~(int64_t)15;
   *CL_out = CL;
   return sl;
 }
@@ -623,7 +1015,7 @@ static cudaError_t launch_t(const StagedArgs& a, cudaStream_t s, const char** wh
     *why = "vocab too large for the cluster-staged kernel";
     return cudaErrorInvalidValue;
   }
-  const size_t smem = (size_t)((sl * (int64_t)sizeof(E) + 127) & ~(int64_t)127) + sizeof(RowCtl);
+  const size_t smem = (size_t)((sl * (int64_t)sizeof(E) + 127) & ~(int64_t)127) + extra_smem();
   cudaError_t e = cudaFuncSetAttribute(k_staged<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;

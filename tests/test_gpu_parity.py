@@ -303,3 +303,48 @@ def test_invalid_arguments_raise():
     with pytest.raises(tv.TsError):
         tv.gather_logprobs(x.to(torch.bfloat16), torch.zeros(4, dtype=torch.int32, device="cuda"),
                            is_probs=True)
+
+
+# ---- routes of the cluster-staged selection ------------------------------------------------
+
+def _route_rows(V, dtype, rng):
+    """Rows that send the selection down each route: ordinary, all-equal (ties swamp the
+    candidate lists: general path), flat high-temperature (large nucleus), spiky."""
+    x = rng.standard_normal((8, V), dtype=np.float32) * np.float32(3.0)
+    x += synth.zipf_bias(V)[None, :]
+    x[1] = 0.5                                   # all equal
+    x[2] = rng.integers(-2, 2, V).astype(np.float32)  # few distinct values, many ties
+    x[3] *= np.float32(0.05)                     # nearly flat
+    x[4, 100:200] = 30.0                         # a block of equal maxima
+    if dtype == "bf16":
+        bits = synth.bf16_bits_from_f32(x)
+        return dict(dtype="bf16", logits_bits=bits, logits=synth.f32_from_bf16_bits(bits))
+    return dict(dtype="f32", logits=x)
+
+
+@pytest.mark.parametrize("V,dtype", [(32000, "bf16"), (201088, "bf16"), (60000, "f32")])
+@pytest.mark.parametrize("k,p,T", [(1, 1.0, 1.0), (50, 1.0, 0.7), (1000, 0.9, 1.5),
+                                   (3000, 1.0, 1.0), (0, 0.95, 1.5), (0, 0.5, 0.3),
+                                   (0, 0.0, 1.0), (7, 0.0, 1.0), (0, 1.0, 1.2)])
+def test_selection_routes(V, dtype, k, p, T):
+    rng = np.random.default_rng(V + k + int(100 * p))
+    d = _route_rows(V, dtype, rng)
+    B, D = 2, 3
+    R = D + 1
+    drafts = rng.integers(0, V, (B, D)).astype(np.int32)
+    drafts[0, :] = d["logits"][:3].argmax(-1)
+    uni = rng.uniform(0.01, 0.99, (B, R)).astype(np.float32)
+    kw = dict(temperature=np.full(B, T, np.float32), top_k=np.full(B, k, np.int32),
+              top_p=np.full(B, p, np.float32))
+    g = tv.chain_spec_sampling(dev_logits(d), True, D, dev(drafts), uniforms=dev(uni),
+                               **{a: dev(b) for a, b in kw.items()})
+    ref = oracle.chain_spec_sampling(d["logits"], True, D, drafts, uniforms=uni, **kw)
+    compare_chain(g, ref, dtype)
+    # the same rows as probabilities through the renorm call
+    pr = oracle.softmax_temp(d["logits"], np.full(8, T, np.float32)).astype(np.float32)
+    got = tv.topk_topp_renorm(dev(pr), dev(np.full(8, k, np.int32)),
+                              dev(np.full(8, p, np.float32))).cpu().numpy()
+    want, marg = oracle.topk_topp_renorm(pr, np.full(8, k, np.int32), np.full(8, p, np.float32))
+    ok = marg > BOUNDARY
+    np.testing.assert_array_equal(got[ok] > 0, want[ok] > 0)
+    np.testing.assert_allclose(got[ok], want[ok], rtol=1e-5, atol=1e-6)
