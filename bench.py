@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-legs", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=48, help="requests in the CPU baseline sample")
+    ap.add_argument("--knobs", default=None,
+                    help="T,top_k,top_p applied to every request (profiling one selection route)")
     ap.add_argument("--batch", type=int, default=512,
                     help="requests per step (512 = the benchmark workload; smaller for profiling)")
     return ap.parse_args()
@@ -196,10 +198,16 @@ def time_device(fn, steps: int, warmup: int, device):
 
 # ---- the workload -----------------------------------------------------------------------
 
-def main_workload(batch: int = 512):
+def main_workload(batch: int = 512, knobs=None):
     from speculative_decoding_verify_temp_gb300 import synth
 
-    return synth.verify_step(B=batch, D=3, V=201088, real_vocab=200019)
+    d = synth.verify_step(B=batch, D=3, V=201088, real_vocab=200019)
+    if knobs:
+        T, k, p = knobs.split(",")
+        d["temperature"][:] = float(T)
+        d["top_k"][:] = int(k)
+        d["top_p"][:] = float(p)
+    return d
 
 
 def cpu_baseline(d, nreq: int):
@@ -232,7 +240,7 @@ def run_reference(args):
     from speculative_decoding_verify_temp_gb300 import synth
 
     oracle.build()
-    d = main_workload(args.batch)
+    d = main_workload(args.batch, args.knobs)
     D = d["D"]
     R = D + 1
     nreq = 8
@@ -280,7 +288,7 @@ def run_ours(args):
     tv.load()
     peak, peak_kind = measured_peaks()
 
-    d = main_workload(args.batch)
+    d = main_workload(args.batch, args.knobs)
     B, D, V = d["B"], d["D"], d["V"]
     R = D + 1
     rows = B * R
@@ -349,7 +357,8 @@ def run_ours(args):
                    "top_k": "uniform {0,20,50,1000}", "top_p": "uniform {1.0,0.95,0.9}",
                    "temperature": "U[0.3,1.5]",
                    "l2": f"inputs {alg_bytes / 1e6:.0f} MB vs 129 MB L2 (no flush)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   **({"knobs_override": args.knobs} if args.knobs else {})},
         "hbm_gbs": achieved, "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,

@@ -280,6 +280,30 @@ ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t
   a.accept_length = p->accept_length;
   a.accept_index = p->accept_index;
   a.logprobs = p->logprobs;
+  if (p->temperature) {
+    // Greedy requests need only the argmax of each row: a streaming pass handles them,
+    // and the staged kernel skips them.
+    tsv::RowStatArgs g{};
+    g.ws = a.ws;
+    g.x = p->target;
+    g.ld = p->ld;
+    g.V = p->vocab;
+    g.rows = a.rows;
+    choose_splits(g.rows, p->vocab, 2048, &g.splits, &g.split_len);
+    g.vec = aligned16(p->target, p->ld, p->target_dtype == TS_BF16 ? 2 : 4);
+    g.want_lse = p->logprobs != nullptr;
+    g.kind = 0;
+    g.D = p->D;
+    g.draft_tokens = p->draft_tokens;
+    g.accepted_tokens = p->accepted_tokens;
+    g.accept_length = p->accept_length;
+    g.accept_index = p->accept_index;
+    g.logprobs = p->logprobs;
+    g.req_temperature = p->temperature;
+    cudaError_t e = tsv::launch_rowstat(g, p->target_dtype == TS_BF16, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "greedy rows launch");
+    a.skip_greedy = 1;
+  }
   const char* why = "target-only chain launch";
   return launched(tsv::launch_staged(a, stream, &why), why);
 }

@@ -69,6 +69,9 @@ struct RowStatArgs {
   int32_t* accept_length;
   int32_t* accept_index;
   float* logprobs;
+  // greedy verify inside a sampled chain: rows of requests whose temperature (per
+  // request) is not greedy are left to the staged kernel
+  const float* req_temperature;
   // gather logprobs
   const int32_t* lp_tokens;
   float* lp_out;
@@ -125,6 +128,7 @@ struct StagedArgs {
   int32_t* accept_length;
   int32_t* accept_index;
   float* logprobs;
+  int32_t skip_greedy;  // chain: greedy requests are handled by the streaming kernel
   Workspace ws;
 };
 

@@ -51,6 +51,7 @@ constexpr int64_t kSliceMax = 160 * 1024;    // bytes of row per CTA we accept
 constexpr int kGatherCap = 4096;             // candidates of a row (held by CTA 0)
 constexpr int kNBins = 512;                  // top-p weight buckets
 constexpr float kBinScale = 16.f;            // buckets per octave
+constexpr int kHistBins = 384;               // buckets over 24 octaves; the rest is the tail
 static_assert(kNBins == kThreads, "the bucket scan gives one bucket to each thread");
 
 struct RowCtl {
@@ -66,7 +67,9 @@ struct RowCtl {
   int32_t b_pad;
   uint64_t b_C;
   uint64_t b_Zk;
-  unsigned long long mass[2][256];  // radix histograms; the top-p buckets use all 512
+  // radix mass histograms as three 32-bit digit sums (14, 14 and 13 bits of each
+  // weight), double-buffered; the top-p buckets use them as [3][512]
+  uint32_t m3[2][3][256];
   uint32_t cnt[2][256];
   // local
   unsigned long long tot_mass[256];
@@ -87,7 +90,22 @@ struct RowCtl {
   uint64_t aux;
   int32_t tok;
   int32_t round;
+  float uj, uD, vx;  // this row's coins and its draft token's value
 };
+
+// Exact accumulation of weights below 2^42 with 32-bit shared-memory atomics: the
+// weight is split into 14-, 14- and 13-bit digits, each summed on its own counter
+// (no overflow for fewer than 2^18 additions per counter).
+__device__ __forceinline__ void add3(uint32_t* d0, uint32_t* d1, uint32_t* d2, uint64_t w) {
+  const uint32_t lo = (uint32_t)w & 0x3FFFu, mid = (uint32_t)(w >> 14) & 0x3FFFu;
+  const uint32_t hi = (uint32_t)(w >> 28);
+  if (lo) atomicAdd(d0, lo);
+  if (mid) atomicAdd(d1, mid);
+  if (hi) atomicAdd(d2, hi);
+}
+__device__ __forceinline__ uint64_t get3(uint32_t a0, uint32_t a1, uint32_t a2) {
+  return (uint64_t)a0 + ((uint64_t)a1 << 14) + ((uint64_t)a2 << 28);
+}
 
 template <typename E>
 struct SV;
@@ -151,7 +169,9 @@ __device__ RadixOut cluster_radix(RowCtl* ctl, cg::cluster_group& cluster, uint3
     const int sh = shifts[di];
     const int buf = ctl->round & 1;
     for (int i = tid; i < 256; i += kThreads) {
-      ctl->mass[buf][i] = 0;
+      ctl->m3[buf][0][i] = 0;
+      ctl->m3[buf][1][i] = 0;
+      ctl->m3[buf][2][i] = 0;
       ctl->cnt[buf][i] = 0;
     }
     __syncthreads();
@@ -160,7 +180,8 @@ __device__ RadixOut cluster_radix(RowCtl* ctl, cg::cluster_group& cluster, uint3
       if ((key & msk) == pre) {
         const int bin = (int)((key >> sh) & 255u);
         atomicAdd(&ctl->cnt[buf][bin], 1u);
-        if (MASS) atomicAdd(&ctl->mass[buf][bin], (unsigned long long)wfn(v));
+        if (MASS)
+          add3(&ctl->m3[buf][0][bin], &ctl->m3[buf][1][bin], &ctl->m3[buf][2][bin], wfn(v));
       }
     });
     __syncthreads();
@@ -170,7 +191,7 @@ __device__ RadixOut cluster_radix(RowCtl* ctl, cg::cluster_group& cluster, uint3
       uint32_t tc = 0;
       for (uint32_t c = 0; c < CL; ++c) {
         RowCtl* pc = cluster.map_shared_rank(ctl, c);
-        tm += pc->mass[buf][tid];
+        tm += get3(pc->m3[buf][0][tid], pc->m3[buf][1][tid], pc->m3[buf][2][tid]);
         tc += pc->cnt[buf][tid];
       }
       ctl->tot_mass[tid] = tm;
@@ -333,25 +354,118 @@ __device__ uint32_t cta_select_bound(const uint32_t* a, int n, uint32_t k, int n
   return prefix;
 }
 
-// Bitonic sort of a[0..n) in shared memory (n a power of two); less(x, y) = "x first".
-template <class Less>
-__device__ void bitonic_sort(uint64_t* a, int n, Less less) {
-  for (int k = 2; k <= n; k <<= 1) {
-    for (int jj = k >> 1; jj > 0; jj >>= 1) {
-      for (int i = threadIdx.x; i < n; i += kThreads) {
-        const int ixj = i ^ jj;
-        if (ixj > i) {
-          const uint64_t x = a[i], y = a[ixj];
-          const bool up = ((i & k) == 0);
-          if (up ? less(y, x) : less(x, y)) {
-            a[i] = y;
-            a[ixj] = x;
-          }
-        }
-      }
-      __syncthreads();
+// CTA-local radix selection over the items of a[0..n) that are >= lo_key, in descending
+// order: count mode finds the set of the `target` largest, mass mode the shortest top set
+// whose mass (wfn of each item) reaches `target`. Returns the smallest item of that set,
+// so an item is selected iff it is >= the result (all eligible items if the target lies
+// beyond their total).
+template <bool MASS, class WFn>
+__device__ uint64_t cta_radix(const uint64_t* a, int n, uint64_t lo_key, uint64_t target, WFn wfn,
+                              const int* shifts, int nsh, RowCtl* ctl, uint64_t* group_max = nullptr,
+                              bool* beyond = nullptr) {
+  uint64_t prefix = 0, mask = 0, above = 0;
+  const int tid = threadIdx.x;
+  bool all = false;
+  for (int di = 0; di < nsh; ++di) {
+    const int sh = shifts[di];
+    if (tid < 256) {
+      ctl->m3[0][0][tid] = 0;
+      ctl->m3[0][1][tid] = 0;
+      ctl->m3[0][2][tid] = 0;
+      ctl->cnt[0][tid] = 0;
     }
+    __syncthreads();
+    for (int i = tid; i < n; i += kThreads) {
+      const uint64_t v = a[i];
+      if (v >= lo_key && (v & mask) == prefix) {
+        const int b = (int)((v >> sh) & 255u);
+        atomicAdd(&ctl->cnt[0][b], 1u);
+        if (MASS) add3(&ctl->m3[0][0][b], &ctl->m3[0][1][b], &ctl->m3[0][2][b], wfn(v));
+      }
+    }
+    __syncthreads();
+    if (tid < 32) {
+      const int lane = tid;
+      unsigned long long lw = 0;
+      for (int q = 0; q < 8; ++q) {
+        const int bin = 255 - 8 * lane - q;
+        lw += MASS ? get3(ctl->m3[0][0][bin], ctl->m3[0][1][bin], ctl->m3[0][2][bin])
+                   : (unsigned long long)ctl->cnt[0][bin];
+      }
+      unsigned long long incl = lw;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      unsigned long long acc = above + (incl - lw), acc_at = 0;
+      int found = -1;
+      for (int q = 0; q < 8; ++q) {
+        const int bin = 255 - 8 * lane - q;
+        const uint32_t c = ctl->cnt[0][bin];
+        const unsigned long long wgt =
+            MASS ? get3(ctl->m3[0][0][bin], ctl->m3[0][1][bin], ctl->m3[0][2][bin])
+                 : (unsigned long long)c;
+        if (c > 0 && acc + wgt >= target) {
+          found = bin;
+          acc_at = acc;
+          break;
+        }
+        acc += wgt;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, found >= 0);
+      if (m == 0) {
+        if (lane == 0) ctl->bin = -1;
+      } else if (lane == __ffs(m) - 1) {
+        ctl->bin = found;
+        ctl->above = acc_at;
+        ctl->bincnt = (int32_t)ctl->cnt[0][found];
+      }
+    }
+    __syncthreads();
+    const int bin = ctl->bin;
+    const uint64_t ab = ctl->above;
+    const int bc = ctl->bincnt;
+    __syncthreads();
+    if (bin < 0) {
+      all = true;
+      break;
+    }
+    prefix |= (uint64_t)bin << sh;
+    mask |= (uint64_t)255u << sh;
+    above = ab;
+    if (!MASS && above + (uint64_t)bc == target) break;
+    if (MASS && bc == 1) break;
   }
+  if (beyond) *beyond = all;
+  // the smallest selected item, and the largest item of the final group
+  unsigned long long mn = ~0ull, gx = 0;
+  for (int i = tid; i < n; i += kThreads) {
+    const uint64_t v = a[i];
+    if (v >= lo_key && (all || (v & mask) >= prefix) && v < mn) mn = v;
+    if (v >= lo_key && !all && (v & mask) == prefix && v > gx) gx = v;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const unsigned long long y = __shfl_xor_sync(0xffffffffu, mn, off);
+    mn = y < mn ? y : mn;
+    const unsigned long long z = __shfl_xor_sync(0xffffffffu, gx, off);
+    gx = z > gx ? z : gx;
+  }
+  if (tid == 0) {
+    ctl->aux = ~0ull;
+    ctl->Z = 0;
+  }
+  __syncthreads();
+  if ((tid & 31) == 0) {
+    atomicMin(reinterpret_cast<unsigned long long*>(&ctl->aux), mn);
+    atomicMax(reinterpret_cast<unsigned long long*>(&ctl->Z), gx);
+  }
+  __syncthreads();
+  const uint64_t r = ctl->aux;
+  if (group_max) *group_max = ctl->Z;
+  __syncthreads();
+  return r;
 }
 
 __device__ __forceinline__ int next_pow2(int n) {
@@ -380,12 +494,38 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
   const int64_t n = max((int64_t)0, min(slice_n, a.V - lo));
   const E* xr = reinterpret_cast<const E*>(a.x) + row * a.ld;
 
+  // the request's temperature, its draft at this row, and the coins: read before the
+  // slice lands, so their latency hides under the copy
+  const int64_t req = (a.mode == kChain) ? row / a.R : row;
+  const int32_t j = (a.mode == kChain) ? (int32_t)(row % a.R) : 0;
+  float T = 1.f;
+  if (a.mode != kRenorm && a.temperature) T = a.temperature[req];
+  if (a.mode == kChain && a.skip_greedy && !(T >= kGreedyT)) return;  // a streaming pass has it
+  const int32_t D = a.D;
+  const int32_t x = (a.mode == kChain && j < D) ? a.draft_tokens[req * D + j] : -1;
+  const bool xvalid = x >= 0 && (int64_t)x < a.V;
+  if (a.mode == kChain) {
+    if (tid == 0) {
+      const uint64_t seed = a.seed ? (uint64_t)a.seed[req] : 0;
+      const uint64_t off = a.offset ? (uint64_t)a.offset[req] : 0;
+      ctl->uj = (j < D) ? (a.uniforms ? a.uniforms[req * a.R + j] : verify_coin(seed, off, (uint32_t)j))
+                        : 0.f;
+      ctl->uD = a.uniforms ? a.uniforms[req * a.R + D] : verify_coin(seed, off, (uint32_t)D);
+      ctl->tok = -1;
+    }
+    if (tid == 32) {
+      ctl->vx = !xvalid ? 0.f
+                        : (sizeof(E) == 2 ? bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(xr)[x])
+                                          : reinterpret_cast<const float*>(xr)[x]);
+    }
+  }
+
   // ---- 1. stage the slice ----------------------------------------------------------
   if (tid == 0) {
     ctl->round = 0;
     ctl->gcount = 0;
   }
-  for (int i = tid; i < kNBins; i += kThreads) (&ctl->mass[0][0])[i] = 0;
+  for (int i = tid; i < 3 * kNBins; i += kThreads) (&ctl->m3[0][0][0])[i] = 0;
   if (vec) {
     const int64_t bulk = (n * (int64_t)sizeof(E)) & ~(int64_t)15;
     const int64_t cb = ((bulk / kChunks) + 15) & ~(int64_t)15;
@@ -516,11 +656,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
   const int32_t am = ctl->am;
 
   // ---- 3. knobs ------------------------------------------------------------------------
-  const int64_t req = (a.mode == kChain) ? row / a.R : row;
-  const int32_t j = (a.mode == kChain) ? (int32_t)(row % a.R) : 0;
-  float T = 1.f, tp = 1.f;
+  float tp = 1.f;
   int32_t k = 0;
-  if (a.mode != kRenorm && a.temperature) T = a.temperature[req];
   if (a.mode != kSoftmax) {
     if (a.top_k) k = a.top_k[req];
     if (a.top_p) tp = a.top_p[req];
@@ -556,42 +693,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
   uint64_t C = 0;
   uint64_t Zk = 0;
 
-  // Walking gbuf[0..cnt) in descending order from a mass `base`: the first index whose
-  // inclusive mass reaches `target` (cnt if none), and the inclusive mass there (the
-  // total if none).
-  auto crossing = [&](int cnt, uint64_t base, uint64_t target, uint64_t& incl_at) -> int {
-    const int per = (cnt + kThreads - 1) / kThreads;
-    const int r0 = min(cnt, tid * per), r1 = min(cnt, r0 + per);
-    uint64_t s = 0;
-    for (int i = r0; i < r1; ++i) s += wfn(key_to_f32((uint32_t)(gbuf[i] >> kIdxBits)));
-    uint64_t tot;
-    const uint64_t ex = block_excl_scan_u64(s, ctl, tot);
-    if (tid == 0) {
-      ctl->found = cnt;
-      ctl->aux = base + tot;
-    }
-    __syncthreads();
-    if (base + ex < target && base + ex + s >= target) {
-      uint64_t acc = base + ex;
-      for (int i = r0; i < r1; ++i) {
-        acc += wfn(key_to_f32((uint32_t)(gbuf[i] >> kIdxBits)));
-        if (acc >= target) {
-          ctl->found = i;
-          ctl->aux = acc;
-          break;
-        }
-      }
-    } else if (tid == 0 && base >= target && cnt > 0) {
-      ctl->found = 0;  // reached before the first element: the first element crosses
-      ctl->aux = base + wfn(key_to_f32((uint32_t)(gbuf[0] >> kIdxBits)));
-    }
-    __syncthreads();
-    const int f = ctl->found;
-    incl_at = ctl->aux;
-    __syncthreads();
-    return f;
-  };
-
   // Every CTA appends its candidates to CTA 0's list; after a cluster barrier CTA 0 sorts
   // them, finds the threshold and writes it to every CTA; a second barrier publishes it.
   uint32_t* g0count = cluster.map_shared_rank(&ctl->gcount, 0);
@@ -600,37 +701,41 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
     const uint32_t pos = atomicAdd(g0count, 1u);
     if (pos < (uint32_t)kGatherCap) g0buf[pos] = cp;
   };
-  // topk: the first k candidates are the top-k set, then top-p inside it; else the
-  // candidates are one weight bucket whose ordered mass starts at `base` and must reach P
+  // topk: the k largest candidates, then top-p inside them; else the candidates are one
+  // weight bucket whose ordered mass starts at `base` and must reach P
+  const int cs_f[7] = {48, 40, 32, 24, 16, 8, 0};
+  const int cs_h[5] = {48, 40, 16, 8, 0};
+  const int* cs = bf16 ? cs_h : cs_f;
+  const int ncs = bf16 ? 5 : 7;
+  auto wcomp = [&](uint64_t c) -> uint64_t { return wfn(key_to_f32((uint32_t)(c >> kIdxBits))); };
+  // the exact mass of the candidates >= c0
+  auto mass_from = [&](int cnt, uint64_t c0) -> uint64_t {
+    uint64_t s = 0;
+    for (int i = tid; i < cnt; i += kThreads)
+      if (gbuf[i] >= c0) s += wcomp(gbuf[i]);
+    uint64_t tot;
+    (void)block_excl_scan_u64(s, ctl, tot);
+    return tot;
+  };
   auto select_and_broadcast = [&](bool topk, uint64_t base, uint64_t P) {
     if (crank == 0) {
       const uint32_t total = ctl->gcount;
       const bool ok = total <= (uint32_t)kGatherCap && total > 0 && (!topk || total >= (uint32_t)k);
       uint64_t Cb = 0, Zb = 0;
       if (ok) {
-        const int n2 = next_pow2(max((int)total, 2));
-        for (int i = (int)total + tid; i < n2; i += kThreads) gbuf[i] = 0ull;
-        __syncthreads();
-        bitonic_sort(gbuf, n2, [](uint64_t p, uint64_t q) { return p > q; });
-        uint64_t incl = 0;
+        const int cnt = (int)total;
         if (topk) {
-          int nk = k;
-          (void)crossing(k, 0, ~0ull, Zb);  // the exact mass of the top-k set
+          Cb = cta_radix<false>(gbuf, cnt, 0, (uint64_t)k, wcomp, cs, ncs, ctl);
+          Zb = mass_from(cnt, Cb);
           if (tpa) {
             const double want = ceil((double)tp * (double)Zb);
             const uint64_t Pk = (want > (double)Zb) ? Zb : (uint64_t)want;
-            const int f = crossing(k, 0, Pk, incl);
-            if (f < k) {
-              nk = f + 1;
-              Zb = incl;
-            }
+            Cb = cta_radix<true>(gbuf, cnt, Cb, Pk, wcomp, cs, ncs, ctl);
+            Zb = mass_from(cnt, Cb);
           }
-          Cb = gbuf[nk - 1];
         } else {
-          int f = crossing((int)total, base, P, incl);
-          if (f >= (int)total) f = (int)total - 1;  // the bucket holds the crossing
-          Cb = gbuf[f];
-          Zb = incl;
+          Cb = cta_radix<true>(gbuf, cnt, 0, P - base, wcomp, cs, ncs, ctl);
+          Zb = base + mass_from(cnt, Cb);
         }
       }
       if (tid < (int)CL) {
@@ -673,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
     } else if (!tk) {
       // ---- 4b. top-p over the whole row: bucket histogram, then the crossing bucket ------
       uint64_t tail = 0;
-      unsigned long long* hist = &ctl->mass[0][0];
+      uint32_t* h3 = &ctl->m3[0][0][0];  // [3][kNBins]
       for (int64_t vi = tid; vi < nvec; vi += kThreads) {
         float xv[NV];
         SV<E>::vec(sv, vi * NV, xv);
@@ -682,17 +787,21 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
           const uint64_t w = wfn(xv[q]);
           if (w == 0) continue;
           const int b = bin512(xv[q]);
-          if (b < kNBins - 1) atomicAdd(&hist[b], (unsigned long long)w);
-          else tail += w;
+          if (b < kHistBins) add3(h3 + b, h3 + kNBins + b, h3 + 2 * kNBins + b, w);
+          else tail += w;  // lighter than 2^-24 of the maximum: the tail bucket
         }
       }
       tail = warp_sum_u64(tail);
-      if ((tid & 31) == 0 && tail) atomicAdd(&hist[kNBins - 1], (unsigned long long)tail);
+      if ((tid & 31) == 0 && tail)
+        add3(h3 + kNBins - 1, h3 + 2 * kNBins - 1, h3 + 3 * kNBins - 1, tail);
       __syncthreads();
       cluster.sync();  // (2) bucket histograms are visible
       // every CTA: the cluster histogram (one bucket per thread), the total, the crossing
       uint64_t hb = 0;
-      for (uint32_t c = 0; c < CL; ++c) hb += cluster.map_shared_rank(&ctl->mass[0][0], c)[tid];
+      for (uint32_t c = 0; c < CL; ++c) {
+        const uint32_t* ph = cluster.map_shared_rank(&ctl->m3[0][0][0], c);
+        hb += get3(ph[tid], ph[kNBins + tid], ph[2 * kNBins + tid]);
+      }
       uint64_t Zt;
       const uint64_t ex = block_excl_scan_u64(hb, ctl, Zt);  // heaviest bucket first
       const double want = ceil((double)tp * (double)Zt);
@@ -714,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
         Zk = wfn(vam);
         cluster.sync();  // (3) every branch here passes the same barriers
         cluster.sync();  // (4)
-      } else if (bstar < 0 || bstar == kNBins - 1) {
+      } else if (bstar < 0 || bstar >= kHistBins) {
         fast = false;  // the crossing lies in the tail bucket: general path
         cluster.sync();  // (3)
         cluster.sync();  // (4)
@@ -847,19 +956,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
   }
 
   // ---- 6b. chain: the accept test of this row's draft and this row's speculative draw ---
-  const int32_t D = a.D;
-  const int32_t x = (j < D) ? a.draft_tokens[req * D + j] : -1;
-  const bool xvalid = x >= 0 && (int64_t)x < a.V;
-  if (tid == 0) {
-    const uint64_t seed = a.seed ? (uint64_t)a.seed[req] : 0;
-    const uint64_t off = a.offset ? (uint64_t)a.offset[req] : 0;
-    ctl->red_f[0][0] =
-        (j < D) ? (a.uniforms ? a.uniforms[req * a.R + j] : verify_coin(seed, off, (uint32_t)j)) : 0.f;
-    ctl->red_f[1][0] = a.uniforms ? a.uniforms[req * a.R + D] : verify_coin(seed, off, (uint32_t)D);
-    ctl->tok = -1;
-  }
-  __syncthreads();
-  const float uj = ctl->red_f[0][0], uD = ctl->red_f[1][0];
+  const float uj = ctl->uj, uD = ctl->uD;
   int32_t acc = 0, tok = am;
   if (greedy) {
     acc = (j < D) && (x == am);
@@ -867,33 +964,88 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
     // the draft token's weight
     uint64_t wx = 0;
     if (xvalid) {
-      const float vx = (sizeof(E) == 2) ? bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(xr)[x])
-                                         : reinterpret_cast<const float*>(xr)[x];
+      const float vx = ctl->vx;
       if (kept(comp_key(fkey(vx), (uint32_t)x), vx)) wx = wfn(vx);
     }
-    {
+    if (fast && tk) {
+      // the kept set is CTA 0's candidate list (>= C): CTA 0 draws from it, walking token
+      // ids in order through a radix selection on the id digits
+      if (crank == 0) {
+        const int cnt = (int)ctl->gcount;
+        const uint64_t Zf = Zk;  // the kept mass, the draft token included if kept
+        if (j < D) acc = ((double)uj * (double)Zf < (double)wx) ? 1 : 0;
+        const uint64_t Zr = Zf - wx;
+        if (Zr == 0) {
+          tok = (wx > 0) ? x : am;  // all the mass sits on the draft token
+        } else {
+          uint64_t t = (uint64_t)((double)uD * (double)Zr);
+          if (t >= Zr) t = Zr - 1;  // rounding: the last token with mass
+          auto wnx = [&](uint64_t c) -> uint64_t {
+            return ((int32_t)comp_idx(c) == x) ? 0ull : wcomp(c);
+          };
+          const int idx_sh[3] = {16, 8, 0};
+          uint64_t g = 0;
+          (void)cta_radix<true>(gbuf, cnt, C, t + 1, wnx, idx_sh, 3, ctl, &g);
+          tok = (int32_t)comp_idx(g);
+        }
+      }
+    } else {
       // token-id order over the slice: contiguous per-thread ranges of whole vectors
       const int64_t per = (nvec + kThreads - 1) / kThreads;
       const int64_t v0 = min(nvec, (int64_t)tid * per), v1 = min(nvec, v0 + per);
-      auto wsum = [&](float v, int64_t gi) -> float {
+      const uint32_t ckey = (uint32_t)(C >> kIdxBits);
+      const bool pretest = fast && C != 0;
+      // the weight of element gi under a kept predicate (0 for the draft token)
+      auto wsum = [&](auto&& keptf, float v, int64_t gi) -> float {
         if (gi == (int64_t)x) return 0.f;
-        if (!kept(comp_key(fkey(v), (uint32_t)gi), v)) return 0.f;
+        if (!keptf(comp_key(fkey(v), (uint32_t)gi), v)) return 0.f;
         return efn(v);
       };
-      const uint32_t ckey = (uint32_t)(C >> kIdxBits);
-      float s = 0.f;
-      for (int64_t vi = v0; vi < v1; ++vi) {
-        float xv[NV];
-        SV<E>::vec(sv, vi * NV, xv);
-        if (fast && C) {
-          float vm = xv[0];
+      auto kfast = [&](uint64_t key, float) -> bool { return key >= C; };
+      // the fp32 mass of this thread's range, in token-id order
+      auto range_sum = [&](auto&& keptf) -> float {
+        float acc_s = 0.f;
+        for (int64_t vi = v0; vi < v1; ++vi) {
+          float xv[NV];
+          SV<E>::vec(sv, vi * NV, xv);
+          if (pretest) {
+            float vm = xv[0];
 #pragma unroll
-          for (int q = 1; q < NV; ++q) vm = fmaxf(vm, xv[q]);
-          if (fkey(vm) < ckey) continue;  // no element of the vector is kept
+            for (int q = 1; q < NV; ++q) vm = fmaxf(vm, xv[q]);
+            if (fkey(vm) < ckey) continue;  // no element of the vector is kept
+          }
+#pragma unroll
+          for (int q = 0; q < NV; ++q) acc_s += wsum(keptf, xv[q], lo + vi * NV + q);
         }
+        return acc_s;
+      };
+      // the first element of this thread's range at which the running mass exceeds tf
+      auto range_find = [&](auto&& keptf, float tf) -> int32_t {
+        float accf = 0.f;
+        int32_t found = -1, lastk = -1;
+        for (int64_t vi = v0; vi < v1 && found < 0; ++vi) {
+          float xv[NV];
+          SV<E>::vec(sv, vi * NV, xv);
+          if (pretest) {
+            float vm = xv[0];
 #pragma unroll
-        for (int q = 0; q < NV; ++q) s += wsum(xv[q], lo + vi * NV + q);
-      }
+            for (int q = 1; q < NV; ++q) vm = fmaxf(vm, xv[q]);
+            if (fkey(vm) < ckey) continue;
+          }
+          for (int q = 0; q < NV; ++q) {
+            const float w = wsum(keptf, xv[q], lo + vi * NV + q);
+            if (w == 0.f) continue;
+            lastk = (int32_t)(lo + vi * NV + q);
+            accf += w;
+            if (accf > tf) {
+              found = lastk;
+              break;
+            }
+          }
+        }
+        return found >= 0 ? found : lastk;
+      };
+      const float s = fast ? range_sum(kfast) : range_sum(kept);
       const uint64_t sfx = fixw(s);
       uint64_t ctot;
       const uint64_t texcl = block_excl_scan_u64(sfx, ctl, ctot);
@@ -920,29 +1072,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
           const bool hit = past ? (sfx > 0 && texcl + sfx == ctot) : (texcl <= tl && tl < texcl + sfx);
           if (hit) {
             const float tf = past ? INFINITY : (float)(tl - texcl) * (1.0f / kFx);
-            float accf = 0.f;
-            int32_t found = -1, lastk = -1;
-            for (int64_t vi = v0; vi < v1 && found < 0; ++vi) {
-              float xv[NV];
-              SV<E>::vec(sv, vi * NV, xv);
-              if (fast && C) {
-                float vm = xv[0];
-#pragma unroll
-                for (int q = 1; q < NV; ++q) vm = fmaxf(vm, xv[q]);
-                if (fkey(vm) < ckey) continue;
-              }
-              for (int q = 0; q < NV; ++q) {
-                const float w = wsum(xv[q], lo + vi * NV + q);
-                if (w == 0.f) continue;
-                lastk = (int32_t)(lo + vi * NV + q);
-                accf += w;
-                if (accf > tf) {
-                  found = lastk;
-                  break;
-                }
-              }
-            }
-            if (found < 0) found = lastk;
+            const int32_t found = fast ? range_find(kfast, tf) : range_find(kept, tf);
             *cluster.map_shared_rank(&ctl->tok, 0) = found;
           }
         }

@@ -83,6 +83,7 @@ template <typename E, bool GUMBEL>
 __global__ void __launch_bounds__(kStreamThreads) k_rowstat(RowStatArgs a) {
   constexpr int N = Vec<E>::N;
   const int64_t row = blockIdx.x / a.splits;
+  if (!GUMBEL && a.req_temperature && a.req_temperature[row / (a.D + 1)] >= kGreedyT) return;
   const int split = (int)(blockIdx.x % a.splits);
   const int64_t lo = (int64_t)split * a.split_len;
   const int64_t hi = min(a.V, lo + a.split_len);
