@@ -101,6 +101,7 @@ size_t workspace_layout(int64_t batch, int32_t R, void* base, Workspace* ws) {
   w.part = reinterpret_cast<Part*>(take(rows * kMaxSplits * sizeof(Part)));
   w.rowres = reinterpret_cast<RowRes*>(take(rows * sizeof(RowRes)));
   w.dpart = reinterpret_cast<DrawPart*>(take((size_t)batch * kMaxSplits * sizeof(DrawPart)));
+  w.cmass = reinterpret_cast<uint64_t*>(take(rows * 8 * sizeof(uint64_t)));
   w.bytes = off;
   if (ws) *ws = w;
   return off;

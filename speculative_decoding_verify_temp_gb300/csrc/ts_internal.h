@@ -41,6 +41,7 @@ struct Workspace {
   Part* part;         // [rows * kMaxSplits]
   RowRes* rowres;     // [rows]
   DrawPart* dpart;    // [batch * kMaxSplits]
+  uint64_t* cmass;    // [rows * 8] per-CTA masses of a cluster-staged row
   size_t bytes;
 };
 

@@ -717,11 +717,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
     (void)block_excl_scan_u64(s, ctl, tot);
     return tot;
   };
-  auto select_and_broadcast = [&](bool topk, uint64_t base, uint64_t P) {
-    if (crank == 0) {
+  // CTA 0: the threshold and the kept mass from its candidate list
+  auto select_local = [&](bool topk, uint64_t base, uint64_t P, bool& ok, uint64_t& Cb,
+                          uint64_t& Zb) {
       const uint32_t total = ctl->gcount;
-      const bool ok = total <= (uint32_t)kGatherCap && total > 0 && (!topk || total >= (uint32_t)k);
-      uint64_t Cb = 0, Zb = 0;
+      ok = total <= (uint32_t)kGatherCap && total > 0 && (!topk || total >= (uint32_t)k);
+      Cb = 0;
+      Zb = 0;
       if (ok) {
         const int cnt = (int)total;
         if (topk) {
@@ -738,6 +740,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
           Zb = base + mass_from(cnt, Cb);
         }
       }
+  };
+  auto select_and_broadcast = [&](bool topk, uint64_t base, uint64_t P) {
+    if (crank == 0) {
+      bool ok;
+      uint64_t Cb, Zb;
+      select_local(topk, base, P, ok, Cb, Zb);
       if (tid < (int)CL) {
         RowCtl* pc = cluster.map_shared_rank(ctl, (uint32_t)tid);
         pc->b_ok = ok ? 1 : 0;
@@ -774,7 +782,21 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
       }
       __syncthreads();
       cluster.sync();  // (2) the candidates are in CTA 0
-      select_and_broadcast(true, 0, 0);  // (3)
+      if (a.mode == kChain) {
+        // CTA 0 selects and draws alone; the other CTAs are done (nothing reads their
+        // shared memory any more) unless the list overflowed
+        const uint32_t total0 = *g0count;
+        if (!(total0 > 0 && total0 <= (uint32_t)kGatherCap && total0 >= (uint32_t)k)) {
+          fast = false;
+        } else if (crank != 0) {
+          return;
+        } else {
+          bool ok;
+          select_local(true, 0, 0, ok, C, Zk);
+        }
+      } else {
+        select_and_broadcast(true, 0, 0);  // (3)
+      }
     } else if (!tk) {
       // ---- 4b. top-p over the whole row: bucket histogram, then the crossing bucket ------
       uint64_t tail = 0;
@@ -956,10 +978,47 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
   }
 
   // ---- 6b. chain: the accept test of this row's draft and this row's speculative draw ---
+  // One thread records the row; the last row of a request to be recorded writes the chain.
+  auto finish_row = [&](int32_t tok_f, int32_t acc_f) {
+    a.ws.rowres[row] = RowRes{M, am, ctl->S1, tok_f, acc_f, {0, 0, 0}};
+    __threadfence();
+    const uint32_t prev = atomicAdd(&a.ws.reqcnt[req], 1u);
+    if (prev != (uint32_t)a.R - 1) return;
+    __threadfence();
+    a.ws.reqcnt[req] = 0;
+    int32_t js = D;
+    for (int32_t jj = 0; jj < D; ++jj)
+      if (!__ldcg(&a.ws.rowres[req * a.R + jj].acc)) {
+        js = jj;
+        break;
+      }
+    for (int32_t jj = 0; jj < a.R; ++jj) {
+      const int64_t rj = req * a.R + jj;
+      int32_t t = -1;
+      if (jj < js) t = a.draft_tokens[req * D + jj];
+      else if (jj == js) t = __ldcg(&a.ws.rowres[rj].tok);
+      a.accepted_tokens[rj] = t;
+      if (a.accept_index) a.accept_index[rj] = (jj <= js) ? (int32_t)rj : -1;
+      if (a.logprobs) {
+        float lp = 0.f;
+        if (jj <= js && t >= 0 && (int64_t)t < a.V) {
+          const E* xj = reinterpret_cast<const E*>(a.x) + rj * a.ld;
+          const float vt = (sizeof(E) == 2) ? bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(xj)[t])
+                                             : reinterpret_cast<const float*>(xj)[t];
+          lp = (vt - __ldcg(&a.ws.rowres[rj].M)) - logf(__ldcg(&a.ws.rowres[rj].S));
+        }
+        a.logprobs[rj] = lp;
+      }
+    }
+    a.accept_length[req] = js + 1;
+  };
   const float uj = ctl->uj, uD = ctl->uD;
   int32_t acc = 0, tok = am;
   if (greedy) {
     acc = (j < D) && (x == am);
+    cluster.sync();  // no CTA leaves while a peer may still read its statistics
+    if (crank == 0 && tid == 0) finish_row(tok, acc);
+    return;
   } else {
     // the draft token's weight
     uint64_t wx = 0;
@@ -988,7 +1047,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
           (void)cta_radix<true>(gbuf, cnt, C, t + 1, wnx, idx_sh, 3, ctl, &g);
           tok = (int32_t)comp_idx(g);
         }
+        if (tid == 0) finish_row(tok, acc);
       }
+      return;
     } else {
       // token-id order over the slice: contiguous per-thread ranges of whole vectors
       const int64_t per = (nvec + kThreads - 1) / kThreads;
@@ -1049,12 +1110,18 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
       const uint64_t sfx = fixw(s);
       uint64_t ctot;
       const uint64_t texcl = block_excl_scan_u64(sfx, ctl, ctot);
-      if (tid == 0) ctl->p_sum = ctot;
-      cluster.sync();  // CTA masses are visible
+      // CTA masses go through global memory, so that a CTA can leave without waiting for
+      // its peers to read its shared memory
+      uint64_t* cm = a.ws.cmass + row * 8;
+      if (tid == 0) {
+        cm[crank] = ctot;
+        __threadfence();
+      }
+      cluster.sync();  // CTA masses are visible; past here no CTA reads another's smem
       uint64_t Zr = 0, cpre = 0;
       int last_nz = -1;
       for (uint32_t c = 0; c < CL; ++c) {
-        const uint64_t pc = cluster.map_shared_rank(ctl, c)->p_sum;
+        const uint64_t pc = __ldcg(cm + c);
         if (c < crank) cpre += pc;
         if (pc > 0) last_nz = (int)c;
         Zr += pc;
@@ -1062,60 +1129,25 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
       const uint64_t Zf = Zr + wx;
       if (j < D) acc = ((double)uj * (double)Zf < (double)wx) ? 1 : 0;
       if (Zr == 0) {
-        tok = (wx > 0) ? x : am;  // all the mass sits on the draft token
-      } else {
-        const uint64_t t = (uint64_t)((double)uD * (double)Zr);
-        const bool past = (t >= Zr);
-        const bool mine = past ? ((int)crank == last_nz) : (cpre <= t && t < cpre + ctot);
-        if (mine) {
-          const uint64_t tl = past ? 0 : t - cpre;
-          const bool hit = past ? (sfx > 0 && texcl + sfx == ctot) : (texcl <= tl && tl < texcl + sfx);
-          if (hit) {
-            const float tf = past ? INFINITY : (float)(tl - texcl) * (1.0f / kFx);
-            const int32_t found = fast ? range_find(kfast, tf) : range_find(kept, tf);
-            *cluster.map_shared_rank(&ctl->tok, 0) = found;
-          }
-        }
+        // all the mass sits on the draft token
+        if (crank == 0 && tid == 0) finish_row((wx > 0) ? x : am, acc);
+        return;
       }
+      const uint64_t t = (uint64_t)((double)uD * (double)Zr);
+      const bool past = (t >= Zr);
+      const bool mine = past ? ((int)crank == last_nz) : (cpre <= t && t < cpre + ctot);
+      if (!mine) return;
+      const uint64_t tl = past ? 0 : t - cpre;
+      const bool hit = past ? (sfx > 0 && texcl + sfx == ctot) : (texcl <= tl && tl < texcl + sfx);
+      if (hit) {
+        // the one thread whose range holds the target finishes the row
+        const float tf = past ? INFINITY : (float)(tl - texcl) * (1.0f / kFx);
+        const int32_t found = fast ? range_find(kfast, tf) : range_find(kept, tf);
+        finish_row(found, acc);
+      }
+      return;
     }
   }
-  cluster.sync();  // the drawn token has reached CTA 0
-  if (crank == 0 && tid == 0) {
-    if (!greedy && ctl->tok >= 0) tok = ctl->tok;
-    a.ws.rowres[row] = RowRes{M, am, ctl->S1, tok, acc, {0, 0, 0}};
-    __threadfence();
-    const uint32_t prev = atomicAdd(&a.ws.reqcnt[req], 1u);
-    if (prev == (uint32_t)a.R - 1) {
-      __threadfence();
-      a.ws.reqcnt[req] = 0;
-      int32_t js = D;
-      for (int32_t jj = 0; jj < D; ++jj)
-        if (!__ldcg(&a.ws.rowres[req * a.R + jj].acc)) {
-          js = jj;
-          break;
-        }
-      for (int32_t jj = 0; jj < a.R; ++jj) {
-        const int64_t rj = req * a.R + jj;
-        int32_t t = -1;
-        if (jj < js) t = a.draft_tokens[req * D + jj];
-        else if (jj == js) t = __ldcg(&a.ws.rowres[rj].tok);
-        a.accepted_tokens[rj] = t;
-        if (a.accept_index) a.accept_index[rj] = (jj <= js) ? (int32_t)rj : -1;
-        if (a.logprobs) {
-          float lp = 0.f;
-          if (jj <= js && t >= 0 && (int64_t)t < a.V) {
-            const E* xj = reinterpret_cast<const E*>(a.x) + rj * a.ld;
-            const float vt = (sizeof(E) == 2) ? bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(xj)[t])
-                                               : reinterpret_cast<const float*>(xj)[t];
-            lp = (vt - __ldcg(&a.ws.rowres[rj].M)) - logf(__ldcg(&a.ws.rowres[rj].S));
-          }
-          a.logprobs[rj] = lp;
-        }
-      }
-      a.accept_length[req] = js + 1;
-    }
-  }
-  cluster.sync();
 }
 
 static size_t extra_smem() {
