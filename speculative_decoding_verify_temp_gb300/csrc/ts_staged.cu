@@ -62,6 +62,8 @@ struct RowCtl {
   float p_ls;
   uint64_t p_sum;
   uint32_t gcount;  // CTA 0: candidates appended by the cluster
+  uint32_t lcnt;    // candidates collected by this CTA
+  uint32_t lbase;   // their place in CTA 0's list
   int32_t p_tok;
   int32_t b_ok;     // written by CTA 0: the selection result
   int32_t b_pad;
@@ -113,6 +115,10 @@ template <>
 struct SV<float> {
   static constexpr int N = 4;  // elements per 16-byte vector
   __device__ __forceinline__ static float get(const float* s, int64_t i) { return s[i]; }
+  __device__ __forceinline__ static float vmax(const float* s, int64_t i) {
+    const float4 r = *reinterpret_cast<const float4*>(s + i);
+    return fmaxf(fmaxf(r.x, r.y), fmaxf(r.z, r.w));
+  }
   __device__ __forceinline__ static void vec(const float* s, int64_t i, float* x) {
     const float4 r = *reinterpret_cast<const float4*>(s + i);
     x[0] = r.x;
@@ -126,6 +132,17 @@ struct SV<uint16_t> {
   static constexpr int N = 8;
   __device__ __forceinline__ static float get(const uint16_t* s, int64_t i) {
     return bf16_bits_to_f32(s[i]);
+  }
+  // the largest of 8 bf16 values with packed bf16x2 maxima
+  __device__ __forceinline__ static uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+  __device__ __forceinline__ static float vmax(const uint16_t* s, int64_t i) {
+    const uint4 r = *reinterpret_cast<const uint4*>(s + i);
+    const uint32_t m = bmax2(bmax2(r.x, r.y), bmax2(r.z, r.w));
+    return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
   }
   __device__ __forceinline__ static void vec(const uint16_t* s, int64_t i, float* x) {
     const uint4 r = *reinterpret_cast<const uint4*>(s + i);
@@ -524,6 +541,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
   if (tid == 0) {
     ctl->round = 0;
     ctl->gcount = 0;
+    ctl->lcnt = 0;
   }
   for (int i = tid; i < 3 * kNBins; i += kThreads) (&ctl->m3[0][0][0])[i] = 0;
   if (vec) {
@@ -573,12 +591,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
   float bv = -INFINITY, lm = -INFINITY, ls = 0.f, lc = 0.f;
   int32_t bi = INT32_MAX;
   for (int64_t vi = tid; vi < nvec; vi += kThreads) {
-    float x[NV];
-    SV<E>::vec(sv, vi * NV, x);
-    float vm = x[0];
-#pragma unroll
-    for (int q = 1; q < NV; ++q) vm = fmaxf(vm, x[q]);
+    const float vm = SV<E>::vmax(sv, vi * NV);
     if (vm > bv || bi == INT32_MAX) {
+      float x[NV];
+      SV<E>::vec(sv, vi * NV, x);
       for (int q = 0; q < NV; ++q)
         if (x[q] == vm) {
           bi = (int32_t)(lo + vi * NV + q);
@@ -587,6 +603,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
       bv = vm;
     }
     if (want_lse && vm > -INFINITY) {
+      float x[NV];
+      SV<E>::vec(sv, vi * NV, x);
       const float nm = fmaxf(lm, vm);
       const float f = ex2((lm - nm) * kLog2e);
       ls *= f;
@@ -695,11 +713,26 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
 
   // Every CTA appends its candidates to CTA 0's list; after a cluster barrier CTA 0 sorts
   // them, finds the threshold and writes it to every CTA; a second barrier publishes it.
+  // Candidates are first collected in this CTA (in the space of the gathered thread
+  // maxima, free by then), then copied to CTA 0 in one block after one reservation.
   uint32_t* g0count = cluster.map_shared_rank(&ctl->gcount, 0);
   uint64_t* g0buf = cluster.map_shared_rank(gbuf, 0);
+  uint64_t* llist = reinterpret_cast<uint64_t*>(tmall);
+  constexpr int kLocalCap = kMaxCluster * kThreads / 2;
   auto append = [&](uint64_t cp) {
-    const uint32_t pos = atomicAdd(g0count, 1u);
-    if (pos < (uint32_t)kGatherCap) g0buf[pos] = cp;
+    const uint32_t pos = atomicAdd(&ctl->lcnt, 1u);
+    if (pos < (uint32_t)kLocalCap) llist[pos] = cp;
+  };
+  auto ship = [&]() {  // after a __syncthreads that follows the appends
+    if (tid == 0) {
+      const uint32_t nl = ctl->lcnt;
+      // an overflowing list reserves past the capacity, so CTA 0 sees the overflow
+      ctl->lbase = atomicAdd(g0count, nl > (uint32_t)kLocalCap ? (uint32_t)kGatherCap + 1u : nl);
+    }
+    __syncthreads();
+    const uint32_t nl = min(ctl->lcnt, (uint32_t)kLocalCap), base = ctl->lbase;
+    for (uint32_t i = tid; i < nl; i += kThreads)
+      if (base + i < (uint32_t)kGatherCap) g0buf[base + i] = llist[i];
   };
   // topk: the k largest candidates, then top-p inside them; else the candidates are one
   // weight bucket whose ordered mass starts at `base` and must reach P
@@ -767,12 +800,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
       __syncthreads();
       const uint32_t tkey = cta_select_bound(tmall, (int)CL * kThreads, (uint32_t)k, bf16 ? 2 : 4, ctl);
       for (int64_t vi = tid; vi < nvec; vi += kThreads) {
+        if (fkey(SV<E>::vmax(sv, vi * NV)) < tkey) continue;
         float xv[NV];
         SV<E>::vec(sv, vi * NV, xv);
-        float vm = xv[0];
-#pragma unroll
-        for (int q = 1; q < NV; ++q) vm = fmaxf(vm, xv[q]);
-        if (fkey(vm) < tkey) continue;
         for (int q = 0; q < NV; ++q) {
           const int64_t li = vi * NV + q;
           if (li >= n) break;
@@ -780,6 +810,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
           if (kq >= tkey) append(comp_key(kq, (uint32_t)(lo + li)));
         }
       }
+      __syncthreads();
+      ship();
       __syncthreads();
       cluster.sync();  // (2) the candidates are in CTA 0
       if (a.mode == kChain) {
@@ -851,12 +883,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
         cluster.sync();  // (4)
       } else {
         for (int64_t vi = tid; vi < nvec; vi += kThreads) {
+          if (bin512(SV<E>::vmax(sv, vi * NV)) > bstar) continue;  // even its heaviest is lighter
           float xv[NV];
           SV<E>::vec(sv, vi * NV, xv);
-          float vm = xv[0];
-#pragma unroll
-          for (int q = 1; q < NV; ++q) vm = fmaxf(vm, xv[q]);
-          if (bin512(vm) > bstar) continue;  // even the heaviest element is lighter
           for (int q = 0; q < NV; ++q) {
             const int64_t li = vi * NV + q;
             if (li >= n) break;
@@ -864,6 +893,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
             append(comp_key(fkey(xv[q]), (uint32_t)(lo + li)));
           }
         }
+        __syncthreads();
+        ship();
         __syncthreads();
         cluster.sync();  // (3) the candidates are in CTA 0
         select_and_broadcast(false, acc0, P);  // (4)
@@ -1063,18 +1094,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
         return efn(v);
       };
       auto kfast = [&](uint64_t key, float) -> bool { return key >= C; };
+      auto kall = [](uint64_t, float) -> bool { return true; };
       // the fp32 mass of this thread's range, in token-id order
       auto range_sum = [&](auto&& keptf) -> float {
         float acc_s = 0.f;
         for (int64_t vi = v0; vi < v1; ++vi) {
+          // no element of the vector is kept if even its largest is below the threshold
+          if (pretest && fkey(SV<E>::vmax(sv, vi * NV)) < ckey) continue;
           float xv[NV];
           SV<E>::vec(sv, vi * NV, xv);
-          if (pretest) {
-            float vm = xv[0];
-#pragma unroll
-            for (int q = 1; q < NV; ++q) vm = fmaxf(vm, xv[q]);
-            if (fkey(vm) < ckey) continue;  // no element of the vector is kept
-          }
 #pragma unroll
           for (int q = 0; q < NV; ++q) acc_s += wsum(keptf, xv[q], lo + vi * NV + q);
         }
@@ -1085,14 +1113,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
         float accf = 0.f;
         int32_t found = -1, lastk = -1;
         for (int64_t vi = v0; vi < v1 && found < 0; ++vi) {
+          if (pretest && fkey(SV<E>::vmax(sv, vi * NV)) < ckey) continue;
           float xv[NV];
           SV<E>::vec(sv, vi * NV, xv);
-          if (pretest) {
-            float vm = xv[0];
-#pragma unroll
-            for (int q = 1; q < NV; ++q) vm = fmaxf(vm, xv[q]);
-            if (fkey(vm) < ckey) continue;
-          }
           for (int q = 0; q < NV; ++q) {
             const float w = wsum(keptf, xv[q], lo + vi * NV + q);
             if (w == 0.f) continue;
@@ -1106,7 +1129,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
         }
         return found >= 0 ? found : lastk;
       };
-      const float s = fast ? range_sum(kfast) : range_sum(kept);
+      const float s = fast ? (C ? range_sum(kfast) : range_sum(kall)) : range_sum(kept);
       const uint64_t sfx = fixw(s);
       uint64_t ctot;
       const uint64_t texcl = block_excl_scan_u64(sfx, ctl, ctot);
@@ -1142,7 +1165,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
       if (hit) {
         // the one thread whose range holds the target finishes the row
         const float tf = past ? INFINITY : (float)(tl - texcl) * (1.0f / kFx);
-        const int32_t found = fast ? range_find(kfast, tf) : range_find(kept, tf);
+        const int32_t found =
+            fast ? (C ? range_find(kfast, tf) : range_find(kall, tf)) : range_find(kept, tf);
         finish_row(found, acc);
       }
       return;
