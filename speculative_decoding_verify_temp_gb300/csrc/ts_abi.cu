@@ -1,6 +1,6 @@
 // The C ABI of libtsverify.so: argument validation, workspace carve-up, launch geometry
 // and dispatch to the kernels. Host code only; every step of the computation runs in
-// the kernels of ts_stream.cu and ts_staged.cu.
+// the kernels of ts_stream.cu, ts_sample.cu and ts_staged.cu.
 #include <stdarg.h>
 #include <stdio.h>
 
@@ -67,8 +67,9 @@ ts_status check_dtype(int dt) {
   return TS_OK;
 }
 
-ts_status take_workspace(int64_t batch, int32_t R, void* ws, size_t ws_bytes, tsv::Workspace* out) {
-  const size_t need = tsv::workspace_layout(batch, R, ws, out);
+ts_status take_workspace(int64_t batch, int32_t R, int64_t vocab, void* ws, size_t ws_bytes,
+                         tsv::Workspace* out) {
+  const size_t need = tsv::workspace_layout(batch, R, vocab, ws, out);
   if (ws == nullptr) return fail(TS_ERR_INVALID_ARG, "workspace is NULL (need %zu bytes)", need);
   if (reinterpret_cast<uintptr_t>(ws) % 256 != 0)
     return fail(TS_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
@@ -87,7 +88,7 @@ ts_status launched(cudaError_t e, const char* what) {
 
 namespace tsv {
 
-size_t workspace_layout(int64_t batch, int32_t R, void* base, Workspace* ws) {
+size_t workspace_layout(int64_t batch, int32_t R, int64_t vocab, void* base, Workspace* ws) {
   const size_t rows = (size_t)batch * (size_t)R;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -102,6 +103,17 @@ size_t workspace_layout(int64_t batch, int32_t R, void* base, Workspace* ws) {
   w.rowres = reinterpret_cast<RowRes*>(take(rows * sizeof(RowRes)));
   w.dpart = reinterpret_cast<DrawPart*>(take((size_t)batch * kMaxSplits * sizeof(DrawPart)));
   w.cmass = reinterpret_cast<uint64_t*>(take(rows * 8 * sizeof(uint64_t)));
+  w.flag = reinterpret_cast<uint32_t*>(take(rows * 4));
+  w.ccount = reinterpret_cast<uint32_t*>(take(rows * 4));
+  if (vocab > 0) {
+    // sized for fp32 rows, which have the most chunks (at most kMaxSplits)
+    int64_t chunk = 0;
+    int32_t splits = 0;
+    (void)sample_splits(vocab, 4, &splits, &chunk);
+    w.cand_splits = splits;
+    w.cand = reinterpret_cast<uint64_t*>(
+        take(rows * (size_t)splits * (size_t)kSTopK * sizeof(uint64_t)));
+  }
   w.bytes = off;
   if (ws) *ws = w;
   return off;
@@ -114,7 +126,8 @@ extern "C" {
 size_t ts_workspace_size(int64_t batch, int32_t rows_per_req, int64_t vocab) {
   (void)vocab;
   if (batch < 1 || rows_per_req < 1) return 0;
-  return tsv::workspace_layout(batch, rows_per_req, nullptr, nullptr);
+  if (vocab < 1 || vocab > TS_MAX_VOCAB) return 0;
+  return tsv::workspace_layout(batch, rows_per_req, vocab, nullptr, nullptr);
 }
 
 ts_status ts_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t stream) {
@@ -198,7 +211,7 @@ ts_status ts_verify_chain_greedy(const void* target_logits, ts_dtype dt, int64_t
   if (!target_logits || !accepted_tokens || !accept_length || (D > 0 && !draft_tokens))
     return fail(TS_ERR_INVALID_ARG, "target_logits, draft_tokens, accepted_tokens and accept_length are required");
   tsv::RowStatArgs a{};
-  if ((st = take_workspace(batch, D + 1, workspace, ws_bytes, &a.ws)) != TS_OK) return st;
+  if ((st = take_workspace(batch, D + 1, vocab, workspace, ws_bytes, &a.ws)) != TS_OK) return st;
   a.x = target_logits;
   a.ld = ld;
   a.V = vocab;
@@ -234,7 +247,7 @@ ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t
     if (p->target_dtype != TS_F32)
       return fail(TS_ERR_UNSUPPORTED_DTYPE, "probability targets must be fp32");
     tsv::DrawArgs a{};
-    if ((st = take_workspace(p->batch, R, workspace, ws_bytes, &a.ws)) != TS_OK) return st;
+    if ((st = take_workspace(p->batch, R, p->vocab, workspace, ws_bytes, &a.ws)) != TS_OK) return st;
     a.p = static_cast<const float*>(p->target);
     a.ld = p->ld;
     a.V = p->vocab;
@@ -261,7 +274,7 @@ ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t
     return fail(TS_ERR_INVALID_ARG, "vocab %lld above the staged limit %d", (long long)p->vocab,
                 tsv::staged_max_vocab(p->target_dtype == TS_BF16));
   tsv::StagedArgs a{};
-  if ((st = take_workspace(p->batch, R, workspace, ws_bytes, &a.ws)) != TS_OK) return st;
+  if ((st = take_workspace(p->batch, R, p->vocab, workspace, ws_bytes, &a.ws)) != TS_OK) return st;
   a.mode = tsv::kChain;
   a.x = p->target;
   a.bf16 = (p->target_dtype == TS_BF16);
@@ -281,7 +294,35 @@ ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t
   a.accept_length = p->accept_length;
   a.accept_index = p->accept_index;
   a.logprobs = p->logprobs;
-  if (p->temperature) {
+  const int esize = p->target_dtype == TS_BF16 ? 2 : 4;
+  tsv::SampleArgs sa{};
+  if (aligned16(p->target, p->ld, esize) &&
+      tsv::sample_splits(p->vocab, esize, &sa.splits, &sa.chunk) && sa.splits <= a.ws.cand_splits) {
+    // Every row: the split-row kernels, then the staged kernel for the rows they flag
+    // (top_k above their limit, candidate overflow, a top-p crossing in the tail).
+    sa.x = p->target;
+    sa.bf16 = a.bf16;
+    sa.ld = p->ld;
+    sa.V = p->vocab;
+    sa.rows = a.rows;
+    sa.R = R;
+    sa.D = p->D;
+    sa.temperature = p->temperature;
+    sa.top_k = p->top_k;
+    sa.top_p = p->top_p;
+    sa.draft_tokens = p->draft_tokens;
+    sa.seed = p->seed;
+    sa.offset = p->offset;
+    sa.uniforms = p->uniforms;
+    sa.accepted_tokens = p->accepted_tokens;
+    sa.accept_length = p->accept_length;
+    sa.accept_index = p->accept_index;
+    sa.logprobs = p->logprobs;
+    sa.ws = a.ws;
+    cudaError_t e = tsv::launch_sample(sa, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "split-row sampling launch");
+    a.flags = a.ws.flag;
+  } else if (p->temperature) {
     // Greedy requests need only the argmax of each row: a streaming pass handles them,
     // and the staged kernel skips them.
     tsv::RowStatArgs g{};
@@ -291,7 +332,7 @@ ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t
     g.V = p->vocab;
     g.rows = a.rows;
     choose_splits(g.rows, p->vocab, 2048, &g.splits, &g.split_len);
-    g.vec = aligned16(p->target, p->ld, p->target_dtype == TS_BF16 ? 2 : 4);
+    g.vec = aligned16(p->target, p->ld, esize);
     g.want_lse = p->logprobs != nullptr;
     g.kind = 0;
     g.D = p->D;
@@ -321,7 +362,7 @@ ts_status ts_gumbel_max_sample(const void* logits, ts_dtype dt, int64_t batch,
   if (!logits || !temperature || !seed || !offset || !tokens_out)
     return fail(TS_ERR_INVALID_ARG, "logits, temperature, seed, offset and tokens_out are required");
   tsv::RowStatArgs a{};
-  if ((st = take_workspace(batch, n_per_req, workspace, ws_bytes, &a.ws)) != TS_OK) return st;
+  if ((st = take_workspace(batch, n_per_req, vocab, workspace, ws_bytes, &a.ws)) != TS_OK) return st;
   a.x = logits;
   a.ld = ld;
   a.V = vocab;
@@ -351,7 +392,7 @@ ts_status ts_gather_logprobs(const void* x, ts_dtype dt, int32_t is_probs, int64
                     "logprobs launch");
   }
   tsv::RowStatArgs a{};
-  if ((st = take_workspace(rows, 1, workspace, ws_bytes, &a.ws)) != TS_OK) return st;
+  if ((st = take_workspace(rows, 1, vocab, workspace, ws_bytes, &a.ws)) != TS_OK) return st;
   a.x = x;
   a.ld = ld;
   a.V = vocab;
@@ -427,13 +468,13 @@ extern "C" ts_status ts_verify_chain_greedy_static(const void* target_logits, ts
     return fail(TS_ERR_INVALID_ARG,
                 "batch*(D+1) = %lld rows exceeds the static scratch limit of %d rows",
                 (long long)rows, TS_STATIC_MAX_ROWS);
-  if (tsv::workspace_layout(batch, D + 1, nullptr, nullptr) > kStaticScratchBytes)
+  if (tsv::workspace_layout(batch, D + 1, 0, nullptr, nullptr) > kStaticScratchBytes)
     return fail(TS_ERR_INVALID_ARG, "the call needs more than the %zu-byte static scratch",
                 kStaticScratchBytes);
   void* base = nullptr;
   if ((st = static_scratch(&base)) != TS_OK) return st;
   tsv::RowStatArgs a{};
-  tsv::workspace_layout(batch, D + 1, base, &a.ws);
+  tsv::workspace_layout(batch, D + 1, 0, base, &a.ws);
   // The array keeps whatever the previous call left; the arrival counters must start at 0.
   cudaError_t e = cudaMemsetAsync(a.ws.rowcnt, 0, (size_t)rows * sizeof(uint32_t), stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(a.ws.reqcnt, 0, (size_t)batch * sizeof(uint32_t), stream);

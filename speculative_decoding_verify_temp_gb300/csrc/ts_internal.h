@@ -8,6 +8,20 @@
 namespace tsv {
 
 constexpr int kMaxSplits = 64;  // row splits of the streaming kernels
+constexpr int kSTopK = 1024;  // largest top_k the split-row sampling kernels serve
+constexpr int kSVecs = 8;     // 16-byte vectors per thread of a chunk (kept in registers)
+constexpr int kSThreads = 256;
+
+// Chunks of a row of V elements of `esize` bytes for the split-row sampling kernels:
+// 256 threads x 8 vectors = 32 KB each. Returns false if a row needs more than
+// kMaxSplits chunks.
+inline bool sample_splits(int64_t V, int esize, int32_t* splits, int64_t* chunk) {
+  const int64_t c = (int64_t)kSThreads * kSVecs * (16 / esize);
+  *chunk = c;
+  const int64_t s = (V + c - 1) / c;
+  *splits = (int32_t)(s < kMaxSplits ? s : kMaxSplits);
+  return s <= kMaxSplits;
+}
 
 // Per-(row, split) partial of the streaming row statistics: argmax (v, i) and the
 // log-sum-exp state s * exp(m) of the raw row.
@@ -42,10 +56,16 @@ struct Workspace {
   RowRes* rowres;     // [rows]
   DrawPart* dpart;    // [batch * kMaxSplits]
   uint64_t* cmass;    // [rows * 8] per-CTA masses of a cluster-staged row
+  uint32_t* flag;     // [rows] rows the split-row sampling kernel leaves to the staged one
+  uint32_t* ccount;   // [rows] candidates collected for a row
+  uint64_t* cand;     // [rows * cand_splits * kSTopK] per-row summaries of the split-row
+                      // kernel (vocab > 0 only)
+  int64_t cand_splits;
   size_t bytes;
 };
 
-size_t workspace_layout(int64_t batch, int32_t R, void* base, Workspace* ws);
+// vocab = 0 lays out no candidate lists.
+size_t workspace_layout(int64_t batch, int32_t R, int64_t vocab, void* base, Workspace* ws);
 
 // ---- streaming kernels (ts_stream.cu) ------------------------------------------
 
@@ -106,6 +126,35 @@ cudaError_t launch_draw_probs(const DrawArgs& a, cudaStream_t s);
 cudaError_t launch_logprobs_probs(const float* p, int64_t ld, int64_t V, int64_t rows,
                                   const int32_t* tokens, float* out, cudaStream_t s);
 
+// ---- split-row sampling kernel (ts_sample.cu) -----------------------------------
+
+// Target-only chain sampling from logits: a chunk kernel that summarises every chunk of
+// every row, then a kernel that finishes every row from the summaries. Rows they cannot
+// serve get ws.flag set and are finished by the cluster-staged kernel afterwards.
+// Requires 16-byte aligned rows.
+struct SampleArgs {
+  const void* x;
+  int32_t bf16;
+  int64_t ld, V, rows;
+  int32_t R, D;
+  int32_t splits;
+  int64_t chunk;  // elements per chunk
+  const float* temperature;  // per request
+  const int32_t* top_k;
+  const float* top_p;
+  const int32_t* draft_tokens;
+  const int64_t* seed;
+  const int64_t* offset;
+  const float* uniforms;
+  int32_t* accepted_tokens;
+  int32_t* accept_length;
+  int32_t* accept_index;
+  float* logprobs;
+  Workspace ws;
+};
+
+cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s);
+
 // ---- cluster-staged row kernels (ts_staged.cu) -----------------------------------
 
 enum StagedMode { kSoftmax = 0, kRenorm = 1, kChain = 2 };
@@ -130,6 +179,7 @@ struct StagedArgs {
   int32_t* accept_index;
   float* logprobs;
   int32_t skip_greedy;  // chain: greedy requests are handled by the streaming kernel
+  uint32_t* flags;      // chain: if set, only rows with flags[row] != 0 (cleared here)
   Workspace ws;
 };
 

@@ -240,6 +240,45 @@ def test_target_only_from_logits(B, D, V, dtype):
     compare_chain(g, ref, dtype, max_boundary_frac=0.05)
 
 
+@pytest.mark.parametrize("pad,dtype", [(8, "bf16"), (3, "bf16"), (4, "f32"), (1, "f32")])
+def test_target_only_mixed_routes_and_strides(pad, dtype):
+    # One launch mixes greedy requests, small and large top-k (above the split-row
+    # kernel's limit: the staged kernel finishes those rows), top-p alone, knobs off and
+    # rows with only a few finite logits; rows are `pad` elements longer than the
+    # vocabulary, so with pad 3 (bf16) or 1 (f32) they are not 16-byte aligned.
+    rng = np.random.default_rng(1000 + pad)
+    B, D, V = 30, 3, 50000
+    R = D + 1
+    x = rng.standard_normal((B * R, V), dtype=np.float32) * np.float32(3.0)
+    x += synth.zipf_bias(V)[None, :]
+    x[5 * R:6 * R] = -np.inf
+    x[5 * R:6 * R, 7:17] = rng.standard_normal((R, 10)).astype(np.float32)
+    x[6 * R:7 * R, 1000:] = -np.inf
+    if dtype == "bf16":
+        x = synth.f32_from_bf16_bits(synth.bf16_bits_from_f32(x))
+    T = rng.choice(np.array([0.0, 0.5, 1.3], np.float32), B)
+    k = rng.choice(np.array([0, 5, 1000, 2000, V + 1], np.int32), B).astype(np.int32)
+    tp = rng.choice(np.array([1.0, 0.9, 0.0], np.float32), B).astype(np.float32)
+    T[5:7] = 1.0
+    k[5:7] = (1000, 50)
+    lg = x.reshape(B, R, V)[:, :D]
+    drafts = np.where(rng.random((B, D)) < 0.6, lg.argmax(-1),
+                      rng.integers(0, V, (B, D))).astype(np.int32)
+    seed = synth.request_seeds(B)
+    off = np.arange(B, dtype=np.int64)
+    full = np.zeros((B * R, V + pad), np.float32)
+    full[:, :V] = x
+    t = torch.from_numpy(full).cuda()
+    if dtype == "bf16":
+        t = t.to(torch.bfloat16)
+    g = tv.chain_spec_sampling(t[:, :V], True, D, dev(drafts), temperature=dev(T),
+                               top_k=dev(k), top_p=dev(tp), seed=dev(seed), offset=dev(off),
+                               logprobs=True)
+    ref = oracle.chain_spec_sampling(x, True, D, drafts, temperature=T, top_k=k, top_p=tp,
+                                     seed=seed, offset=off)
+    compare_chain(g, ref, dtype)
+
+
 def test_target_only_explicit_uniforms_and_knobs_off():
     rng = np.random.default_rng(77)
     B, D, V = 40, 3, 5000
