@@ -24,9 +24,10 @@
  *  - Ties: the argmax and top-k keep the lowest token id among equal values.
  *  - Workspace: calls that need scratch take `workspace`/`ws_bytes`, a caller-owned
  *    device buffer of at least ts_workspace_size(...) bytes that must be zero-filled
- *    once before its first use (ts_workspace_init does that). Every call leaves it
- *    zero again, so it can be reused by later calls on the same stream without
- *    clearing. Calls that overlap on the GPU must not share a workspace.
+ *    once before its first use (ts_workspace_init does that). Every call leaves the
+ *    counters it keeps there at zero again (the rest is scratch), so it can be reused
+ *    by later calls on the same stream without clearing. Calls that overlap on the GPU
+ *    must not share a workspace.
  *  - Errors: arguments are validated on the host before any launch; an invalid call
  *    returns TS_ERR_INVALID_ARG / TS_ERR_UNSUPPORTED_DTYPE and enqueues nothing. A
  *    failed launch returns TS_ERR_CUDA. ts_last_error_message() (thread-local) gives

@@ -105,6 +105,7 @@ size_t workspace_layout(int64_t batch, int32_t R, int64_t vocab, void* base, Wor
   w.cmass = reinterpret_cast<uint64_t*>(take(rows * 8 * sizeof(uint64_t)));
   w.flag = reinterpret_cast<uint32_t*>(take(rows * 4));
   w.ccount = reinterpret_cast<uint32_t*>(take(rows * 4));
+  w.work = reinterpret_cast<uint32_t*>(take(2 * 4));
   if (vocab > 0) {
     // sized for fp32 rows, which have the most chunks (at most kMaxSplits)
     int64_t chunk = 0;
@@ -141,7 +142,10 @@ ts_status ts_device_error(uint32_t* word_host, int clear) {
   if (!word_host) return fail(TS_ERR_INVALID_ARG, "word_host is NULL");
   uint32_t w = 0;
   cudaError_t e = tsv::staged_read_error(&w, clear);
+  uint32_t w2 = 0;
+  if (e == cudaSuccess) e = tsv::row_read_error(&w2, clear);
   if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  w |= w2 << 8;
   *word_host = w;
   if (w) return fail(TS_ERR_TIMEOUT, "a bounded device wait gave up (word 0x%x)", w);
   g_msg[0] = 0;
@@ -296,10 +300,9 @@ ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t
   a.logprobs = p->logprobs;
   const int esize = p->target_dtype == TS_BF16 ? 2 : 4;
   tsv::SampleArgs sa{};
-  if (aligned16(p->target, p->ld, esize) &&
+  if (aligned16(p->target, p->ld, esize) && p->vocab <= tsv::kRowMaxVocab &&
       tsv::sample_splits(p->vocab, esize, &sa.splits, &sa.chunk) && sa.splits <= a.ws.cand_splits) {
-    // Every row: the split-row kernels, then the staged kernel for the rows they flag
-    // (top_k above their limit, candidate overflow, a top-p crossing in the tail).
+    // Every row: the row-streaming kernel.
     sa.x = p->target;
     sa.bf16 = a.bf16;
     sa.ld = p->ld;
@@ -319,9 +322,7 @@ ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t
     sa.accept_index = p->accept_index;
     sa.logprobs = p->logprobs;
     sa.ws = a.ws;
-    cudaError_t e = tsv::launch_sample(sa, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "split-row sampling launch");
-    a.flags = a.ws.flag;
+    return launched(tsv::launch_sample(sa, stream), "row-streaming sampling launch");
   } else if (p->temperature) {
     // Greedy requests need only the argmax of each row: a streaming pass handles them,
     // and the staged kernel skips them.

@@ -58,6 +58,7 @@ struct Workspace {
   uint64_t* cmass;    // [rows * 8] per-CTA masses of a cluster-staged row
   uint32_t* flag;     // [rows] rows the split-row sampling kernel leaves to the staged one
   uint32_t* ccount;   // [rows] candidates collected for a row
+  uint32_t* work;     // [2] the row kernel's next-row counter and finished-CTA count
   uint64_t* cand;     // [rows * cand_splits * kSTopK] per-row summaries of the split-row
                       // kernel (vocab > 0 only)
   int64_t cand_splits;
@@ -128,10 +129,9 @@ cudaError_t launch_logprobs_probs(const float* p, int64_t ld, int64_t V, int64_t
 
 // ---- split-row sampling kernel (ts_sample.cu) -----------------------------------
 
-// Target-only chain sampling from logits: a chunk kernel that summarises every chunk of
-// every row, then a kernel that finishes every row from the summaries. Rows they cannot
-// serve get ws.flag set and are finished by the cluster-staged kernel afterwards.
-// Requires 16-byte aligned rows.
+// Target-only chain sampling from logits: a persistent row-streaming kernel that serves
+// every row (greedy ones included). Requires 16-byte aligned rows and vocab <=
+// kRowMaxVocab.
 struct SampleArgs {
   const void* x;
   int32_t bf16;
@@ -154,6 +154,8 @@ struct SampleArgs {
 };
 
 cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s);
+cudaError_t row_read_error(uint32_t* word, int clear);
+constexpr int64_t kRowMaxVocab = (int64_t)1 << 18;  // the row kernel's exact digit sums
 
 // ---- cluster-staged row kernels (ts_staged.cu) -----------------------------------
 

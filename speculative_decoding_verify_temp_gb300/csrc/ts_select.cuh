@@ -10,6 +10,15 @@
 namespace tsv {
 namespace sel {
 
+// Barrier policies: the whole CTA, or the 256 consumer threads of a warp-specialised CTA
+// (named barrier 1; the producer warp never takes part).
+struct BlockBar {
+  __device__ __forceinline__ static void sync() { __syncthreads(); }
+};
+struct ConsumerBar {
+  __device__ __forceinline__ static void sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+};
+
 // Scratch a CTA needs for one selection at a time.
 struct Scratch {
   uint32_t m3[3][256];  // per-bin mass as 14-, 14- and 13-bit digit sums
@@ -33,7 +42,7 @@ __device__ __forceinline__ uint64_t get3(uint32_t a0, uint32_t a1, uint32_t a2) 
 }
 
 // Exclusive scan of a u64 over the block, in thread order; writes the block total.
-template <int NT>
+template <int NT, class Bar = BlockBar>
 __device__ __forceinline__ uint64_t excl_scan(uint64_t v, Scratch& s, uint64_t& total) {
   constexpr int NW = NT / 32;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -44,7 +53,7 @@ __device__ __forceinline__ uint64_t excl_scan(uint64_t v, Scratch& s, uint64_t& 
     if (lane >= o) incl += y;
   }
   if (lane == 31) s.scan[w] = incl;
-  __syncthreads();
+  Bar::sync();
   if (w == 0) {
     uint64_t t = lane < NW ? s.scan[lane] : 0;
 #pragma unroll
@@ -54,10 +63,10 @@ __device__ __forceinline__ uint64_t excl_scan(uint64_t v, Scratch& s, uint64_t& 
     }
     if (lane < NW) s.scan[lane] = t;
   }
-  __syncthreads();
+  Bar::sync();
   const uint64_t before = (w > 0) ? s.scan[w - 1] : 0;
   total = s.scan[NW - 1];
-  __syncthreads();
+  Bar::sync();
   return before + incl - v;
 }
 
@@ -104,7 +113,7 @@ __device__ __forceinline__ void find_bin(Scratch& s, uint64_t above, uint64_t ta
 // selected iff it is >= the result. group_max receives the largest item of the final
 // digit group (the crossing item itself once the group holds one item); beyond is set
 // if the target lies past the eligible total (then every eligible item is selected).
-template <int NT, bool MASS, class Item, class WFn>
+template <int NT, bool MASS, class Bar = BlockBar, class Item, class WFn>
 __device__ uint64_t radix(int n, Item item, uint64_t lo_key, uint64_t target, WFn wfn,
                           const int* shifts, int nsh, Scratch& s, uint64_t* group_max = nullptr,
                           bool* beyond = nullptr) {
@@ -119,7 +128,7 @@ __device__ uint64_t radix(int n, Item item, uint64_t lo_key, uint64_t target, WF
       s.m3[2][i] = 0;
       s.cnt[i] = 0;
     }
-    __syncthreads();
+    Bar::sync();
     for (int i = tid; i < n; i += NT) {
       const uint64_t v = item(i);
       if (v >= lo_key && (v & mask) == prefix) {
@@ -128,18 +137,18 @@ __device__ uint64_t radix(int n, Item item, uint64_t lo_key, uint64_t target, WF
         if (MASS) add3(&s.m3[0][b], &s.m3[1][b], &s.m3[2][b], wfn(v));
       }
     }
-    __syncthreads();
+    Bar::sync();
     if (tid < 32) {
       if (MASS)
         find_bin(s, above, target, [&](int b) { return get3(s.m3[0][b], s.m3[1][b], s.m3[2][b]); });
       else
         find_bin(s, above, target, [&](int b) { return (unsigned long long)s.cnt[b]; });
     }
-    __syncthreads();
+    Bar::sync();
     const int bin = s.bin;
     const uint64_t ab = s.above;
     const int bc = s.bincnt;
-    __syncthreads();
+    Bar::sync();
     if (bin < 0) {
       all = true;
       break;
@@ -168,45 +177,124 @@ __device__ uint64_t radix(int n, Item item, uint64_t lo_key, uint64_t target, WF
     s.aux = ~0ull;
     s.gmax = 0;
   }
-  __syncthreads();
+  Bar::sync();
   if ((tid & 31) == 0) {
     atomicMin(reinterpret_cast<unsigned long long*>(&s.aux), mn);
     atomicMax(reinterpret_cast<unsigned long long*>(&s.gmax), gx);
   }
-  __syncthreads();
+  Bar::sync();
   const uint64_t r = s.aux;
   if (group_max) *group_max = s.gmax;
-  __syncthreads();
+  Bar::sync();
   return r;
 }
 
-// The largest C made of whole top digits of a 32-bit key such that at least k of the
-// items key(0..n) are >= C (0 if fewer than k items): a lower bound for the k-th largest.
-template <int NT, class Key>
+// AND and OR of the 32-bit values f(i) over i < n with pred(i), reduced over the block.
+template <int NT, class Bar, class F>
+__device__ __forceinline__ void block_and_or(int n, F f, Scratch& s, uint32_t& and_, uint32_t& or_) {
+  constexpr int NW = NT / 32;
+  uint32_t a = 0xFFFFFFFFu, o = 0u;
+  for (int i = threadIdx.x; i < n; i += NT) {
+    uint32_t v;
+    if (f(i, v)) {
+      a &= v;
+      o |= v;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    a &= __shfl_xor_sync(0xffffffffu, a, off);
+    o |= __shfl_xor_sync(0xffffffffu, o, off);
+  }
+  if ((threadIdx.x & 31) == 0) s.scan[threadIdx.x >> 5] = ((uint64_t)a << 32) | o;
+  Bar::sync();
+  a = 0xFFFFFFFFu;
+  o = 0u;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    a &= (uint32_t)(s.scan[w] >> 32);
+    o |= (uint32_t)s.scan[w];
+  }
+  Bar::sync();
+  and_ = a;
+  or_ = o;
+}
+
+// The largest C, made of the keys' common top bits and whole 8-bit digits below them down
+// to bit `lowbit`, such that at least k of the items key(0..n) are >= C (0 if fewer than
+// k items): a lower bound for the k-th largest. Digits start below the bits every key
+// shares, so that clustered keys still spread over the bins.
+template <int NT, class Bar = BlockBar, class Key>
 __device__ uint32_t select_bound(int n, Key key, uint32_t k, int ndig, Scratch& s) {
-  uint32_t prefix = 0, mask = 0;
-  uint64_t above = 0;
+  const int lowbit = 32 - 8 * ndig;
   const int tid = threadIdx.x;
-  for (int di = 0; di < ndig; ++di) {
-    const int sh = 24 - 8 * di;
+  if (n < (int)k || k == 0) return 0u;
+  uint32_t ka, ko;
+  block_and_or<NT, Bar>(n, [&](int i, uint32_t& v) { v = key(i); return true; }, s, ka, ko);
+  const uint32_t diff = ka ^ ko;
+  const uint32_t lowmask = (lowbit >= 32) ? 0xFFFFFFFFu : ((1u << lowbit) - 1u);
+  if ((diff & ~lowmask) == 0u) return ka & ~lowmask;  // every key the same above lowbit
+  const int h = 31 - __clz(diff & ~lowmask);
+  uint32_t mask = (h >= 31) ? 0u : ~((2u << h) - 1u);
+  uint32_t prefix = ka & mask;
+  uint64_t above = 0;
+  int sh = h - 7;
+  for (;;) {
+    if (sh < lowbit) sh = lowbit;
     for (int i = tid; i < 256; i += NT) s.cnt[i] = 0;
-    __syncthreads();
+    Bar::sync();
     for (int i = tid; i < n; i += NT) {
       const uint32_t v = key(i);
       if ((v & mask) == prefix) atomicAdd(&s.cnt[(v >> sh) & 255u], 1u);
     }
-    __syncthreads();
+    Bar::sync();
     if (tid < 32) find_bin(s, above, k, [&](int b) { return (unsigned long long)s.cnt[b]; });
-    __syncthreads();
+    Bar::sync();
     const int bin = s.bin;
     const uint64_t ab = s.above;
-    __syncthreads();
+    Bar::sync();
     if (bin < 0) return prefix;  // fewer than k items in the group: keep it whole
     prefix |= (uint32_t)bin << sh;
     mask |= 255u << sh;
     above = ab;
+    if (sh == lowbit) break;
+    sh -= 8;
   }
   return prefix;
+}
+
+// radix() over composite keys (32-bit value key << 24 | 24-bit reversed id) whose value
+// digits start below the bits that all eligible items share, down to value bit
+// `lowvbit` (16 when the values are widened bf16, whose low key bits follow from the
+// high ones), then the three id digits.
+template <int NT, bool MASS, class Bar = BlockBar, class Item, class WFn>
+__device__ uint64_t radix_adaptive(int n, Item item, uint64_t lo_key, uint64_t target, WFn wfn,
+                                   int lowvbit, Scratch& s, uint64_t* group_max = nullptr,
+                                   bool* beyond = nullptr) {
+  uint32_t ka, ko;
+  block_and_or<NT, Bar>(
+      n,
+      [&](int i, uint32_t& v) {
+        const uint64_t c = item(i);
+        v = (uint32_t)(c >> 24);
+        return c >= lo_key;
+      },
+      s, ka, ko);
+  int shifts[8];
+  int ns = 0;
+  const uint32_t lowmask = (1u << lowvbit) - 1u;
+  const uint32_t diff = (ka ^ ko) & ~lowmask;
+  if (ka <= ko && diff != 0u) {
+    const int h = 31 - __clz(diff);
+    for (int sh = h - 7;; sh -= 8) {
+      shifts[ns++] = 24 + (sh < lowvbit ? lowvbit : sh);
+      if (sh <= lowvbit) break;
+    }
+  }
+  shifts[ns++] = 16;
+  shifts[ns++] = 8;
+  shifts[ns++] = 0;
+  return radix<NT, MASS, Bar>(n, item, lo_key, target, wfn, shifts, ns, s, group_max, beyond);
 }
 
 }  // namespace sel
