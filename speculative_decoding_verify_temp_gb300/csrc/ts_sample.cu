@@ -45,6 +45,7 @@ constexpr int kRStageBytes = 16384;          // 1024 vectors of 16 bytes
 constexpr int kRStageVecs = kRStageBytes / 16;
 constexpr int kRVecs = kRStageVecs / kRCons;  // vectors per consumer thread and stage
 constexpr int kRListCap = 2048;              // the first part of the candidate space
+constexpr int kRSmallE = 4;                  // lists of up to 128 candidates: one warp
 constexpr int kRSoft = 3072;                 // top-k list size that triggers a compaction
 constexpr int kRBins = 2048;                 // top-p buckets (128 octaves)
 constexpr int kRHead = 1024;                 // buckets above the first stage's maximum
@@ -117,6 +118,59 @@ __device__ __forceinline__ float warp_sum_f32(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
+}
+
+// Ascending bitonic sort of the 32 E values of a warp, element e * 32 + lane in v[e].
+template <int E>
+__device__ __forceinline__ void warp_bitonic_asc(uint64_t (&v)[E]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int kb = 2; kb <= 32 * E; kb <<= 1) {
+#pragma unroll
+    for (int jb = kb >> 1; jb > 0; jb >>= 1) {
+      if (jb >= 32) {
+        const int jj = jb >> 5;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if (e & jj) continue;
+          const bool up = ((e * 32 + lane) & kb) == 0;
+          const uint64_t lo = v[e], hi = v[e ^ jj];
+          if (up ? (lo > hi) : (lo < hi)) {
+            v[e] = hi;
+            v[e ^ jj] = lo;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const bool up = ((e * 32 + lane) & kb) == 0;
+          const uint64_t pv = __shfl_xor_sync(0xffffffffu, v[e], jb);
+          const bool lower = (lane & jb) == 0;
+          v[e] = (lower == up) ? (v[e] < pv ? v[e] : pv) : (v[e] > pv ? v[e] : pv);
+        }
+      }
+    }
+  }
+}
+
+// Inclusive scan of the warp's 32 E values in element order (e * 32 + lane); returns the
+// total.
+template <int E>
+__device__ __forceinline__ uint64_t warp_scan_incl(uint64_t (&v)[E]) {
+  const int lane = threadIdx.x & 31;
+  uint64_t carry = 0;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    uint64_t x = v[e];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    v[e] = x + carry;
+    carry += __shfl_sync(0xffffffffu, x, 31);
+  }
+  return carry;
 }
 
 // Exclusive scan of a double over the consumer threads in thread order (a fixed order of
@@ -910,6 +964,83 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
       if (tid == 0) finish_row(am, (j < D && x == am) ? 1 : 0);
     } else if (bad || kn.kind == kRowStaged) {
       general();
+    } else if (kn.kind == kRowTopK && (int)sm.lcnt <= 32 * kRSmallE) {
+      // few candidates: one warp finishes the row (sorts in registers, scans by shuffles)
+      if (warp == 0) {
+        const int nl = (int)sm.lcnt;
+        uint64_t v[kRSmallE], w[kRSmallE];
+#pragma unroll
+        for (int e = 0; e < kRSmallE; ++e) {
+          const int i = e * 32 + lane;
+          v[e] = (i < nl) ? sm.w.cross[i] : 0ull;
+        }
+        warp_bitonic_asc(v);  // element i has descending rank 32 E - 1 - i
+#pragma unroll
+        for (int e = 0; e < kRSmallE; ++e) {
+          const int r = 32 * kRSmallE - 1 - (e * 32 + lane);
+          w[e] = (v[e] != 0ull && r < k) ? wcomp(v[e]) : 0ull;
+        }
+        uint64_t incl[kRSmallE];
+#pragma unroll
+        for (int e = 0; e < kRSmallE; ++e) incl[e] = w[e];
+        const uint64_t Zk = warp_scan_incl(incl);
+        // top-p within the top k: rank r kept iff r = 0 or the mass before it is below P
+        uint64_t P = Zk;
+        if (kn.tp < 1.f) {
+          const double want = ceil((double)kn.tp * (double)Zk);
+          P = (want > (double)Zk) ? Zk : (uint64_t)want;
+        }
+        uint64_t Z = 0, wx = 0;
+        bool kept[kRSmallE];
+#pragma unroll
+        for (int e = 0; e < kRSmallE; ++e) {
+          const int r = 32 * kRSmallE - 1 - (e * 32 + lane);
+          const uint64_t before = Zk - incl[e];
+          kept[e] = v[e] != 0ull && r < k && (r == 0 || before < P);
+          if (kept[e]) {
+            Z += w[e];
+            if ((int32_t)comp_token(v[e]) == x) wx = w[e];
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          Z += __shfl_xor_sync(0xffffffffu, Z, o);
+          wx += __shfl_xor_sync(0xffffffffu, wx, o);
+        }
+        const int32_t acc = (j < D) && ((double)uj * (double)Z < (double)wx) ? 1 : 0;
+        const uint64_t Zr = Z - wx;
+        int32_t tok = (wx > 0) ? x : am;
+        if (Zr > 0) {
+          uint64_t t = (uint64_t)((double)uD * (double)Zr);
+          if (t >= Zr) t = Zr - 1;
+          // the kept tokens in id order, the draft token without weight
+          uint64_t key2[kRSmallE], cw[kRSmallE];
+#pragma unroll
+          for (int e = 0; e < kRSmallE; ++e)
+            key2[e] = kept[e] ? (((uint64_t)comp_token(v[e]) << 32) | (uint32_t)(v[e] >> kIdxBits))
+                              : ~0ull;
+          warp_bitonic_asc(key2);
+#pragma unroll
+          for (int e = 0; e < kRSmallE; ++e)
+            cw[e] = (key2[e] != ~0ull && (int32_t)(key2[e] >> 32) != x)
+                        ? wfn(key_to_value((uint32_t)key2[e]))
+                        : 0ull;
+          (void)warp_scan_incl(cw);
+          // the first token whose inclusive prefix mass exceeds t
+          int32_t f = INT32_MAX;
+#pragma unroll
+          for (int e = 0; e < kRSmallE; ++e) {
+            const uint64_t wi = (key2[e] != ~0ull && (int32_t)(key2[e] >> 32) != x)
+                                    ? wfn(key_to_value((uint32_t)key2[e]))
+                                    : 0ull;
+            if (wi > 0 && cw[e] > t && cw[e] - wi <= t) f = (int32_t)(key2[e] >> 32);
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) f = min(f, __shfl_xor_sync(0xffffffffu, f, o));
+          if (f != INT32_MAX) tok = f;
+        }
+        if (lane == 0) finish_row(tok, acc);
+      }
     } else if (kn.kind == kRowTopK) {
       const int nl = (int)sm.lcnt;
       auto item = [&](int i) { return sm.w.cross[i]; };
