@@ -279,6 +279,39 @@ def test_target_only_mixed_routes_and_strides(pad, dtype):
     compare_chain(g, ref, dtype)
 
 
+@pytest.mark.parametrize("V,dtype", [(1, "f32"), (7, "bf16"), (9, "f32"), (4095, "f32"),
+                                     (8191, "bf16"), (8193, "bf16"), (16385, "f32"),
+                                     (24577, "bf16")])
+def test_target_only_vocab_edges(V, dtype):
+    # vocabularies around the row kernel's 16 KB stages, with a ragged last vector; rows are
+    # padded to 16 elements so that they stay 16-byte aligned (the row kernel's route)
+    rng = np.random.default_rng(V + 7)
+    B, D = 12, 3
+    R = D + 1
+    x = rng.standard_normal((B * R, V), dtype=np.float32) * np.float32(2.0)
+    if dtype == "bf16":
+        x = synth.f32_from_bf16_bits(synth.bf16_bits_from_f32(x))
+    T = rng.choice(np.array([0.0, 0.7, 1.3], np.float32), B).astype(np.float32)
+    k = rng.choice(np.array([0, 1, 5, 300, V + 1], np.int32), B).astype(np.int32)
+    tp = rng.choice(np.array([1.0, 0.9, 0.0], np.float32), B).astype(np.float32)
+    lg = x.reshape(B, R, V)[:, :D]
+    drafts = np.where(rng.random((B, D)) < 0.6, lg.argmax(-1),
+                      rng.integers(0, V, (B, D))).astype(np.int32)
+    seed = synth.request_seeds(B)
+    off = np.arange(B, dtype=np.int64)
+    ld = (V + 15) // 16 * 16
+    full = np.zeros((B * R, ld), np.float32)
+    full[:, :V] = x
+    t = torch.from_numpy(full).cuda()
+    if dtype == "bf16":
+        t = t.to(torch.bfloat16)
+    g = tv.chain_spec_sampling(t[:, :V], True, D, dev(drafts), temperature=dev(T),
+                               top_k=dev(k), top_p=dev(tp), seed=dev(seed), offset=dev(off))
+    ref = oracle.chain_spec_sampling(x, True, D, drafts, temperature=T, top_k=k, top_p=tp,
+                                     seed=seed, offset=off)
+    compare_chain(g, ref, dtype)
+
+
 def test_target_only_explicit_uniforms_and_knobs_off():
     rng = np.random.default_rng(77)
     B, D, V = 40, 3, 5000
