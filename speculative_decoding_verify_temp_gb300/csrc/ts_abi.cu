@@ -159,6 +159,10 @@ ts_status ts_softmax_temp(const void* logits, ts_dtype dt, int64_t rows, int64_t
   if ((st = check_dtype(dt)) != TS_OK) return st;
   if ((st = check_common(rows, vocab, ld)) != TS_OK) return st;
   if (!logits || !probs_out) return fail(TS_ERR_INVALID_ARG, "logits and probs_out are required");
+  if (aligned16(logits, ld, dt == TS_BF16 ? 2 : 4))
+    return launched(tsv::launch_softmax(logits, dt == TS_BF16, rows, ld, vocab, temperature,
+                                        probs_out, stream),
+                    "softmax launch");
   if (vocab > tsv::staged_max_vocab(dt == TS_BF16))
     return fail(TS_ERR_INVALID_ARG, "vocab %lld above the staged limit %d", (long long)vocab,
                 tsv::staged_max_vocab(dt == TS_BF16));
