@@ -188,6 +188,21 @@ ts_status ts_topk_topp_renorm(const float* probs, int64_t rows, int64_t vocab, i
   if (!probs || !probs_out) return fail(TS_ERR_INVALID_ARG, "probs and probs_out are required");
   if (probs_out == probs && ld != vocab)
     return fail(TS_ERR_INVALID_ARG, "in-place renorm needs ld == vocab");
+  if (aligned16(probs, ld, 4) && vocab <= tsv::kRowMaxVocab) {
+    // the row kernel in its renorm mode: rows streamed through shared memory, no workspace
+    tsv::SampleArgs sa{};
+    sa.x = probs;
+    sa.bf16 = 0;
+    sa.ld = ld;
+    sa.V = vocab;
+    sa.rows = rows;
+    sa.R = 1;
+    sa.D = 0;
+    sa.top_k = top_k;
+    sa.top_p = top_p;
+    sa.out = probs_out;
+    return launched(tsv::launch_renorm_rows(sa, stream), "row renorm launch");
+  }
   if (vocab > tsv::staged_max_vocab(0))
     return fail(TS_ERR_INVALID_ARG, "vocab %lld above the staged limit %d", (long long)vocab,
                 tsv::staged_max_vocab(0));

@@ -155,9 +155,12 @@ struct SampleArgs {
   int32_t* accept_index;
   float* logprobs;
   Workspace ws;
+  float* out;  // top-k/top-p renorm of probability rows: [rows, V] fp32 (no workspace)
 };
 
 cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s);
+// The row kernel in its renorm mode (fp32 probability rows, 16-byte aligned).
+cudaError_t launch_renorm_rows(const SampleArgs& a, cudaStream_t s);
 cudaError_t row_read_error(uint32_t* word, int clear);
 constexpr int64_t kRowMaxVocab = (int64_t)1 << 18;  // the row kernel's exact digit sums
 

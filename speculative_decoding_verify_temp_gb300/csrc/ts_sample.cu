@@ -203,6 +203,11 @@ __device__ __forceinline__ double excl_scan_f64(double v, double* sc, double& to
 
 // The absolute top-p bucket coordinate of a value: floor(x log2(e) / T * 16).
 __device__ __forceinline__ float babs(float v, float sl2) { return floorf(v * sl2 * 16.f); }
+// The upper edge of linear probability bucket b (b <= 2032: p <= 1): the float whose bits
+// are (b + 1) << 19.
+__device__ __forceinline__ float rn_edge(float b) {
+  return __uint_as_float(((uint32_t)b + 1u) << 19);
+}
 
 // Waits for the phase of `bar` with the given parity, giving up (and setting the error
 // word) after a bounded number of suspended polls.
@@ -265,7 +270,7 @@ struct RowSmem {
   double res_d;
 };
 
-template <typename E>
+template <typename E, bool RN>
 __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
   extern __shared__ __align__(128) unsigned char dsm[];
   constexpr int N = SVec<E>::N;
@@ -283,26 +288,35 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
     }
     fence_mbar_init();
   }
-  if (tid < 16) sm.tab[tid] = exp2(-(double)tid / 16.0);
+  if (tid < 16) {
+    sm.tab[tid] = exp2(-(double)tid / 16.0);
+  }
   __syncthreads();
 
   // ---- producer warp ------------------------------------------------------------------
   if (warp == kRWarps) {
     if (lane == 0) {
       uint32_t g = 0;
+      int64_t rr = blockIdx.x;
       for (;;) {
-        // rows are taken from a shared counter, so that CTAs with cheap rows take more; the
-        // counter runs over the rows twice, the costly kinds on the first round and the
-        // others on the second, so that no costly row is left for the end
-        const int64_t idx = (int64_t)atomicAdd(&a.ws.work[0], 1u);
-        const int64_t row = (idx < a.rows) ? idx : idx - a.rows;
-        if (idx < 2 * a.rows) {
-          const Knobs kq = row_knobs(a, row / a.R);
-          const bool costly = kq.kind == kRowTopP || kq.kind == kRowStaged ||
-                              (kq.kind == kRowTopK && kq.k > kRCons);
-          if (costly != (idx < a.rows)) continue;
+        int64_t row = -1;
+        if constexpr (RN) {  // renorm: rows in turn, no workspace
+          row = (rr < a.rows) ? rr : -1;
+          rr += gridDim.x;
+        } else {
+          // rows are taken from a shared counter, so that CTAs with cheap rows take more;
+          // the counter runs over the rows twice, the costly kinds on the first round and
+          // the others on the second, so that no costly row is left for the end
+          const int64_t idx = (int64_t)atomicAdd(&a.ws.work[0], 1u);
+          if (idx < 2 * a.rows) {
+            row = (idx < a.rows) ? idx : idx - a.rows;
+            const Knobs kq = row_knobs(a, row / a.R);
+            const bool costly = kq.kind == kRowTopP || kq.kind == kRowStaged ||
+                                (kq.kind == kRowTopK && kq.k > kRCons);
+            if (costly != (idx < a.rows)) continue;
+          }
         }
-        if (idx >= 2 * a.rows) {  // one last stage tells the consumers to stop
+        if (row < 0) {  // one last stage tells the consumers to stop
           const int slot = (int)(g % kRNSt);
           const uint32_t use = g / kRNSt;
           if (use > 0) bounded_wait(&sm.empty[slot], (use - 1) & 1u);
@@ -312,8 +326,9 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
         }
         const unsigned char* src =
             reinterpret_cast<const unsigned char*>(a.x) + row * a.ld * (int64_t)sizeof(E);
-        // top-p rows are streamed twice: the histogram, then the kept masses
-        const int npass = (row_knobs(a, row / a.R).kind == kRowTopP) ? 2 : 1;
+        // top-p rows are streamed twice (the histogram, then the kept masses); renorm rows
+        // once more to write the output
+        const int npass = ((row_knobs(a, row / a.R).kind == kRowTopP) ? 2 : 1) + (RN ? 1 : 0);
         for (int cc = 0; cc < npass * nst; ++cc, ++g) {
           const int c = cc % nst;
           const int slot = (int)(g % kRNSt);
@@ -393,7 +408,25 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
     const bool xvalid = x >= 0 && (int64_t)x < V;
     const float sl2 = (kn.kind == kRowGreedy) ? 0.f : __fdiv_rn(kLog2e, kn.T);
     const int32_t k = kn.k;
-    uint64_t* const rowslots = a.ws.cand + row * a.ws.cand_splits * (int64_t)kSTopK;
+    // top-p buckets, whether an element has weight, and its weight relative to the upper
+    // edge of its bucket b. Logits: b = floor(16 log2 w) of w = e^(x/T). Probabilities:
+    // the exponent and leading 4 mantissa bits of p (16 linear buckets an octave; the
+    // float's bits order them exactly)
+    auto live = [&](float v) -> bool {
+      if constexpr (RN) return v > 0.f;
+      else return v != -INFINITY;
+    };
+    auto bucket_of = [&](float v) -> float {
+      if constexpr (RN) return (float)(__float_as_uint(fminf(v, 1.f)) >> 19);
+      else return babs(v, sl2);
+    };
+    auto edge_w = [&](float v, float b) -> float {
+      if constexpr (RN) return __fdividef(fminf(v, 1.f), rn_edge(b));
+      else return ex2(fmaf(v, sl2, -(b + 1.f) * 0.0625f));
+    };
+    uint64_t* const rowslots =
+        RN ? nullptr : a.ws.cand + row * a.ws.cand_splits * (int64_t)kSTopK;
+    uint64_t zsum = 0;  // renorm rows without knobs: the row's exact mass
     if (tid == 0) {
       sm.lcnt = 0;
       sm.bad = 0;
@@ -490,6 +523,15 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
               ++pos;
             }
         }
+      } else if (RN && kn.kind == kRowPlain) {
+        // renorm without knobs: the row's exact mass
+#pragma unroll
+        for (int u = 0; u < kRVecs; ++u) {
+          float xv[N];
+          SVec<E>::unpack(vec_at(vbase + u * 32), xv);
+#pragma unroll
+          for (int q = 0; q < N; ++q) zsum += fixw(fminf(fmaxf(xv[q], 0.f), 1.f));
+        }
       } else if (kn.kind == kRowPlain) {
         // warp w's 128 vectors of the stage: their mass relative to their own maximum, the
         // draft token left out
@@ -525,8 +567,8 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
           if (tid == 0) {
             float mm = sm.redf[0][0];
             for (int w = 1; w < kRWarps; ++w) mm = fmaxf(mm, sm.redf[0][w]);
-            sm.base = (mm > -INFINITY) ? babs(mm, sl2) + (float)kRHead : 0.f;
-            if (!(mm > -INFINITY)) sm.bad = 1;
+            sm.base = live(mm) ? bucket_of(mm) + (float)kRHead : 0.f;
+            if (!live(mm)) sm.bad = 1;
           }
           cbar();
         }
@@ -534,14 +576,14 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
         bool out = false;
 #pragma unroll
         for (int u = 0; u < kRVecs; ++u) {
-          if (!(vmv[u] > -INFINITY)) continue;
+          if (!live(vmv[u])) continue;
           float xv[N];
           SVec<E>::unpack(vec_at(vbase + u * 32), xv);
 #pragma unroll
           for (int q = 0; q < N; ++q) {
             const float v = xv[q];
-            if (v == -INFINITY) continue;
-            const float b = babs(v, sl2);
+            if (!live(v)) continue;
+            const float b = bucket_of(v);
             const float idx = base - b;
             if (idx < 0.f) {
               out = true;  // above the window
@@ -549,7 +591,7 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
             }
             if (idx >= (float)kRBins) continue;  // below 2^-64 of the maximum: negligible
             // the weight relative to its bucket's upper edge, in (2^-1/16, 1], 25 bits
-            const uint32_t r = __float2uint_rz(ex2(fmaf(v, sl2, -(b + 1.f) * 0.0625f)) * 33554432.f);
+            const uint32_t r = __float2uint_rz(edge_w(v, b) * 33554432.f);
             const int ib = (int)idx;
             atomicAdd(&sm.w.t.u.h2[0][ib], r & 0x1FFFu);
             atomicAdd(&sm.w.t.u.h2[1][ib], r >> 13);
@@ -664,7 +706,10 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
     const int32_t am = sm.am;
     const float uj = sm.uj, uD = sm.uD, vx = sm.vx;
     const bool bad = sm.bad != 0;
-    auto wfn = [&](float v) -> uint64_t { return fixw(ex2((v - M) * sl2)); };
+    auto wfn = [&](float v) -> uint64_t {
+      if constexpr (RN) return fixw(fminf(fmaxf(v, 0.f), 1.f));
+      else return fixw(ex2((v - M) * sl2));
+    };
     auto wcomp = [&](uint64_t cc) -> uint64_t {
       return wfn(key_to_value((uint32_t)(cc >> kIdxBits)));
     };
@@ -763,7 +808,7 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
     // kSTopK, candidate overflow, a maximum above the bucket window, a crossing bucket too
     // large): radix selections over the whole row, read again from memory for every
     // digit, in the order top-k, top-p within it, then the draw in token-id order.
-    auto general = [&]() {
+    auto general_select = [&](uint64_t& Cout, uint64_t& Zout) {
       const int n = (int)V;
       auto gitem = [&](int i) -> uint64_t {
         return comp_key(fkey(SVec<E>::at(xr, i)), (uint32_t)i);
@@ -790,6 +835,16 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
         C = sel::radix_adaptive<kRCons, true, sel::ConsumerBar>(n, gitem, C, P, wcomp, lowv, sm.sc);
         Z = gmass(C);
       }
+      Cout = C;
+      Zout = Z;
+    };
+    auto general = [&]() {
+      const int n = (int)V;
+      auto gitem = [&](int i) -> uint64_t {
+        return comp_key(fkey(SVec<E>::at(xr, i)), (uint32_t)i);
+      };
+      uint64_t C, Z;
+      general_select(C, Z);
       uint64_t wx = 0;
       if (xvalid && comp_key(fkey(vx), (uint32_t)x) >= C) wx = wfn(vx);
       const int32_t acc = (j < D) && ((double)uj * (double)Z < (double)wx) ? 1 : 0;
@@ -812,7 +867,175 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
     };
 
     // ---- finish the row -----------------------------------------------------------------
-    if (kn.kind == kRowTopP) {
+    if constexpr (RN) {
+      // renorm: the kept set (a threshold composite C, and for top-p rows the bucket rule)
+      // and its exact mass Z, then one more pass that writes max(p, 0) / Z or 0
+      uint64_t C = 0, Z = 0;
+      bool bucket_rule = false;
+      float fbk = 0.f;
+      const float base = sm.base;
+      if (kn.kind == kRowTopP) {
+        bool active = !bad && kn.tp > 0.f;
+        int bstar = -1;
+        double pre = 0.0, P = 0.0;
+        if (active) {
+          // mass of bucket i = (digit sums) 2^-25 (upper edge of bucket base - i)
+          double hm[kRBPT];
+          double hsum = 0.0;
+#pragma unroll
+          for (int q = 0; q < kRBPT; ++q) {
+            const int i = kRBPT * tid + q;
+            const uint64_t h = (uint64_t)sm.w.t.u.h2[0][i] + ((uint64_t)sm.w.t.u.h2[1][i] << 13);
+            hm[q] = h ? (double)h * (1.0 / 33554432.0) * (double)rn_edge(base - (float)i) : 0.0;
+            hsum += hm[q];
+          }
+          double Zt;
+          const double hex = excl_scan_f64(hsum, sm.dscan, Zt);
+          P = (double)kn.tp * Zt;
+          if (tid == 0) sm.owner = -1;
+          cbar();
+          double acc_b = hex;
+#pragma unroll
+          for (int q = 0; q < kRBPT; ++q) {
+            if (hm[q] > 0.0 && acc_b < P && P <= acc_b + hm[q]) {
+              sm.owner = kRBPT * tid + q;
+              sm.res_d = acc_b;
+            }
+            acc_b += hm[q];
+          }
+          cbar();
+          bstar = sm.owner;
+          pre = sm.res_d;
+          active = bstar >= 0;
+        }
+        if (tid == 0) sm.lcnt = 0;
+        cbar();
+        // the second pass: the exact mass above the crossing bucket, and its elements
+        const float fb = (float)bstar;
+        uint64_t zab = 0;
+        for (int c = 0; c < nst; ++c, ++g) {
+          const int slot = (int)(g % kRNSt);
+          bounded_wait(&sm.full[slot], (g / kRNSt) & 1u);
+          if (active) {
+            const uint4* sv = reinterpret_cast<const uint4*>(ring + slot * kRStageBytes);
+            const int64_t c0 = (int64_t)c * SE;
+            const int nc = (int)min((int64_t)SE, V - c0);
+            const int nvf = nc / N;
+#pragma unroll
+            for (int u = 0; u < kRVecs; ++u) {
+              const int vi = vbase + u * 32;
+              const uint4 r = stage_vec(sv, c0, nc, nvf, vi);
+              const float vm = SVec<E>::vmax(r);
+              if (!live(vm) || base - bucket_of(vm) > fb) continue;  // all lighter
+              float xv[N];
+              SVec<E>::unpack(r, xv);
+#pragma unroll
+              for (int q = 0; q < N; ++q) {
+                const float v = xv[q];
+                if (!live(v)) continue;
+                const float idx = base - bucket_of(v);
+                if (idx < fb) {
+                  zab += wfn(v);
+                } else if (idx == fb && wfn(v) > 0) {
+                  const uint32_t pos = atomicAdd(&sm.lcnt, 1u);
+                  if (pos < (uint32_t)kRCrossCap)
+                    sm.w.cross[pos] = comp_key(fkey(v), (uint32_t)(c0 + (int64_t)vi * N + q));
+                }
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.empty[slot]);
+        }
+        cbar();
+        const uint32_t cnt = sm.lcnt;
+        if (kn.tp <= 0.f) {  // only the argmax is kept
+          C = comp_key(fkey(M), (uint32_t)am);
+          Z = wfn(M);
+        } else if (!active || cnt > (uint32_t)kRCrossCap || cnt == 0) {
+          general_select(C, Z);
+        } else {
+          const double want = ceil((P - pre) * 1099511627776.0);
+          const uint64_t Pb = want < 1.0 ? 1ull : (uint64_t)want;
+          C = sel::radix_adaptive<kRCons, true, sel::ConsumerBar>(
+              (int)cnt, [&](int i) { return sm.w.cross[i]; }, 1ull, Pb, wcomp, lowv, sm.sc);
+          uint64_t mine = zab;
+          for (uint32_t i = tid; i < cnt; i += kRCons) {
+            const uint64_t cc = sm.w.cross[i];
+            if (cc >= C) mine += wcomp(cc);
+          }
+          (void)sel::excl_scan<kRCons, sel::ConsumerBar>(mine, sm.sc, Z);
+          bucket_rule = true;
+          fbk = fb;
+        }
+      } else if (bad || kn.kind == kRowStaged) {
+        general_select(C, Z);
+      } else if (kn.kind == kRowTopK) {
+        const int nl = (int)sm.lcnt;
+        auto item = [&](int i) { return sm.w.cross[i]; };
+        const uint64_t Ck = sel::radix_adaptive<kRCons, false, sel::ConsumerBar>(
+            nl, item, 1ull, (uint64_t)k, [](uint64_t) { return (uint64_t)1; }, lowv, sm.sc);
+        auto mass_from = [&](uint64_t c0) -> uint64_t {
+          uint64_t sum = 0;
+          for (int i = tid; i < nl; i += kRCons) {
+            const uint64_t cc = sm.w.cross[i];
+            if (cc >= c0) sum += wcomp(cc);
+          }
+          uint64_t tot;
+          (void)sel::excl_scan<kRCons, sel::ConsumerBar>(sum, sm.sc, tot);
+          return tot;
+        };
+        C = Ck;
+        Z = mass_from(Ck);
+        if (kn.tp < 1.f) {
+          const double want = ceil((double)kn.tp * (double)Z);
+          const uint64_t P = (want > (double)Z) ? Z : (uint64_t)want;
+          C = sel::radix_adaptive<kRCons, true, sel::ConsumerBar>(nl, item, Ck, P, wcomp, lowv, sm.sc);
+          Z = mass_from(C);
+        }
+      } else {  // no knobs: everything is kept
+        (void)sel::excl_scan<kRCons, sel::ConsumerBar>(zsum, sm.sc, Z);
+      }
+      // the write pass
+      const float scale = (Z > 0) ? __fdiv_rn(kFx, __ull2float_rn(Z)) : 0.f;
+      float* orow = a.out + row * V;
+      const bool vout = ((reinterpret_cast<uintptr_t>(orow) & 15) == 0);
+      for (int c = 0; c < nst; ++c, ++g) {
+        const int slot = (int)(g % kRNSt);
+        bounded_wait(&sm.full[slot], (g / kRNSt) & 1u);
+        const uint4* sv = reinterpret_cast<const uint4*>(ring + slot * kRStageBytes);
+        const int64_t c0 = (int64_t)c * SE;
+        const int nc = (int)min((int64_t)SE, V - c0);
+        const int nvf = nc / N;
+#pragma unroll
+        for (int u = 0; u < kRVecs; ++u) {
+          const int vi = vbase + u * 32;
+          if (vi * N >= nc) continue;
+          float xv[N], y[N];
+          SVec<E>::unpack(stage_vec(sv, c0, nc, nvf, vi), xv);
+#pragma unroll
+          for (int q = 0; q < N; ++q) {
+            const float v = xv[q];
+            const int64_t gi = c0 + (int64_t)vi * N + q;
+            bool kp = comp_key(fkey(v), (uint32_t)gi) >= C;
+            if (bucket_rule && live(v)) {
+              const float idx = base - bucket_of(v);
+              kp = idx < fbk || (idx == fbk && kp);
+            }
+            y[q] = kp ? fmaxf(v, 0.f) * scale : 0.f;
+          }
+          const int64_t e0 = c0 + (int64_t)vi * N;
+          if (vout && vi < nvf) {
+            __stcs(reinterpret_cast<float4*>(orow + e0), make_float4(y[0], y[1], y[2], y[3]));
+          } else {
+            for (int q = 0; q < N; ++q)
+              if (e0 + q < V) orow[e0 + q] = y[q];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[slot]);
+      }
+    } else if (kn.kind == kRowTopP) {
       // top-p alone: bucket masses (thread t holds buckets 8t .. 8t + 7), the crossing
       // bucket, then the second pass over the row
       const float base = sm.base;
@@ -1155,7 +1378,7 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
     cbar();  // the row's shared state is free for the next row
   }
   // the last CTA to finish leaves the row counter at zero for the next call
-  if (tid == 0) {
+  if (!RN && tid == 0) {
     __threadfence();
     if (atomicAdd(&a.ws.work[1], 1u) == gridDim.x - 1) {
       a.ws.work[0] = 0u;
@@ -1164,25 +1387,32 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
   }
 }
 
-cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s) {
+namespace {
+template <typename E, bool RN>
+cudaError_t launch_row_kernel(const SampleArgs& a, cudaStream_t s) {
   int dev = 0, nsm = 148;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const int64_t want = (int64_t)nsm * 2;
+  const int64_t want = (int64_t)nsm * 2;  // two CTAs an SM
   const unsigned grid = (unsigned)(a.rows < want ? a.rows : want);
   const size_t dyn = (size_t)kRNSt * kRStageBytes + sizeof(RowSmem);
-  if (a.bf16) {
-    e = cudaFuncSetAttribute(k_row<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
-    if (e != cudaSuccess) return e;
-    k_row<uint16_t><<<grid, kRThreads, dyn, s>>>(a);
-  } else {
-    e = cudaFuncSetAttribute(k_row<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
-    if (e != cudaSuccess) return e;
-    k_row<float><<<grid, kRThreads, dyn, s>>>(a);
-  }
+  e = cudaFuncSetAttribute(k_row<E, RN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  if (e != cudaSuccess) return e;
+  k_row<E, RN><<<grid, kRThreads, dyn, s>>>(a);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s) {
+  if (a.rows <= 0) return cudaSuccess;
+  return a.bf16 ? launch_row_kernel<uint16_t, false>(a, s) : launch_row_kernel<float, false>(a, s);
+}
+
+cudaError_t launch_renorm_rows(const SampleArgs& a, cudaStream_t s) {
+  if (a.rows <= 0 || a.bf16 || !a.out) return cudaErrorInvalidValue;
+  return launch_row_kernel<float, true>(a, s);
 }
 
 cudaError_t row_read_error(uint32_t* word, int clear) {

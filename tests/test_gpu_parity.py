@@ -169,6 +169,56 @@ def test_renorm_in_place():
     np.testing.assert_allclose(t.cpu().numpy(), ref, rtol=1e-5, atol=1e-7)
 
 
+def _renorm_rows(rng, rows, V):
+    """Probability rows of several shapes: smooth, heavy-tailed down to denormals, sparse,
+    one-hot and flat."""
+    kind = rng.integers(0, 5, rows)
+    p = np.empty((rows, V), np.float32)
+    for r in range(rows):
+        if kind[r] == 0:
+            x = rng.standard_normal(V).astype(np.float32) * np.float32(2.0)
+        elif kind[r] == 1:
+            x = rng.standard_normal(V).astype(np.float32) * np.float32(30.0)
+        else:
+            x = rng.standard_normal(V).astype(np.float32)
+        q = oracle.softmax_temp(x[None])[0]
+        if kind[r] == 2:
+            q = q * (rng.random(V) < 0.1)
+            q[rng.integers(0, V)] += 0.01
+        elif kind[r] == 3:
+            q = np.zeros(V)
+            q[rng.integers(0, V)] = 1.0
+        elif kind[r] == 4:
+            q = np.full(V, 1.0)
+        p[r] = (q / q.sum()).astype(np.float32)
+    return p
+
+
+@pytest.mark.parametrize("V,rows", [(1, 40), (7, 320), (4095, 320), (4097, 320), (8193, 320),
+                                    (70001, 40), (262144, 12)])
+def test_renorm_row_kernel_edges(V, rows):
+    # vocabularies around the row kernel's 16 KB stages and its largest vocabulary, padded
+    # rows (16-byte aligned, ld > V), more rows than resident CTAs, every knob kind
+    rng = np.random.default_rng(V + rows)
+    p = _renorm_rows(rng, rows, V)
+    k = rng.choice(np.array([0, 1, 5, 300, 1024, 1025, 3000, V + 1, -3], np.int32),
+                   rows).astype(np.int32)
+    tp = rng.choice(np.array([1.0, 0.9, 0.5, 0.0], np.float32), rows).astype(np.float32)
+    ld = (V + 3) // 4 * 4 + 4
+    full = np.full((rows, ld), 7.0, np.float32)  # the padding must not be read
+    full[:, :V] = p
+    t = torch.from_numpy(full).cuda()
+    got = tv.topk_topp_renorm(t[:, :V], dev(k), dev(tp)).cpu().numpy()
+    ref, marg = oracle.topk_topp_renorm(p, k, tp)
+    ok = marg > BOUNDARY
+    assert ok.mean() > 0.9
+    np.testing.assert_array_equal(got[ok] > 0, ref[ok] > 0)
+    np.testing.assert_allclose(got[ok], ref[ok], rtol=1e-5, atol=1e-6)
+    # rows near a top-p boundary still hold a valid distribution over a prefix of the order
+    np.testing.assert_allclose(got.sum(-1), 1.0, rtol=1e-5)
+    assert (got[p == 0] == 0).all()
+
+
 # ---- chain speculative sampling: probability rows ----------------------------------------------
 
 def test_rejection_tiny_config():
