@@ -51,8 +51,7 @@ constexpr int kRBins = 2048;                 // top-p buckets (128 octaves)
 constexpr int kRHead = 1024;                 // buckets above the first stage's maximum
 constexpr int kRBPT = kRBins / kRCons;       // buckets per consumer thread at the end
 constexpr int kRCrossCap = kRListCap + (2 * kRBins * 4) / 8;  // top-k or crossing elements
-constexpr uint32_t kRWaitLimit = 1u << 16;
-constexpr uint32_t kRHintNs = 20000;
+constexpr uint64_t kRWaitNs = 2000000000ull;  // a stage wait gives up after 2 s
 constexpr double kInvFx = 1.0 / 1099511627776.0;
 
 static __device__ unsigned int g_row_err;
@@ -209,17 +208,40 @@ __device__ __forceinline__ float rn_edge(float b) {
   return __uint_as_float(((uint32_t)b + 1u) << 19);
 }
 
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 // Waits for the phase of `bar` with the given parity, giving up (and setting the error
-// word) after a bounded number of suspended polls.
+// word) after kRWaitNs or once another thread has given up.
 __device__ __forceinline__ void bounded_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t it = 0;
-  while (!mbar_try_wait_hint(bar, parity, kRHintNs)) {
-    ++it;
-    if (it > kRWaitLimit || ((it & 255u) == 0 && *(volatile unsigned int*)&g_row_err)) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((it & 63u) == 0 &&
+        (global_ns() - t0 > kRWaitNs || *(volatile unsigned int*)&g_row_err)) {
       atomicOr(&g_row_err, 1u);
       return;
     }
   }
+}
+
+// Reserves n consecutive entries of a shared list for each lane of the (converged) warp
+// with one atomic on the list's counter; returns the lane's first entry.
+__device__ __forceinline__ uint32_t warp_reserve(uint32_t* counter, uint32_t n, int lane) {
+  uint32_t incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+  uint32_t base = 0;
+  if (lane == 31 && total) base = atomicAdd(counter, total);
+  return __shfl_sync(0xffffffffu, base, 31) + incl - n;
 }
 
 // The request's knobs and the way its rows are served.
@@ -437,6 +459,7 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
     cbar();
 
     float bv = -INFINITY, lm = -INFINITY, ls = 0.f, lc = 0.f;
+    float tl = 0.f;  // top-p renorm: this thread's tail mass
     int64_t bvi = -1;  // the row vector holding this thread's maximum (first one)
 
     // ---- the stages of the row -------------------------------------------------------
@@ -448,12 +471,22 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
       const int nc = (int)min((int64_t)SE, V - c0);
       const int nvf = nc / N;
       auto vec_at = [&](int vi) -> uint4 { return stage_vec(sv, c0, nc, nvf, vi); };
-      // warp w takes the stage's vectors 128 w .. 128 w + 127, lane l those l + 32 u
+      // warp w takes the stage's vectors 128 w .. 128 w + 127, lane l those l + 32 u; the
+      // warp frees the slot once its vectors are in registers (the first stage of a large
+      // top-k stays until its threshold search has read it in place)
+      uint4 rv[kRVecs];
+#pragma unroll
+      for (int u = 0; u < kRVecs; ++u) rv[u] = vec_at(vbase + u * 32);
+      const bool hold = kn.kind == kRowTopK && c == 0 && k > kRCons;
+      if (!hold) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[slot]);
+      }
       float vmv[kRVecs];
 #pragma unroll
       for (int u = 0; u < kRVecs; ++u) {
         const int vi = vbase + u * 32;
-        const uint4 r = vec_at(vi);
+        const uint4 r = rv[u];
         const float vm = SVec<E>::vmax(r);
         vmv[u] = vm;
         if (vm > bv || (bvi < 0 && vi * N < nc)) {  // (an all -inf row keeps its lowest id)
@@ -508,7 +541,7 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
           if (!(vmv[u] > -INFINITY) || fkey(vmv[u]) < tau) continue;
           const int vi = vbase + u * 32;
           float xv[N];
-          SVec<E>::unpack(vec_at(vi), xv);
+          SVec<E>::unpack(rv[u], xv);
           uint32_t m = 0;
 #pragma unroll
           for (int q = 0; q < N; ++q)
@@ -528,7 +561,7 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
 #pragma unroll
         for (int u = 0; u < kRVecs; ++u) {
           float xv[N];
-          SVec<E>::unpack(vec_at(vbase + u * 32), xv);
+          SVec<E>::unpack(rv[u], xv);
 #pragma unroll
           for (int q = 0; q < N; ++q) zsum += fixw(fminf(fmaxf(xv[q], 0.f), 1.f));
         }
@@ -544,7 +577,7 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
           for (int u = 0; u < kRVecs; ++u) {
             const int vi = vbase + u * 32;
             float xv[N];
-            SVec<E>::unpack(vec_at(vi), xv);
+            SVec<E>::unpack(rv[u], xv);
 #pragma unroll
             for (int q = 0; q < N; ++q) {
               const float w = ex2((xv[q] - em) * sl2);
@@ -573,12 +606,26 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
           cbar();
         }
         const float base = sm.base;
+        // probabilities: vectors lighter than 2^-24 of this thread's running maximum skip
+        // the histogram and add to the thread's tail sum. Their total is below V 2^-24 of
+        // the row's mass, so for top_p <= 1 - V 2^-24 the crossing lies above them; the
+        // finish checks that it does and otherwise leaves the row to the general path.
+        // Vectors below 2^-41 of it weigh nothing in the fixed-point masses (2^-40 units)
+        // and are skipped.
+        const float tail_below = bv * 5.9604644775390625e-8f;
+        const float zero_below = bv * 4.547473508864641e-13f;
         bool out = false;
 #pragma unroll
         for (int u = 0; u < kRVecs; ++u) {
-          if (!live(vmv[u])) continue;
+          if (!live(vmv[u]) || (RN && vmv[u] < zero_below)) continue;
           float xv[N];
-          SVec<E>::unpack(vec_at(vbase + u * 32), xv);
+          SVec<E>::unpack(rv[u], xv);
+          if (RN && vmv[u] < tail_below) {
+#pragma unroll
+            for (int q = 0; q < N; ++q)
+              if (live(xv[q])) tl += xv[q];
+            continue;
+          }
 #pragma unroll
           for (int q = 0; q < N; ++q) {
             const float v = xv[q];
@@ -599,9 +646,10 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
         }
         if (out) sm.bad = 1;
       }
-      // the stage's slot is free again
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[slot]);
+      if (hold) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[slot]);
+      }
 
       // the candidate count is checked every few stages (and after the last): a stage adds
       // few candidates once the threshold has settled
@@ -866,6 +914,17 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
       if (tid == 0) finish_row(tok, acc);
     };
 
+    // the consumers' sum of a float (top-p tail masses)
+    auto consumer_sum = [&](float v) -> double {
+      v = warp_sum_f32(v);
+      if (lane == 0) sm.redf[1][warp] = v;
+      cbar();
+      double t = 0.0;
+      for (int w = 0; w < kRWarps; ++w) t += (double)sm.redf[1][w];
+      cbar();
+      return t;
+    };
+
     // ---- finish the row -----------------------------------------------------------------
     if constexpr (RN) {
       // renorm: the kept set (a threshold composite C, and for top-p rows the bucket rule)
@@ -889,9 +948,10 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
             hm[q] = h ? (double)h * (1.0 / 33554432.0) * (double)rn_edge(base - (float)i) : 0.0;
             hsum += hm[q];
           }
+          const double ttail = consumer_sum(tl);
           double Zt;
           const double hex = excl_scan_f64(hsum, sm.dscan, Zt);
-          P = (double)kn.tp * Zt;
+          P = (double)kn.tp * (Zt + ttail);
           if (tid == 0) sm.owner = -1;
           cbar();
           double acc_b = hex;
@@ -906,7 +966,10 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
           cbar();
           bstar = sm.owner;
           pre = sm.res_d;
-          active = bstar >= 0;
+          // (a crossing among the tail's weights is left to the general path)
+          active = bstar >= 0 &&
+                   (ttail == 0.0 ||
+                    __uint_as_float((uint32_t)(base - (float)bstar) << 19) >= M * 1.1920929e-7f);
         }
         if (tid == 0) sm.lcnt = 0;
         cbar();
@@ -916,36 +979,55 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
         for (int c = 0; c < nst; ++c, ++g) {
           const int slot = (int)(g % kRNSt);
           bounded_wait(&sm.full[slot], (g / kRNSt) & 1u);
+          const int64_t c0 = (int64_t)c * SE;
+          uint4 rv[kRVecs];
           if (active) {
             const uint4* sv = reinterpret_cast<const uint4*>(ring + slot * kRStageBytes);
-            const int64_t c0 = (int64_t)c * SE;
             const int nc = (int)min((int64_t)SE, V - c0);
             const int nvf = nc / N;
 #pragma unroll
+            for (int u = 0; u < kRVecs; ++u) rv[u] = stage_vec(sv, c0, nc, nvf, vbase + u * 32);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.empty[slot]);
+          if (active) {
+            uint32_t mk[kRVecs];
+            uint32_t nsel = 0;
+#pragma unroll
             for (int u = 0; u < kRVecs; ++u) {
-              const int vi = vbase + u * 32;
-              const uint4 r = stage_vec(sv, c0, nc, nvf, vi);
-              const float vm = SVec<E>::vmax(r);
+              mk[u] = 0;
+              const float vm = SVec<E>::vmax(rv[u]);
               if (!live(vm) || base - bucket_of(vm) > fb) continue;  // all lighter
               float xv[N];
-              SVec<E>::unpack(r, xv);
+              SVec<E>::unpack(rv[u], xv);
 #pragma unroll
               for (int q = 0; q < N; ++q) {
                 const float v = xv[q];
                 if (!live(v)) continue;
                 const float idx = base - bucket_of(v);
-                if (idx < fb) {
-                  zab += wfn(v);
-                } else if (idx == fb && wfn(v) > 0) {
-                  const uint32_t pos = atomicAdd(&sm.lcnt, 1u);
-                  if (pos < (uint32_t)kRCrossCap)
-                    sm.w.cross[pos] = comp_key(fkey(v), (uint32_t)(c0 + (int64_t)vi * N + q));
-                }
+                if (idx < fb) zab += wfn(v);
+                else if (idx == fb && wfn(v) > 0) mk[u] |= 1u << q;
+              }
+              nsel += (uint32_t)__popc(mk[u]);
+            }
+            if (__any_sync(0xffffffffu, nsel != 0)) {
+              uint32_t pos = warp_reserve(&sm.lcnt, nsel, lane);
+#pragma unroll
+              for (int u = 0; u < kRVecs; ++u) {
+                if (!mk[u]) continue;
+                float xv[N];
+                SVec<E>::unpack(rv[u], xv);
+#pragma unroll
+                for (int q = 0; q < N; ++q)
+                  if (mk[u] & (1u << q)) {
+                    if (pos < (uint32_t)kRCrossCap)
+                      sm.w.cross[pos] = comp_key(
+                          fkey(xv[q]), (uint32_t)(c0 + (int64_t)(vbase + u * 32) * N + q));
+                    ++pos;
+                  }
               }
             }
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.empty[slot]);
         }
         cbar();
         const uint32_t cnt = sm.lcnt;
@@ -1007,12 +1089,17 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
         const int64_t c0 = (int64_t)c * SE;
         const int nc = (int)min((int64_t)SE, V - c0);
         const int nvf = nc / N;
+        uint4 rw[kRVecs];
+#pragma unroll
+        for (int u = 0; u < kRVecs; ++u) rw[u] = stage_vec(sv, c0, nc, nvf, vbase + u * 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[slot]);
 #pragma unroll
         for (int u = 0; u < kRVecs; ++u) {
           const int vi = vbase + u * 32;
           if (vi * N >= nc) continue;
           float xv[N], y[N];
-          SVec<E>::unpack(stage_vec(sv, c0, nc, nvf, vi), xv);
+          SVec<E>::unpack(rw[u], xv);
 #pragma unroll
           for (int q = 0; q < N; ++q) {
             const float v = xv[q];
@@ -1032,8 +1119,6 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
               if (e0 + q < V) orow[e0 + q] = y[q];
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[slot]);
       }
     } else if (kn.kind == kRowTopP) {
       // top-p alone: bucket masses (thread t holds buckets 8t .. 8t + 7), the crossing

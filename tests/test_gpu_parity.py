@@ -362,6 +362,46 @@ def test_target_only_vocab_edges(V, dtype):
     compare_chain(g, ref, dtype)
 
 
+def test_top_p_crossing_in_the_far_tail():
+    # one dominant token and a long tail of tokens below 2^-24 of it: for top_p close to 1
+    # the crossing falls among the tail's weights (the streaming histogram leaves those out
+    # and hands such rows to the general path); smaller top_p keeps the head alone
+    rng = np.random.default_rng(31)
+    B, D, V = 4, 1, 131072
+    R = D + 1
+    x = (rng.standard_normal((B * R, V)) * 0.1 - 18.0).astype(np.float32)
+    x[:, 5] = 0.0
+    x[:, 77] = -2.0
+    T = np.ones(B, np.float32)
+    tp = np.array([0.999, 0.9999, 0.5, 0.99], np.float32)
+    k = np.zeros(B, np.int32)
+    drafts = np.full((B, D), 77, np.int32)
+    seed = synth.request_seeds(B)
+    off = np.arange(B, dtype=np.int64)
+    g = tv.chain_spec_sampling(dev(x), True, D, dev(drafts), temperature=dev(T), top_k=dev(k),
+                               top_p=dev(tp), seed=dev(seed), offset=dev(off))
+    ref = oracle.chain_spec_sampling(x, True, D, drafts, temperature=T, top_k=k, top_p=tp,
+                                     seed=seed, offset=off)
+    compare_chain(g, ref, "f32")
+    # the same rows as probabilities through the renorm call
+    p = oracle.softmax_temp(x).astype(np.float32)
+    tpr = np.repeat(tp, R)
+    got = tv.topk_topp_renorm(dev(p), None, dev(tpr)).cpu().numpy()
+    want, marg = oracle.topk_topp_renorm(p, None, tpr)
+    ok = marg > BOUNDARY
+    assert ok.sum() == 4  # top_p 0.5 and 0.99 keep the head alone
+    np.testing.assert_array_equal(got[ok] > 0, want[ok] > 0)
+    np.testing.assert_allclose(got[ok], want[ok], rtol=1e-5, atol=1e-6)
+    # a crossing among near-equal tail weights is a boundary case: the kept set is still a
+    # prefix of the (value desc, index asc) order, of about the oracle's size
+    for r in np.flatnonzero(~ok):
+        order = np.lexsort((np.arange(V), -p[r]))
+        m = int((got[r] > 0).sum())
+        assert (got[r][order[:m]] > 0).all()
+        assert abs(m - int((want[r] > 0).sum())) <= V // 100
+        np.testing.assert_allclose(got[r].sum(), 1.0, rtol=1e-5)
+
+
 def test_target_only_explicit_uniforms_and_knobs_off():
     rng = np.random.default_rng(77)
     B, D, V = 40, 3, 5000
