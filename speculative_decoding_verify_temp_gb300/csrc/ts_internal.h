@@ -58,7 +58,8 @@ struct Workspace {
   uint64_t* cmass;    // [rows * 8] per-CTA masses of a cluster-staged row
   uint32_t* flag;     // [rows] rows the split-row sampling kernel leaves to the staged one
   uint32_t* ccount;   // [rows] candidates collected for a row
-  uint32_t* work;     // [2] the row kernel's next-row counter and finished-CTA count
+  uint32_t* work;     // [4] the row kernel's 64-bit next-row counter ([0..1], 8-byte
+                      // aligned) and finished-CTA count ([2])
   uint64_t* cand;     // [rows * cand_splits * kSTopK] per-row summaries of the split-row
                       // kernel (vocab > 0 only)
   int64_t cand_splits;

@@ -51,7 +51,8 @@ constexpr int kRBins = 2048;                 // top-p buckets (128 octaves)
 constexpr int kRHead = 1024;                 // buckets above the first stage's maximum
 constexpr int kRBPT = kRBins / kRCons;       // buckets per consumer thread at the end
 constexpr int kRCrossCap = kRListCap + (2 * kRBins * 4) / 8;  // top-k or crossing elements
-constexpr uint64_t kRWaitNs = 2000000000ull;  // a stage wait gives up after 2 s
+constexpr long long kRWaitCycles = 1ll << 32;  // a stage wait gives up after 2^32 SM
+                                               // clock cycles (about 2 s)
 constexpr double kInvFx = 1.0 / 1099511627776.0;
 
 static __device__ unsigned int g_row_err;
@@ -208,25 +209,32 @@ __device__ __forceinline__ float rn_edge(float b) {
   return __uint_as_float(((uint32_t)b + 1u) << 19);
 }
 
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
+__device__ __forceinline__ bool row_error() { return *(volatile unsigned int*)&g_row_err != 0; }
+
+// Waits for the phase of `bar` with the given parity; gives up (setting the error word)
+// after kRWaitCycles of this SM's clock (monotonic) or once any thread has given up.
+// Returns whether the phase completed.
+__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0 && (clock64() - t0 > kRWaitCycles || row_error())) {
+      atomicOr(&g_row_err, 1u);
+      return false;
+    }
+  }
 }
 
-// Waits for the phase of `bar` with the given parity, giving up (and setting the error
-// word) after kRWaitNs or once another thread has given up.
-__device__ __forceinline__ void bounded_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return;
-  const uint64_t t0 = global_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return;
-    if ((it & 63u) == 0 &&
-        (global_ns() - t0 > kRWaitNs || *(volatile unsigned int*)&g_row_err)) {
+// As bounded_wait, but only the time limit ends it: used to let the copies a CTA has
+// issued land before it exits, also after an error.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kRWaitCycles) {
       atomicOr(&g_row_err, 1u);
       return;
     }
-  }
 }
 
 // Reserves n consecutive entries of a shared list for each lane of the (converged) warp
@@ -318,32 +326,38 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
   // ---- producer warp ------------------------------------------------------------------
   if (warp == kRWarps) {
     if (lane == 0) {
-      uint32_t g = 0;
+      uint32_t g = 0;  // stages issued so far
+      bool ok = true;
       int64_t rr = blockIdx.x;
-      for (;;) {
+      while (ok) {
         int64_t row = -1;
         if constexpr (RN) {  // renorm: rows in turn, no workspace
           row = (rr < a.rows) ? rr : -1;
           rr += gridDim.x;
         } else {
-          // rows are taken from a shared counter, so that CTAs with cheap rows take more;
-          // the counter runs over the rows twice, the costly kinds on the first round and
-          // the others on the second, so that no costly row is left for the end
-          const int64_t idx = (int64_t)atomicAdd(&a.ws.work[0], 1u);
-          if (idx < 2 * a.rows) {
-            row = (idx < a.rows) ? idx : idx - a.rows;
+          // rows are taken from a shared counter, so that CTAs with cheap rows take more.
+          // The counter runs over the rows four times, taking on each round the rows of one
+          // cost tier, longest first (top-p and general rows, then large top-k, then the
+          // other sampled rows, then greedy rows): the step then ends on short rows.
+          const uint64_t idx = atomicAdd(reinterpret_cast<unsigned long long*>(a.ws.work), 1ull);
+          if (idx < 4ull * (uint64_t)a.rows) {
+            const int tier = (int)(idx / (uint64_t)a.rows);
+            row = (int64_t)(idx % (uint64_t)a.rows);
             const Knobs kq = row_knobs(a, row / a.R);
-            const bool costly = kq.kind == kRowTopP || kq.kind == kRowStaged ||
-                                (kq.kind == kRowTopK && kq.k > kRCons);
-            if (costly != (idx < a.rows)) continue;
+            int t = 3;
+            if (kq.kind == kRowTopP || kq.kind == kRowStaged) t = 0;
+            else if (kq.kind == kRowTopK && kq.k > kRCons) t = 1;
+            else if (kq.kind != kRowGreedy) t = 2;
+            if (t != tier) continue;
           }
         }
         if (row < 0) {  // one last stage tells the consumers to stop
           const int slot = (int)(g % kRNSt);
           const uint32_t use = g / kRNSt;
-          if (use > 0) bounded_wait(&sm.empty[slot], (use - 1) & 1u);
+          if ((use > 0 && !bounded_wait(&sm.empty[slot], (use - 1) & 1u)) || row_error()) break;
           sm.srow[slot] = -1;
           mbar_arrive_expect_tx(&sm.full[slot], 0u);
+          ++g;  // (the marker is the latest use of its slot)
           break;
         }
         const unsigned char* src =
@@ -355,7 +369,11 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
           const int c = cc % nst;
           const int slot = (int)(g % kRNSt);
           const uint32_t use = g / kRNSt;
-          if (use > 0) bounded_wait(&sm.empty[slot], (use - 1) & 1u);
+          // after an error nothing more is issued (a slot may still be in use)
+          if ((use > 0 && !bounded_wait(&sm.empty[slot], (use - 1) & 1u)) || row_error()) {
+            ok = false;
+            break;
+          }
           const int64_t nc = min((int64_t)SE, V - (int64_t)c * SE);
           const uint32_t bytes = (uint32_t)((nc * (int64_t)sizeof(E)) & ~(int64_t)15);
           sm.srow[slot] = row;
@@ -365,6 +383,10 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
                      &sm.full[slot]);
         }
       }
+      // no copy of this CTA may still be in flight when it exits: wait for the last use
+      // of every slot (the consumers have normally waited for them already)
+      for (uint32_t h = (g > (uint32_t)kRNSt ? g - (uint32_t)kRNSt : 0u); h < g; ++h)
+        drain_wait(&sm.full[h % kRNSt], (h / kRNSt) & 1u);
     }
     return;
   }
@@ -1465,9 +1487,9 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
   // the last CTA to finish leaves the row counter at zero for the next call
   if (!RN && tid == 0) {
     __threadfence();
-    if (atomicAdd(&a.ws.work[1], 1u) == gridDim.x - 1) {
-      a.ws.work[0] = 0u;
-      a.ws.work[1] = 0u;
+    if (atomicAdd(&a.ws.work[2], 1u) == gridDim.x - 1) {
+      *reinterpret_cast<unsigned long long*>(a.ws.work) = 0ull;
+      a.ws.work[2] = 0u;
     }
   }
 }
