@@ -51,6 +51,7 @@ constexpr int kRBins = 2048;                 // top-p buckets (128 octaves)
 constexpr int kRHead = 1024;                 // buckets above the first stage's maximum
 constexpr int kRBPT = kRBins / kRCons;       // buckets per consumer thread at the end
 constexpr int kRCrossCap = kRListCap + (2 * kRBins * 4) / 8;  // top-k or crossing elements
+constexpr int kRNList = 512;                 // renorm rows a CTA can list (tiered order)
 constexpr long long kRWaitCycles = 1ll << 32;  // a stage wait gives up after 2^32 SM
                                                // clock cycles (about 2 s)
 constexpr double kInvFx = 1.0 / 1099511627776.0;
@@ -298,6 +299,10 @@ struct RowSmem {
   int32_t owner;
   uint64_t res_u;
   double res_d;
+  // renorm: this CTA's rows in the cost-tiered order, and the counts that build it
+  int32_t rnrows[kRNList];
+  uint32_t tcnt[3];
+  uint32_t wtc[kRThreads / 32][3];
 };
 
 template <typename E, bool RN>
@@ -321,7 +326,53 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
   if (tid < 16) {
     sm.tab[tid] = exp2(-(double)tid / 16.0);
   }
+  if (tid < 3) sm.tcnt[tid] = 0;
   __syncthreads();
+
+  // Renorm rows (no workspace, so no shared counter): every CTA orders the rows the same
+  // way, by cost tier (large top-k and general rows, then top-p rows, then the rest) and
+  // by row within a tier, and takes every gridDim.x-th row of that order from its own
+  // index on, so that each CTA gets about the same number of rows of each tier. Rows in
+  // turn when the list would not fit.
+  int32_t rn_n = -1;
+  if constexpr (RN) {
+    if (a.rows <= (int64_t)kRNList * (int64_t)gridDim.x) {
+      auto tier_of = [&](int64_t r) -> int {
+        const Knobs kq = row_knobs(a, r);
+        if (kq.kind == kRowStaged || (kq.kind == kRowTopK && kq.k > kRCons)) return 0;
+        return (kq.kind == kRowTopP) ? 1 : 2;
+      };
+      uint32_t cnt3[3] = {0u, 0u, 0u};
+      for (int64_t r = tid; r < a.rows; r += kRThreads) ++cnt3[tier_of(r)];
+      for (int t = 0; t < 3; ++t)
+        if (cnt3[t]) atomicAdd(&sm.tcnt[t], cnt3[t]);
+      __syncthreads();
+      uint32_t run[3] = {0u, sm.tcnt[0], sm.tcnt[0] + sm.tcnt[1]};  // next position per tier
+      const uint32_t lt = (1u << lane) - 1u;
+      for (int64_t r0 = 0; r0 < a.rows; r0 += kRThreads) {
+        const int64_t r = r0 + tid;
+        const int t = (r < a.rows) ? tier_of(r) : 3;
+        uint32_t before = 0;
+        for (int q = 0; q < 3; ++q) {
+          const uint32_t m = __ballot_sync(0xffffffffu, t == q);
+          if (lane == 0) sm.wtc[warp][q] = (uint32_t)__popc(m);
+          if (t == q) before = (uint32_t)__popc(m & lt);
+        }
+        __syncthreads();
+        if (t < 3) {
+          uint32_t pos = run[t] + before;
+          for (int w = 0; w < warp; ++w) pos += sm.wtc[w][t];
+          if (pos % gridDim.x == blockIdx.x) sm.rnrows[pos / gridDim.x] = (int32_t)r;
+        }
+        for (int q = 0; q < 3; ++q)
+          for (int w = 0; w < kRThreads / 32; ++w) run[q] += sm.wtc[w][q];
+        __syncthreads();
+      }
+      rn_n = (a.rows > (int64_t)blockIdx.x)
+                 ? (int32_t)((a.rows - 1 - (int64_t)blockIdx.x) / gridDim.x + 1)
+                 : 0;
+    }
+  }
 
   // ---- producer warp ------------------------------------------------------------------
   if (warp == kRWarps) {
@@ -329,11 +380,17 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
       uint32_t g = 0;  // stages issued so far
       bool ok = true;
       int64_t rr = blockIdx.x;
+      int32_t q = 0;
       while (ok) {
         int64_t row = -1;
-        if constexpr (RN) {  // renorm: rows in turn, no workspace
-          row = (rr < a.rows) ? rr : -1;
-          rr += gridDim.x;
+        if constexpr (RN) {  // renorm: the listed rows, else rows in turn
+          if (rn_n >= 0) {
+            row = (q < rn_n) ? (int64_t)sm.rnrows[q] : -1;
+            ++q;
+          } else {
+            row = (rr < a.rows) ? rr : -1;
+            rr += gridDim.x;
+          }
         } else {
           // rows are taken from a shared counter, so that CTAs with cheap rows take more.
           // The counter runs over the rows four times, taking on each round the rows of one
@@ -674,8 +731,10 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
       }
 
       // the candidate count is checked every few stages (and after the last): a stage adds
-      // few candidates once the threshold has settled
-      const int cstride = (k > kRCons) ? 2 : 8;
+      // few candidates once the threshold has settled. Large k is checked every stage: a
+      // first-stage threshold at k = 1000 passes a quarter of a 4096-entry fp32 stage, so
+      // two stages could fill the list past its capacity
+      const int cstride = (k > kRCons) ? 1 : 8;
       const uint32_t soft = (k > kRCons) ? (uint32_t)kRListCap : (uint32_t)kRSoft;
       if (kn.kind == kRowTopK && ((c + 1) % cstride == 0 || c == nst - 1)) {
         cbar();

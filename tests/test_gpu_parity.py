@@ -362,6 +362,24 @@ def test_target_only_vocab_edges(V, dtype):
     compare_chain(g, ref, dtype)
 
 
+def test_renorm_many_short_rows():
+    # more rows than the CTAs' tiered row lists hold (they then take rows in turn), and a
+    # count just below that limit
+    for rows in (160000, 150000):
+        rng = np.random.default_rng(rows)
+        V = 8
+        p = rng.random((rows, V)).astype(np.float32)
+        p /= p.sum(-1, keepdims=True)
+        k = rng.choice(np.array([0, 1, 3, 5], np.int32), rows).astype(np.int32)
+        tp = rng.choice(np.array([1.0, 0.5, 0.8], np.float32), rows).astype(np.float32)
+        got = tv.topk_topp_renorm(dev(p), dev(k), dev(tp)).cpu().numpy()
+        want, marg = oracle.topk_topp_renorm(p, k, tp)
+        ok = marg > BOUNDARY
+        assert ok.mean() > 0.99
+        np.testing.assert_array_equal(got[ok] > 0, want[ok] > 0)
+        np.testing.assert_allclose(got[ok], want[ok], rtol=1e-5, atol=1e-6)
+
+
 def test_top_p_crossing_in_the_far_tail():
     # one dominant token and a long tail of tokens below 2^-24 of it: for top_p close to 1
     # the crossing falls among the tail's weights (the streaming histogram leaves those out
