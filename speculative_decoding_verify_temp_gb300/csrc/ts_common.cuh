@@ -36,6 +36,11 @@ __device__ __forceinline__ uint32_t fkey(float x) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// The float of an order key from fkey (the key of -0 gives +0).
+__device__ __forceinline__ float key_to_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // Composite order key: value descending, then token id ascending, is composite
 // descending. Token ids must be below 2^24.
 __device__ __forceinline__ uint64_t comp_key(uint32_t key, uint32_t idx) {

@@ -58,6 +58,7 @@ struct Workspace {
   uint64_t* cmass;    // [rows * 8] per-CTA masses of a cluster-staged row
   uint32_t* flag;     // [rows] rows the split-row sampling kernel leaves to the staged one
   uint32_t* ccount;   // [rows] candidates collected for a row
+  uint32_t* best;     // [rows] Gumbel-max: the row's best score so far (order key, 0: none)
   uint32_t* work;     // [4] the row kernel's 64-bit next-row counter ([0..1], 8-byte
                       // aligned) and finished-CTA count ([2])
   uint64_t* cand;     // [rows * cand_splits * kSTopK] per-row summaries of the split-row

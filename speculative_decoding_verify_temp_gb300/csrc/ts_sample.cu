@@ -106,9 +106,6 @@ struct SVec<uint16_t> {
   }
 };
 
-__device__ __forceinline__ float key_to_value(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
 __device__ __forceinline__ uint32_t comp_token(uint64_t c) {
   return kIdxMax - (uint32_t)(c & kIdxMax);
 }

@@ -118,13 +118,16 @@ __global__ void __launch_bounds__(kStreamThreads) k_rowstat(RowStatArgs a) {
   int32_t bi = INT32_MAX;
   float lm = -INFINITY, ls = 0.f, lc = 0.f;
   const bool lse = !GUMBEL && a.want_lse;
+  // Gumbel: the best score any CTA of the row has published so far (a lower bound of the
+  // row's best): an element group whose largest possible score is below it is skipped
+  float wbound = -INFINITY;
 
   // Elements x[0..n) with indices base.. base+n-1, n a multiple of 4 for the vector path.
   auto visit = [&](const float* x, int n, int64_t base) {
     if (GUMBEL && noise) {
       for (int g = 0; g < n; g += 4) {
         const float gm = fmaxf(fmaxf(x[g], x[g + 1]), fmaxf(x[g + 2], x[g + 3]));
-        if (gm * invT + kGumbelCap >= bv) {
+        if (gm * invT + kGumbelCap >= fmaxf(bv, wbound)) {
           const uint32_t gi = (uint32_t)((base + g) >> 2);
           const uint4 r = philox4x32_10(make_uint4(gi, c1, c2, c3), k0, k1);
           const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
@@ -167,23 +170,34 @@ __global__ void __launch_bounds__(kStreamThreads) k_rowstat(RowStatArgs a) {
   if (a.vec) {
     const int64_t nv = (hi - lo) / N;
     const uint4* vp = reinterpret_cast<const uint4*>(xr + lo);
-    int64_t vi = threadIdx.x;
     constexpr int U = 4;
-    for (; vi + (U - 1) * kStreamThreads < nv; vi += U * kStreamThreads) {
+    // rounds of U vectors a thread (the same count for every thread of the CTA)
+    const int64_t rounds = (nv + U * kStreamThreads - 1) / (U * kStreamThreads);
+    for (int64_t rd = 0; rd < rounds; ++rd) {
+      const int64_t vi = rd * (U * kStreamThreads) + threadIdx.x;
       uint4 r[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) r[u] = ldg_stream(vp + vi + u * kStreamThreads);
+      for (int u = 0; u < U; ++u)
+        if (vi + u * kStreamThreads < nv) r[u] = ldg_stream(vp + vi + u * kStreamThreads);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
+        if (vi + u * kStreamThreads >= nv) continue;
         float x[N];
         Vec<E>::unpack(r[u], x);
         visit(x, N, lo + (vi + u * kStreamThreads) * N);
       }
-    }
-    for (; vi < nv; vi += kStreamThreads) {
-      float x[N];
-      Vec<E>::unpack(ldg_stream(vp + vi), x);
-      visit(x, N, lo + vi * N);
+      if (GUMBEL && noise) {
+        // publish the warp's best score to the row and take the row's best back
+        float m = bv;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float rb = m;
+        if ((threadIdx.x & 31) == 0) {
+          const uint32_t old = atomicMax(&a.ws.best[row], m > -INFINITY ? fkey(m) : 0u);
+          if (old != 0u) rb = fmaxf(rb, key_to_value(old));
+        }
+        wbound = __shfl_sync(0xffffffffu, rb, 0);
+      }
     }
     // ragged tail: fewer than N elements, padded with -inf to a multiple of 4
     const int64_t t0 = lo + nv * N;
@@ -231,6 +245,7 @@ __global__ void __launch_bounds__(kStreamThreads) k_rowstat(RowStatArgs a) {
     warp_lse(m, s);
     if (lane == 0) {
       a.ws.rowcnt[row] = 0;
+      if (GUMBEL) a.ws.best[row] = 0;
       const int32_t am = (i == INT32_MAX) ? 0 : i;
       if (a.kind == 2) {
         a.tokens_out[row] = am;
