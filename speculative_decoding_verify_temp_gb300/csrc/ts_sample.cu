@@ -1268,7 +1268,9 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
               const int64_t gi = c0 + (int64_t)vi * N + q;
               if (idx < fb) {
                 if (gi != (int64_t)x) s += ex2((v - M) * sl2);
-              } else if (idx == fb && wfn(v) > 0) {
+              } else if (idx == fb) {
+                // (a candidate of zero fixed-point weight sorts after every positive one,
+                // so it never moves the mass cut)
                 const uint32_t pos = atomicAdd(&sm.lcnt, 1u);
                 if (pos < (uint32_t)kRCrossCap) sm.w.cross[pos] = comp_key(fkey(v), (uint32_t)gi);
               }
