@@ -131,11 +131,17 @@ __global__ void __launch_bounds__(kStreamThreads) k_rowstat(RowStatArgs a) {
           const uint32_t gi = (uint32_t)((base + g) >> 2);
           const uint4 r = philox4x32_10(make_uint4(gi, c1, c2, c3), k0, k1);
           const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
+          const float bound = fmaxf(bv, wbound);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             if (x[g + k] == -INFINITY) continue;
-            const float e = -logf(u01(wv[k]));
-            const float s = x[g + k] * invT - __logf(e);
+            const float u = u01(wv[k]);
+            const float xs = x[g + k] * invT;
+            // -ln(-ln u) <= -ln(1 - u) (1 - u is exact): an element whose bound, with a
+            // margin far above the fast log's error, stays below the best cannot win
+            if (xs - __logf(1.f - u) + 1e-3f < bound) continue;
+            const float e = -logf(u);
+            const float s = xs - __logf(e);
             if (s > bv) {
               bv = s;
               bi = (int32_t)(base + g + k);
