@@ -73,9 +73,10 @@ ts_status ts_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t strea
 const char* ts_last_error_message(void);
 
 /* Synchronises the current device and reads (then, if clear != 0, clears) the
- * library's device error word: 0 if no bounded wait ever gave up. Returns
- * TS_ERR_TIMEOUT if a wait gave up, TS_ERR_CUDA if the read failed. A diagnostic,
- * not part of the hot path. */
+ * library's device error word: 0 if no bounded wait ever gave up; otherwise bits 0-7
+ * come from the cluster-staged kernels, bits 8-15 from the row-streaming kernel and
+ * bits 16-23 from the staged softmax. Returns TS_ERR_TIMEOUT if a wait gave up,
+ * TS_ERR_CUDA if the read failed. A diagnostic, not part of the hot path. */
 ts_status ts_device_error(uint32_t* word_host, int clear);
 
 /* Temperature softmax [TS-FI verify(): softmax(logits, temperature)].

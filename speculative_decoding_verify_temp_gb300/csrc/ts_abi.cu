@@ -143,10 +143,11 @@ ts_status ts_device_error(uint32_t* word_host, int clear) {
   if (!word_host) return fail(TS_ERR_INVALID_ARG, "word_host is NULL");
   uint32_t w = 0;
   cudaError_t e = tsv::staged_read_error(&w, clear);
-  uint32_t w2 = 0;
+  uint32_t w2 = 0, w3 = 0;
   if (e == cudaSuccess) e = tsv::row_read_error(&w2, clear);
+  if (e == cudaSuccess) e = tsv::softmax_read_error(&w3, clear);
   if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
-  w |= w2 << 8;
+  w |= (w2 << 8) | (w3 << 16);
   *word_host = w;
   if (w) return fail(TS_ERR_TIMEOUT, "a bounded device wait gave up (word 0x%x)", w);
   g_msg[0] = 0;

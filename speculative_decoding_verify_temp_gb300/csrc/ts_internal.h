@@ -129,6 +129,7 @@ cudaError_t launch_draw_probs(const DrawArgs& a, cudaStream_t s);
 // Temperature softmax of 16-byte aligned rows into [rows, V] fp32 (ts_stream.cu).
 cudaError_t launch_softmax(const void* x, int bf16, int64_t rows, int64_t ld, int64_t V,
                            const float* temperature, float* out, cudaStream_t s);
+cudaError_t softmax_read_error(uint32_t* word, int clear);
 
 cudaError_t launch_logprobs_probs(const float* p, int64_t ld, int64_t V, int64_t rows,
                                   const int32_t* tokens, float* out, cudaStream_t s);

@@ -7,10 +7,13 @@
 //                        chosen-token logprobs (gather_token_logprobs_torch), or the
 //                        temperature-only Gumbel-max draw (TensorRT-LLM interface.py,
 //                        _sample_sharded_temperature).
-//  k_softmax             temperature softmax (TokenSpeed flashinfer.py verify():
-//                        softmax(logits, temperature)): a cluster of CTAs per row streams
-//                        its slices twice, the row maximum and sum combined through
-//                        distributed shared memory in between.
+//  k_softmax_smem        temperature softmax (TokenSpeed flashinfer.py verify():
+//                        softmax(logits, temperature)): a cluster of CTAs per row, each
+//                        CTA's slice brought into shared memory once by bulk copies, the
+//                        row maximum and sum combined through distributed shared memory,
+//                        the probabilities written from the staged copy.
+//  k_softmax             the same for rows too long to stage: the slices are streamed
+//                        twice.
 //  k_draw_probs          chain speculative sampling on probability rows (TensorRT-LLM
 //                        interface.py, rejection_sampling_one_model): the accept tests,
 //                        then one streamed pass over the single row that the final
@@ -762,8 +765,229 @@ __global__ void __launch_bounds__(kStreamThreads) k_softmax(const void* x, int64
     orow[i] = prob(Vec<E>::scalar(xr, i), i);
 }
 
+// The same softmax with each CTA's slice staged once in shared memory: bulk copies bring
+// the slice in (16 KB chunks, one mbarrier each, all in flight at once), both passes read
+// it from there, so the logits are read from HBM once.
+constexpr int kSmChunk = 16384;       // bytes a chunk
+constexpr int kSmMaxChunks = 8;       // slices of at most 128 KB
+constexpr long long kSmWaitCycles = 1ll << 32;
+static __device__ unsigned int g_softmax_err;
+
+template <typename E>
+__global__ void __launch_bounds__(kStreamThreads) k_softmax_smem(const void* x, int64_t ld,
+                                                                 int64_t V,
+                                                                 const float* temperature,
+                                                                 float* out, int64_t slice) {
+  extern __shared__ __align__(128) unsigned char sbuf[];
+  __shared__ uint64_t bars[kSmMaxChunks];
+  __shared__ float s_part[4];
+  __shared__ float s_v[32], s_m[32], s_s[32];
+  __shared__ int32_t s_i[32];
+  cg::cluster_group cluster = cg::this_cluster();
+  const int crank = (int)cluster.block_rank();
+  const int CL = (int)cluster.num_blocks();
+  const int64_t row = blockIdx.x / CL;
+  constexpr int N = Vec<E>::N;
+  const E* xr = reinterpret_cast<const E*>(x) + row * ld;
+  const int64_t lo = (int64_t)crank * slice;
+  const int64_t hi = min(V, lo + slice);
+  const float T = temperature ? temperature[row] : 1.f;
+  const bool greedy = !(T >= kGreedyT);
+  const float sl2 = greedy ? 0.f : __fdiv_rn(kLog2e, T);
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int64_t nv = (hi > lo) ? (hi - lo) / N : 0;  // whole vectors of the slice
+  const uint32_t bytes = (uint32_t)(nv * 16);      // staged bytes (whole vectors)
+  const int nch = (int)((bytes + kSmChunk - 1) / kSmChunk);
+  const uint4* sv = reinterpret_cast<const uint4*>(sbuf);
+
+  if (tid == 0) {
+    for (int c = 0; c < nch; ++c) mbar_init(&bars[c], 1);
+    fence_mbar_init();
+    const unsigned char* src = reinterpret_cast<const unsigned char*>(xr + lo);
+    for (int c = 0; c < nch; ++c) {
+      const uint32_t nb = min((uint32_t)kSmChunk, bytes - (uint32_t)c * kSmChunk);
+      mbar_arrive_expect_tx(&bars[c], nb);
+      bulk_g2s(sbuf + (size_t)c * kSmChunk, src + (size_t)c * kSmChunk, nb, &bars[c]);
+    }
+  }
+  __syncthreads();
+
+  // ---- 1. maximum, argmax, sum of exp((x - m) / T) with a running maximum m -------------
+  float bv = -INFINITY, ls = 0.f, lc = 0.f;
+  int32_t bi = INT32_MAX;
+  auto visit = [&](const float* xv, int n, int64_t base) {
+    float vm = xv[0];
+    for (int q = 1; q < n; ++q) vm = fmaxf(vm, xv[q]);
+    if (vm > bv || bi == INT32_MAX) {
+      for (int q = 0; q < n; ++q)
+        if (xv[q] == vm) {
+          bi = (int32_t)(base + q);
+          break;
+        }
+      if (!greedy && vm > bv && bv > -INFINITY) {
+        const float f = ex2((bv - vm) * sl2);
+        ls *= f;
+        lc *= f;
+      }
+      bv = fmaxf(bv, vm);
+    }
+    if (!greedy && bv > -INFINITY) {
+      float vs = 0.f;
+      for (int q = 0; q < n; ++q) vs += ex2((xv[q] - bv) * sl2);
+      kahan_add(ls, lc, vs);
+    }
+  };
+  constexpr int VPC = kSmChunk / 16;  // vectors a chunk
+  for (int c = 0; c < nch; ++c) {
+    // wait for chunk c: only the time limit ends the wait, so that the CTA never leaves
+    // with a copy in flight while the copies are still landing
+    const long long t0 = clock64();
+    while (!mbar_try_wait(&bars[c], 0u)) {
+      if (clock64() - t0 > kSmWaitCycles) {
+        atomicOr(&g_softmax_err, 1u);
+        break;
+      }
+    }
+    const int64_t v1 = min(nv, (int64_t)(c + 1) * VPC);
+    for (int64_t vi = (int64_t)c * VPC + tid; vi < v1; vi += kStreamThreads) {
+      float xv[N];
+      Vec<E>::unpack(sv[vi], xv);
+      visit(xv, N, lo + vi * N);
+    }
+  }
+  const int64_t t0 = lo + nv * N;
+  if (tid == 0 && t0 < hi) {  // the slice's ragged tail, from global memory
+    float xv[N];
+    const int n = (int)(hi - t0);
+    for (int q = 0; q < N; ++q) xv[q] = q < n ? Vec<E>::scalar(xr, t0 + q) : -INFINITY;
+    visit(xv, N, t0);
+  }
+  ls += lc;
+  auto merge = [&](float& m, float& sum, int32_t& i, float m2, float s2, int32_t i2) {
+    const float nm = fmaxf(m, m2);
+    if (!greedy && nm > -INFINITY)
+      sum = ((m > -INFINITY) ? sum * ex2((m - nm) * sl2) : 0.f) +
+            ((m2 > -INFINITY) ? s2 * ex2((m2 - nm) * sl2) : 0.f);
+    if (m2 > m || (m2 == m && i2 < i)) i = i2;
+    m = nm;
+  };
+  {
+    float m = bv, sum = ls;
+    int32_t i = bi;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      merge(m, sum, i, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, sum, o),
+            __shfl_xor_sync(0xffffffffu, i, o));
+    if (lane == 0) {
+      s_m[w] = m;
+      s_s[w] = sum;
+      s_i[w] = i;
+    }
+    __syncthreads();
+    if (w == 0) {
+      const int nw = kStreamThreads / 32;
+      m = lane < nw ? s_m[lane] : -INFINITY;
+      sum = lane < nw ? s_s[lane] : 0.f;
+      i = lane < nw ? s_i[lane] : INT32_MAX;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+        merge(m, sum, i, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, sum, o),
+              __shfl_xor_sync(0xffffffffu, i, o));
+      if (lane == 0) {
+        s_part[0] = m;
+        s_part[1] = sum;
+        s_part[2] = __int_as_float(i);
+      }
+    }
+  }
+  cluster.sync();  // the CTAs' partials are visible
+  if (tid == 0) {
+    float m = -INFINITY, sum = 0.f;
+    int32_t i = INT32_MAX;
+    for (int c = 0; c < CL; ++c) {  // every CTA merges in the same order
+      const float* pp = cluster.map_shared_rank(s_part, c);
+      merge(m, sum, i, pp[0], pp[1], __float_as_int(pp[2]));
+    }
+    s_v[0] = m;
+    s_v[1] = (sum > 0.f) ? __frcp_rn(sum) : 0.f;
+    s_i[0] = i;
+  }
+  cluster.sync();  // no CTA leaves while a peer may still read its partial
+  const float M = s_v[0], inv = s_v[1];
+  const int32_t am = s_i[0];
+
+  // ---- 2. the probabilities of the slice, from the staged copy ------------------------
+  float* orow = out + row * V;
+  auto prob = [&](float v, int64_t gi) -> float {
+    if (greedy) return (gi == (int64_t)am) ? 1.f : 0.f;
+    return ex2((v - M) * sl2) * inv;
+  };
+  const bool vout = ((reinterpret_cast<uintptr_t>(orow + lo) & 15) == 0);
+  for (int64_t vi = tid; vi < nv; vi += kStreamThreads) {
+    float xv[N];
+    Vec<E>::unpack(sv[vi], xv);
+    const int64_t base = lo + vi * N;
+    float y[N];
+#pragma unroll
+    for (int q = 0; q < N; ++q) y[q] = prob(xv[q], base + q);
+    if (vout) {
+      float4* op = reinterpret_cast<float4*>(orow + base);
+#pragma unroll
+      for (int h = 0; h < N / 4; ++h) __stcs(op + h, make_float4(y[4 * h], y[4 * h + 1], y[4 * h + 2], y[4 * h + 3]));
+    } else {
+#pragma unroll
+      for (int q = 0; q < N; ++q) orow[base + q] = y[q];
+    }
+  }
+  for (int64_t i = lo + nv * N + tid; i < hi; i += kStreamThreads)
+    orow[i] = prob(Vec<E>::scalar(xr, i), i);
+}
+
+cudaError_t softmax_read_error(uint32_t* word, int clear) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_softmax_err, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (clear && v) {
+    const unsigned int z = 0;
+    e = cudaMemcpyToSymbol(g_softmax_err, &z, sizeof(z));
+  }
+  *word = v;
+  return e;
+}
+
 cudaError_t launch_softmax(const void* x, int bf16, int64_t rows, int64_t ld, int64_t V,
                            const float* temperature, float* out, cudaStream_t s) {
+  // staged: the smallest cluster (1, 2, 4 or 8 CTAs) whose slices fit 128 KB of shared
+  // memory, slices of whole 16-byte vectors (a multiple of 8 elements). (Smaller slices,
+  // 3 or 4 CTAs an SM, measured slower on the 201088-token bf16 rows.)
+  const int64_t esize = bf16 ? 2 : 4;
+  for (int cl = 1; cl <= 8; cl *= 2) {
+    const int64_t slice = (((V + cl - 1) / cl) + 7) & ~(int64_t)7;
+    if (slice * esize > (int64_t)kSmChunk * kSmMaxChunks) continue;
+    const size_t dyn = (size_t)((slice * esize + 15) & ~(int64_t)15);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(rows * cl));
+    cfg.blockDim = dim3(kStreamThreads);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (bf16) {
+      e = cudaFuncSetAttribute(k_softmax_smem<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+      if (e != cudaSuccess) return e;
+      return cudaLaunchKernelEx(&cfg, k_softmax_smem<uint16_t>, x, ld, V, temperature, out, slice);
+    }
+    e = cudaFuncSetAttribute(k_softmax_smem<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, k_softmax_smem<float>, x, ld, V, temperature, out, slice);
+  }
+  // larger rows: the streaming kernel (each slice read twice)
   // slices of whole 16-byte vectors: a multiple of 8 elements
   const int64_t slice = (((V + kSoftCL - 1) / kSoftCL) + 7) & ~(int64_t)7;
   cudaLaunchConfig_t cfg{};

@@ -93,7 +93,8 @@ def test_gather_logprobs(rows, V, dtype):
 # ---- softmax -------------------------------------------------------------------------------
 
 @pytest.mark.parametrize("rows,V,dtype", [(8, 1024, "f32"), (5, 40000, "f32"), (6, 128256, "bf16"),
-                                          (3, 201088, "bf16"), (4, 151936, "f32"), (3, 17, "bf16")])
+                                          (3, 201088, "bf16"), (4, 151936, "f32"), (3, 17, "bf16"),
+                                          (2, 300000, "f32")])
 def test_softmax_temp(rows, V, dtype):
     rng = np.random.default_rng(rows * 7 + V)
     d = _rand_logits(rng, rows, V, dtype)
@@ -101,6 +102,29 @@ def test_softmax_temp(rows, V, dtype):
     T[0] = 0.0  # greedy row
     got = tv.softmax_temp(dev_logits(d), dev(T)).cpu().numpy()
     ref = oracle.softmax_temp(d["logits"], T)
+    np.testing.assert_allclose(got, ref, **TOL[dtype])
+    np.testing.assert_allclose(got.sum(-1), 1.0, rtol=1e-5)
+
+
+@pytest.mark.parametrize("V,dtype", [(1001, "bf16"), (65539, "bf16"), (40001, "f32")])
+def test_softmax_temp_padded_rows(V, dtype):
+    # 16-byte aligned rows (ld padded) whose vocabulary ends inside a vector: the staged
+    # slices end on a ragged tail read from global memory
+    rng = np.random.default_rng(V)
+    rows = 5
+    x = rng.standard_normal((rows, V)).astype(np.float32) * np.float32(2.0)
+    if dtype == "bf16":
+        x = synth.f32_from_bf16_bits(synth.bf16_bits_from_f32(x))
+    T = rng.uniform(0.3, 1.5, rows).astype(np.float32)
+    T[1] = 0.0
+    ld = (V + 7) // 8 * 8
+    full = np.zeros((rows, ld), np.float32)
+    full[:, :V] = x
+    t = torch.from_numpy(full).cuda()
+    if dtype == "bf16":
+        t = t.to(torch.bfloat16)
+    got = tv.softmax_temp(t[:, :V], dev(T)).cpu().numpy()
+    ref = oracle.softmax_temp(x, T)
     np.testing.assert_allclose(got, ref, **TOL[dtype])
     np.testing.assert_allclose(got.sum(-1), 1.0, rtol=1e-5)
 
