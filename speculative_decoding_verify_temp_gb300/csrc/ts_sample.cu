@@ -548,16 +548,12 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
       const int nvf = nc / N;
       auto vec_at = [&](int vi) -> uint4 { return stage_vec(sv, c0, nc, nvf, vi); };
       // warp w takes the stage's vectors 128 w .. 128 w + 127, lane l those l + 32 u; the
-      // warp frees the slot once its vectors are in registers (the first stage of a large
-      // top-k stays until its threshold search has read it in place)
+      // warp frees the slot once its vectors are in registers
       uint4 rv[kRVecs];
 #pragma unroll
       for (int u = 0; u < kRVecs; ++u) rv[u] = vec_at(vbase + u * 32);
-      const bool hold = kn.kind == kRowTopK && c == 0 && k > kRCons;
-      if (!hold) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[slot]);
-      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[slot]);
       float vmv[kRVecs];
 #pragma unroll
       for (int u = 0; u < kRVecs; ++u) {
@@ -598,14 +594,19 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
                 kRStageVecs, [&](int i) { return sm.w.t.u.tkeys[i]; }, (uint32_t)k, bf16 ? 2 : 4,
                 sm.sc);
           } else {
-            const E* se = reinterpret_cast<const E*>(sv);
+            // the stage's order keys, from registers into the (still empty) candidate area
+            uint32_t* skeys = reinterpret_cast<uint32_t*>(sm.w.cross);
+#pragma unroll
+            for (int u = 0; u < kRVecs; ++u) {
+              float xv[N];
+              SVec<E>::unpack(rv[u], xv);
+#pragma unroll
+              for (int q = 0; q < N; ++q)
+                skeys[(vbase + u * 32) * N + q] = (xv[q] > -INFINITY) ? fkey(xv[q]) : 0u;
+            }
+            cbar();
             t0 = sel::select_bound<kRCons, sel::ConsumerBar>(
-                nc,
-                [&](int i) {
-                  const float v = (i < nvf * N) ? SVec<E>::at(se, i) : SVec<E>::at(xr, c0 + i);
-                  return (v > -INFINITY) ? fkey(v) : 0u;
-                },
-                (uint32_t)k, bf16 ? 2 : 4, sm.sc);
+                nc, [&](int i) { return skeys[i]; }, (uint32_t)k, bf16 ? 2 : 4, sm.sc);
           }
           if (tid == 0) sm.tau = t0;
           cbar();
@@ -721,10 +722,6 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
           }
         }
         if (out) sm.bad = 1;
-      }
-      if (hold) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[slot]);
       }
 
       // the candidate count is checked every few stages (and after the last): a stage adds
