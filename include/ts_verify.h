@@ -32,7 +32,11 @@
  *    returns TS_ERR_INVALID_ARG / TS_ERR_UNSUPPORTED_DTYPE and enqueues nothing. A
  *    failed launch returns TS_ERR_CUDA. ts_last_error_message() (thread-local) gives
  *    the reason for the last failure of the calling thread.
- *  - Limits: 1 <= vocab <= TS_MAX_VOCAB, 0 <= D <= TS_MAX_DRAFT, batch >= 1.
+ *  - Limits: 1 <= vocab <= TS_MAX_VOCAB, 0 <= D <= TS_MAX_DRAFT, batch >= 1. Rows the
+ *    streaming kernels cannot take (not 16-byte aligned, or longer than they stage)
+ *    go to a cluster-staged kernel that holds at most 655360 bf16 / 327680 fp32
+ *    tokens a row: ts_softmax_temp, ts_topk_topp_renorm and ts_chain_spec_sampling
+ *    reject larger such rows with TS_ERR_INVALID_ARG.
  *  - Inputs with NaN are outside the contract (no fault; results unspecified).
  */
 #ifndef TS_VERIFY_H
