@@ -8,13 +8,13 @@
 namespace tsv {
 
 constexpr int kMaxSplits = 64;  // row splits of the streaming kernels
-constexpr int kSTopK = 1024;  // largest top_k the split-row sampling kernels serve
-constexpr int kSVecs = 8;     // 16-byte vectors per thread of a chunk (kept in registers)
+constexpr int kSTopK = 1024;  // largest top_k the row kernel's candidate lists serve
+constexpr int kSVecs = 8;     // 16-byte vectors a thread covers in a 32 KB chunk
 constexpr int kSThreads = 256;
 
-// Chunks of a row of V elements of `esize` bytes for the split-row sampling kernels:
-// 256 threads x 8 vectors = 32 KB each. Returns false if a row needs more than
-// kMaxSplits chunks.
+// 32 KB chunks (256 threads x 8 vectors) of a row of V elements of `esize` bytes: the row
+// kernel keeps kSTopK workspace slots per chunk for a row (per-range masses of its
+// plain and top-p rows). Returns false if a row needs more than kMaxSplits chunks.
 inline bool sample_splits(int64_t V, int esize, int32_t* splits, int64_t* chunk) {
   const int64_t c = (int64_t)kSThreads * kSVecs * (16 / esize);
   *chunk = c;
@@ -56,12 +56,12 @@ struct Workspace {
   RowRes* rowres;     // [rows]
   DrawPart* dpart;    // [batch * kMaxSplits]
   uint64_t* cmass;    // [rows * 8] per-CTA masses of a cluster-staged row
-  uint32_t* flag;     // [rows] rows the split-row sampling kernel leaves to the staged one
+  uint32_t* flag;     // [rows] (reserved)
   uint32_t* ccount;   // [rows] candidates collected for a row
   uint32_t* best;     // [rows] Gumbel-max: the row's best score so far (order key, 0: none)
   uint32_t* work;     // [4] the row kernel's 64-bit next-row counter ([0..1], 8-byte
                       // aligned) and finished-CTA count ([2])
-  uint64_t* cand;     // [rows * cand_splits * kSTopK] per-row summaries of the split-row
+  uint64_t* cand;     // [rows * cand_splits * kSTopK] per-row range masses of the row
                       // kernel (vocab > 0 only)
   int64_t cand_splits;
   size_t bytes;
@@ -134,7 +134,7 @@ cudaError_t softmax_read_error(uint32_t* word, int clear);
 cudaError_t launch_logprobs_probs(const float* p, int64_t ld, int64_t V, int64_t rows,
                                   const int32_t* tokens, float* out, cudaStream_t s);
 
-// ---- split-row sampling kernel (ts_sample.cu) -----------------------------------
+// ---- row-streaming kernel (ts_sample.cu) -----------------------------------------
 
 // Target-only chain sampling from logits: a persistent row-streaming kernel that serves
 // every row (greedy ones included). Requires 16-byte aligned rows and vocab <=
@@ -191,7 +191,6 @@ struct StagedArgs {
   int32_t* accept_index;
   float* logprobs;
   int32_t skip_greedy;  // chain: greedy requests are handled by the streaming kernel
-  uint32_t* flags;      // chain: if set, only rows with flags[row] != 0 (cleared here)
   Workspace ws;
 };
 

@@ -1,6 +1,6 @@
-// CTA-level selection helpers for the split-row sampling kernel: exact scans and radix
-// selections over 64-bit composite keys (value descending, then token id ascending),
-// with masses summed exactly as three 32-bit digit counters.
+// CTA-level selection helpers for the row-streaming and cluster-staged kernels: exact
+// scans and radix selections over 64-bit composite keys (value descending, then token id
+// ascending), with masses summed exactly as three 32-bit digit counters.
 #pragma once
 
 #include <stdint.h>

@@ -518,9 +518,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
   float T = 1.f;
   if (a.mode != kRenorm && a.temperature) T = a.temperature[req];
   if (a.mode == kChain && a.skip_greedy && !(T >= kGreedyT)) return;  // a streaming pass has it
-  // rows the split-row kernel finished already (every CTA of the cluster reads the flag
-  // before the first cluster barrier; CTA 0 clears it after that barrier)
-  if (a.mode == kChain && a.flags && __ldcg(&a.flags[row]) == 0u) return;
   const int32_t D = a.D;
   const int32_t x = (a.mode == kChain && j < D) ? a.draft_tokens[req * D + j] : -1;
   const bool xvalid = x >= 0 && (int64_t)x < a.V;
@@ -653,7 +650,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_staged(StagedArgs a, int64_t sl
     }
   }
   cluster.sync();  // (1) partial statistics and thread maxima are visible
-  if (a.flags && crank == 0 && tid == 0) a.flags[row] = 0u;
   if (tid < 32) {
     const int lane = tid;
     float v = -INFINITY, m = -INFINITY, s = 0.f;
