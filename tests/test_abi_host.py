@@ -87,3 +87,34 @@ def test_invalid_arguments_are_rejected_before_launch(lib):
     a.accept_length = 256
     st = lib.ts_chain_spec_sampling(ctypes.byref(a), P(512), 1 << 20, None)
     assert st == 1 and "seed" in _err(lib)
+
+
+def test_staged_vocabulary_limit_is_rejected_before_launch(lib):
+    # rows the streaming kernels cannot take (here: an ld that breaks 16-byte alignment)
+    # go to the cluster-staged kernel, which holds at most 655360 bf16 / 327680 fp32
+    # tokens a row; longer rows are rejected on the host
+    P = ctypes.c_void_p
+    fake = P(256)
+    V = 700000
+    st = lib.ts_softmax_temp(fake, 1, 2, V, V + 1, None, fake, None)
+    assert st == 1 and "staged limit" in _err(lib)
+    V = 330000
+    st = lib.ts_topk_topp_renorm(fake, 2, V, V + 1, None, None, P(4096), None)
+    assert st == 1 and "staged limit" in _err(lib)
+    from speculative_decoding_verify_temp_gb300.tsverify import ChainArgs
+    a = ChainArgs()
+    a.target = 256
+    a.target_dtype = 1
+    a.target_is_logits = 1
+    a.batch, a.D, a.vocab, a.ld = 2, 1, 700000, 700000
+    a.draft_tokens = a.accepted_tokens = a.accept_length = 256
+    a.seed = a.offset = 256
+    st = lib.ts_chain_spec_sampling(ctypes.byref(a), P(512), 1 << 40, None)
+    assert st == 1 and "staged limit" in _err(lib)
+
+
+def test_in_place_renorm_needs_contiguous_rows(lib):
+    P = ctypes.c_void_p
+    p = P(4096)
+    st = lib.ts_topk_topp_renorm(p, 2, 100, 104, None, None, p, None)
+    assert st == 1 and "in-place" in _err(lib)
