@@ -99,7 +99,8 @@ ts_status ts_softmax_temp(const void* logits, ts_dtype dt, int64_t rows, int64_t
  * preceding kept mass is below top_p times the kept mass (the first token always).
  * The result is renormalised; dropped tokens are 0.
  * probs: [rows, ld] fp32 (non-negative); top_k: [rows] or NULL; top_p: [rows] or NULL;
- * probs_out: [rows, vocab] fp32 contiguous; may equal probs when ld == vocab. */
+ * probs_out: [rows, vocab] fp32 contiguous; may equal probs when ld == vocab. A row
+ * whose kept tokens carry no mass (in 2^-40 units of the row) is written as zeros. */
 ts_status ts_topk_topp_renorm(const float* probs, int64_t rows, int64_t vocab, int64_t ld,
                               const int32_t* top_k, const float* top_p, float* probs_out,
                               cudaStream_t stream);
