@@ -1,34 +1,41 @@
 // Row-streaming kernel for target-only chain sampling from logits (TokenSpeed
 // flashinfer.py verify(): sampling_argmax for greedy requests; softmax with temperature,
-// fused top-k/top-p renorm and chain_speculative_sampling_target_only for the others).
+// fused top-k/top-p renorm and chain_speculative_sampling_target_only for the others),
+// and, in its renorm mode, for top-k/top-p renormalisation of probability rows
+// (fused_topk_topp_renorm).
 //
-// A persistent CTA takes rows in turn. A producer warp streams each row through a ring
-// of kRNSt shared-memory stages of 16 KB (TMA bulk copies completing on mbarriers, the
-// next row's stages already in flight while a row is finished); 8 consumer warps keep
-// running row state as the stages arrive and finish the row after its last stage:
+// A persistent CTA (2 an SM) takes one row after another: chain rows from a shared
+// counter that runs over the rows in four cost tiers, longest kind first; renorm rows
+// (no workspace) from a tiered order that every CTA computes alike. A producer warp
+// streams each row through a ring of kRNSt shared-memory stages of 16 KB (bulk copies
+// completing on mbarriers, the next row's stages already in flight while a row is
+// finished); 8 consumer warps copy their vectors of a stage to registers, free the slot,
+// keep running row state, and finish the row after its last stage:
 //  - every row: maximum, argmax (lowest id), temperature-1 log-sum-exp;
 //  - top-k (k <= kSTopK): a candidate list in shared memory above a running threshold:
 //    first a lower bound of the row's k-th value from the first stage (its k-th largest
 //    vector maximum, or for k > 256 its k-th largest value), later the k-th largest
-//    candidate value whenever the list fills; at
-//    the end the row's top k, the top-p prefix within it, and the draw in token-id order
-//    by a radix walk over the ids;
-//  - neither knob: the mass of every warp step (32 consecutive vectors) relative to the
-//    step maximum; at the end the steps scaled to the row maximum locate the draw, and
-//    only that step is read again;
+//    candidate value whenever the list fills; at the end the row's top k, the top-p
+//    prefix within it, and the draw in token-id order by a radix walk over the ids;
+//  - neither knob: the mass of every warp's 128 vectors of a stage relative to their
+//    maximum; at the end these ranges, scaled to the row maximum, locate the draw, and
+//    only that range is read again;
 //  - top-p alone: a histogram over sixteenth-of-an-octave buckets on fixed edges
 //    (multiples of T ln 2 / 16) of the weights relative to their bucket's upper edge, so
-//    that no maximum is needed while streaming; at the end the bucket where the ordered
-//    mass crosses top_p, one more read of the row for the whole-bucket masses per warp
-//    step and the crossing bucket's elements (resolved exactly), then the draw.
-// Rows the summaries cannot serve (top_k above kSTopK, candidate overflow, a row maximum
-// far above the first stage's, an oversized crossing bucket) take a general path: radix
+//    that no maximum is needed while streaming (probabilities: linear buckets from the
+//    float's exponent and leading mantissa bits); at the end the bucket where the ordered
+//    mass crosses top_p, one more read of the row for the whole-bucket masses per range
+//    and the crossing bucket's elements (resolved exactly), then the draw.
+// Renorm rows are read once more through the ring to write max(p, 0) / Z or 0. Rows the
+// summaries cannot serve (top_k above kSTopK, candidate overflow, a row maximum far
+// above the first stage's, an oversized crossing bucket) take a general path: radix
 // selections over the whole row, read again from memory.
 //
-// Weights are 2^((x - M) log2(e) / T) for the row maximum M; masses that decide a
-// selection are sums of floor(w * 2^40); composite keys order tokens by value, then by
-// lowest id. Every wait on an mbarrier is bounded; a wait that gives up sets an error
-// word and the kernel carries on (ts_device_error reports it).
+// Weights are 2^((x - M) log2(e) / T) for the row maximum M (probabilities: p); masses
+// that decide a selection are sums of floor(w * 2^40); composite keys order tokens by
+// value, then by lowest id. Every wait on an mbarrier is bounded by the SM clock; a wait
+// that gives up sets an error word (ts_device_error reports it), after which the
+// producer issues no more copies and waits for those in flight before the CTA exits.
 #include <stdint.h>
 
 #include "ts_common.cuh"
