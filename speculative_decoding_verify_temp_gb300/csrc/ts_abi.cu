@@ -103,8 +103,6 @@ size_t workspace_layout(int64_t batch, int32_t R, int64_t vocab, void* base, Wor
   w.rowres = reinterpret_cast<RowRes*>(take(rows * sizeof(RowRes)));
   w.dpart = reinterpret_cast<DrawPart*>(take((size_t)batch * kMaxSplits * sizeof(DrawPart)));
   w.cmass = reinterpret_cast<uint64_t*>(take(rows * 8 * sizeof(uint64_t)));
-  w.flag = reinterpret_cast<uint32_t*>(take(rows * 4));
-  w.ccount = reinterpret_cast<uint32_t*>(take(rows * 4));
   w.best = reinterpret_cast<uint32_t*>(take(rows * 4));
   w.work = reinterpret_cast<uint32_t*>(take(4 * 4));
   if (vocab > 0) {

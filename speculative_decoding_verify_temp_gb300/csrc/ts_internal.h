@@ -56,8 +56,6 @@ struct Workspace {
   RowRes* rowres;     // [rows]
   DrawPart* dpart;    // [batch * kMaxSplits]
   uint64_t* cmass;    // [rows * 8] per-CTA masses of a cluster-staged row
-  uint32_t* flag;     // [rows] (reserved)
-  uint32_t* ccount;   // [rows] candidates collected for a row
   uint32_t* best;     // [rows] Gumbel-max: the row's best score so far (order key, 0: none)
   uint32_t* work;     // [4] the row kernel's 64-bit next-row counter ([0..1], 8-byte
                       // aligned) and finished-CTA count ([2])
