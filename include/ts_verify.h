@@ -78,10 +78,22 @@ const char* ts_last_error_message(void);
 
 /* Synchronises the current device and reads (then, if clear != 0, clears) the
  * library's device error word: 0 if no bounded wait ever gave up; otherwise bits 0-7
- * come from the cluster-staged kernels, bits 8-15 from the row-streaming kernel and
- * bits 16-23 from the staged softmax. Returns TS_ERR_TIMEOUT if a wait gave up,
- * TS_ERR_CUDA if the read failed. A diagnostic, not part of the hot path. */
+ * come from the cluster-staged kernels, bits 8-15 from the renorm row kernel, bits
+ * 16-23 from the staged softmax and bits 24-31 from the chain kernel (bit 24: a stage
+ * wait gave up; bit 25: a CTA's wait for its own copies in flight ran out). The word is
+ * sticky until cleared, but it only reports: a later call is not affected by it.
+ * Returns TS_ERR_TIMEOUT if a wait gave up, TS_ERR_CUDA if the read failed. A
+ * diagnostic, not part of the hot path. */
 ts_status ts_device_error(uint32_t* word_host, int clear);
+
+/* Sets how many SM clock cycles a stage wait of the chain kernel (ts_chain_spec_sampling
+ * from logits) may take before it gives up; 0 restores the default of 2^32 (about 2 s).
+ * Process-wide; takes effect for calls enqueued afterwards. A CTA whose wait gives up
+ * issues no more copies, waits (on the long budget) for the copies it has in flight,
+ * and leaves the requests it had not finished with accept_length = 0; their other
+ * outputs are unspecified. ts_device_error then reports TS_ERR_TIMEOUT. A diagnostic:
+ * it exists so that this path can be tested. */
+ts_status ts_set_wait_cycles(uint64_t cycles);
 
 /* Temperature softmax [TS-FI verify(): softmax(logits, temperature)].
  * probs_out[r, i] = exp((x_ri - M_r)/T_r) / sum_k exp((x_rk - M_r)/T_r), M_r the row max;

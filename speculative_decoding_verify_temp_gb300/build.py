@@ -1,6 +1,6 @@
 """Builds libtsverify.so (the C ABI and its sm_103a kernels) in the package directory.
 
-Four translation units are compiled in parallel with nvcc for sm_103a and linked
+Five translation units are compiled in parallel with nvcc for sm_103a and linked
 into one shared library with the CUDA runtime linked statically, so the library
 depends only on the driver. Objects go to ``_build/`` next to the sources.
 """
@@ -15,8 +15,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtsverify.so")
-SOURCES = ["ts_abi.cu", "ts_stream.cu", "ts_sample.cu", "ts_staged.cu"]
-HEADERS = ["ts_common.cuh", "ts_internal.h", "ts_select.cuh"]
+SOURCES = ["ts_abi.cu", "ts_stream.cu", "ts_sample.cu", "ts_staged.cu", "ts_chain.cu"]
+HEADERS = ["ts_common.cuh", "ts_internal.h", "ts_select.cuh", "ts_rowutil.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]
 

@@ -3,7 +3,9 @@
 // the kernels of ts_stream.cu, ts_sample.cu and ts_staged.cu.
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 
+#include <atomic>
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -14,6 +16,10 @@
 namespace {
 
 thread_local char g_msg[512] = "";
+
+// SM clock cycles a stage wait of the chain kernel may take before it gives up.
+constexpr uint64_t kDefaultWaitCycles = (uint64_t)1 << 32;
+std::atomic<uint64_t> g_wait_cycles{kDefaultWaitCycles};
 
 ts_status fail(ts_status st, const char* fmt, ...) {
   va_list ap;
@@ -105,6 +111,8 @@ size_t workspace_layout(int64_t batch, int32_t R, int64_t vocab, void* base, Wor
   w.cmass = reinterpret_cast<uint64_t*>(take(rows * 8 * sizeof(uint64_t)));
   w.best = reinterpret_cast<uint32_t*>(take(rows * 4));
   w.work = reinterpret_cast<uint32_t*>(take(4 * 4));
+  w.order = reinterpret_cast<uint32_t*>(take(rows * 4));
+  w.creq = reinterpret_cast<uint32_t*>(take((size_t)batch * 4));
   if (vocab > 0) {
     // sized for fp32 rows, which have the most chunks (at most kMaxSplits)
     int64_t chunk = 0;
@@ -137,15 +145,22 @@ ts_status ts_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t strea
 
 const char* ts_last_error_message(void) { return g_msg; }
 
+ts_status ts_set_wait_cycles(uint64_t cycles) {
+  g_wait_cycles.store(cycles ? cycles : kDefaultWaitCycles, std::memory_order_relaxed);
+  g_msg[0] = 0;
+  return TS_OK;
+}
+
 ts_status ts_device_error(uint32_t* word_host, int clear) {
   if (!word_host) return fail(TS_ERR_INVALID_ARG, "word_host is NULL");
   uint32_t w = 0;
   cudaError_t e = tsv::staged_read_error(&w, clear);
-  uint32_t w2 = 0, w3 = 0;
+  uint32_t w2 = 0, w3 = 0, w4 = 0;
   if (e == cudaSuccess) e = tsv::row_read_error(&w2, clear);
   if (e == cudaSuccess) e = tsv::softmax_read_error(&w3, clear);
+  if (e == cudaSuccess) e = tsv::chain_read_error(&w4, clear);
   if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
-  w |= (w2 << 8) | (w3 << 16);
+  w |= (w2 << 8) | (w3 << 16) | (w4 << 24);
   *word_host = w;
   if (w) return fail(TS_ERR_TIMEOUT, "a bounded device wait gave up (word 0x%x)", w);
   g_msg[0] = 0;
@@ -341,6 +356,9 @@ ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t
     sa.accept_index = p->accept_index;
     sa.logprobs = p->logprobs;
     sa.ws = a.ws;
+    sa.wait_cycles = g_wait_cycles.load(std::memory_order_relaxed);
+    if (getenv("TS_CHAIN_KERNEL") && atoi(getenv("TS_CHAIN_KERNEL")) == 2)
+      return launched(tsv::launch_chain(sa, stream), "row-streaming chain launch");
     return launched(tsv::launch_sample(sa, stream), "row-streaming sampling launch");
   } else if (p->temperature) {
     // Greedy requests need only the argmax of each row: a streaming pass handles them,

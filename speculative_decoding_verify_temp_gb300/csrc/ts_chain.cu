@@ -1,0 +1,1450 @@
+// Row-streaming kernel for target-only chain sampling from logits (TokenSpeed
+// flashinfer.py verify(): sampling_argmax for greedy requests; softmax with temperature,
+// fused top-k/top-p renorm and chain_speculative_sampling_target_only for the others).
+//
+// Two launches per call:
+//  - k_chain_plan (one CTA) orders the rows by cost tier (top-p and general rows first,
+//    then large top-k rows, then the other sampled rows, greedy rows last), so that the
+//    step ends on short rows, and clears the per-launch state: the row claim counter, the
+//    per-request row counts and accept_length (0 until a request's chain is written).
+//  - k_chain: persistent CTAs (two an SM) of 8 warps, all of which compute. Thread 0 also
+//    keeps a ring of kCNSt shared-memory stages of 16 KB filled with bulk copies that
+//    complete on mbarriers: after its warp has read stage g it refills the slot of stage
+//    g - 1 (once every warp has released it), claiming rows from the planned order one
+//    row ahead. Each warp copies its four 16-byte vectors of a stage to registers, frees
+//    the slot, and keeps running row state in a loop specialised for the row's kind:
+//     - every row: maximum and its first token id (lowest id among equal values), and
+//       the temperature-1 log-sum-exp when logprobs are asked for;
+//     - top-k (k <= kSTopK): a candidate list in shared memory above a threshold: first a
+//       lower bound of the row's k-th value from the first stage, later the k-th largest
+//       candidate value whenever the list fills; at the end the row's top k, the top-p
+//       prefix within it, and the draw in token-id order;
+//     - neither knob: the mass of every warp's 128 vectors of a stage relative to their
+//       maximum; at the end these ranges, scaled to the row maximum, locate the draw, and
+//       only that range is read again;
+//     - top-p alone: three passes over the row, the first from HBM, the other two from L2
+//       (the first two passes load with an evict-last cache policy, every other load
+//       evict-first). Pass 1: a histogram of the weights over 32 octaves below a window
+//       top set by the first stage's maximum, one column of bins per thread (no shared
+//       atomics); it locates the octave where the ordered mass crosses top_p. Pass 2 (the
+//       row maximum now known): the row's mass and a histogram over sixteenths of the two
+//       octaves around the crossing, which locates the crossing sixteenth. Pass 3: the
+//       kept mass of each warp range above the two sixteenths around the crossing and
+//       the elements within them, resolved exactly; then the draw.
+//    Rows the summaries cannot serve (top_k above kSTopK, candidate overflow, a top-p
+//    crossing outside its windows) take a general path: radix selections over the whole
+//    row, read again from memory.
+//
+// Weights are 2^((x - M) log2(e) / T) for the row maximum M; masses that decide a
+// selection are sums of floor(w * 2^40); composite keys order tokens by value, then by
+// lowest id. Every wait on an mbarrier is bounded: a stage wait by the launch's
+// wait_cycles of SM clock. A wait that gives up sets the CTA's abort flag and the
+// library's sticky error word (ts_device_error); the CTA then issues no more copies,
+// leaves its current row unwritten at the next row boundary, waits for the copies it has
+// in flight and exits. The requests it leaves keep accept_length = 0 from the planning
+// launch, and the next launch starts from a clean state.
+#include <stdint.h>
+
+#include <type_traits>
+
+#include "ts_common.cuh"
+#include "ts_internal.h"
+#include "ts_rowutil.cuh"
+#include "ts_select.cuh"
+
+namespace tsv {
+namespace {
+
+constexpr int kCC = 224;                       // compute threads (7 warps)
+constexpr int kCW = kCC / 32;
+constexpr int kCThreads = kCC + 32;            // + the producer warp
+constexpr int kCNSt = 4;                       // ring stages
+constexpr int kCVecs = 4;                      // vectors per compute thread and stage
+constexpr int kCStageVecs = kCC * kCVecs;      // 896 vectors of 16 bytes
+constexpr int kCStageBytes = kCStageVecs * 16;  // 14336
+constexpr int kCCap = 4096;                    // candidate / crossing list capacity
+constexpr int kCHalf = kCCap / 2;
+constexpr int kCSmallE = 4;                    // lists of up to 128 candidates: one warp
+constexpr int kCMerge = 128;                   // top-k: k up to this takes its first bound
+                                               // from the first stage's vector maxima and
+                                               // is compacted only at the end
+constexpr int kPB = 32;                        // top-p bins per level
+constexpr int kPHead = 8;                      // octaves of the window above the first stage
+constexpr long long kCDrainCycles = 1ll << 32;
+constexpr uint32_t kNoRow = 0xFFFFFFFFu;
+constexpr uint32_t kRowMask = (1u << 30) - 1u;
+constexpr double kCInvFx = 1.0 / 1099511627776.0;  // 2^-40
+
+enum CKind : int { kCGreedy = 0, kCTopK = 1, kCPlain = 2, kCTopP = 3, kCGeneral = 4 };
+
+template <int K>
+using KindTag = std::integral_constant<int, K>;
+
+}  // namespace
+
+static __device__ unsigned int g_chain_err;
+
+namespace {
+
+struct CKnobs {
+  float T, tp;
+  int32_t k;
+  int kind;
+};
+
+// The request's knobs and the way its rows are served. top_p <= 0 keeps only the argmax,
+// which is the greedy distribution.
+__device__ __forceinline__ CKnobs cknobs(const SampleArgs& a, int64_t req) {
+  CKnobs kn;
+  kn.T = a.temperature ? a.temperature[req] : 1.f;
+  kn.k = a.top_k ? a.top_k[req] : 0;
+  kn.tp = a.top_p ? a.top_p[req] : 1.f;
+  const bool tk = kn.k > 0 && (int64_t)kn.k < a.V;
+  if (!(kn.T >= kGreedyT)) kn.kind = kCGreedy;
+  else if (tk) kn.kind = (kn.k <= kSTopK) ? kCTopK : kCGeneral;
+  else if (kn.tp < 1.f) kn.kind = (kn.tp > 0.f) ? kCTopP : kCGreedy;
+  else kn.kind = kCPlain;
+  return kn;
+}
+
+__device__ __forceinline__ int ctier(const CKnobs& kn) {
+  if (kn.kind == kCTopP || kn.kind == kCGeneral) return 0;
+  if (kn.kind == kCTopK && kn.k > kCMerge) return 1;
+  return (kn.kind != kCGreedy) ? 2 : 3;
+}
+
+__device__ __forceinline__ bool ld_abort(const int32_t* f) {
+  return *reinterpret_cast<const volatile int32_t*>(f) != 0;
+}
+
+// Waits for the phase of `bar` with the given parity; gives up after `budget` cycles of
+// this SM's clock or as soon as the CTA's abort flag is up, raising it (and the sticky
+// error word). Returns whether the phase completed.
+__device__ __forceinline__ bool cwait(uint64_t* bar, uint32_t parity, unsigned long long budget,
+                                      int32_t* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0u &&
+        (ld_abort(abort_flag) || (unsigned long long)(clock64() - t0) > budget)) {
+      *reinterpret_cast<volatile int32_t*>(abort_flag) = 1;
+      atomicOr(&g_chain_err, 1u);
+      return false;
+    }
+  }
+}
+
+// Waits, on the long budget only, for a copy this CTA issued: no copy may be in flight
+// when the CTA exits.
+__device__ __forceinline__ void cdrain(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kCDrainCycles) {
+      atomicOr(&g_chain_err, 2u);
+      return;
+    }
+}
+
+// 1-D bulk copy global -> shared with an L2 cache policy.
+__device__ __forceinline__ void bulk_g2s_pol(void* dst, const void* src, uint32_t bytes,
+                                             uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+// The compute warps' barrier (named barrier 1; the producer warp never takes part).
+struct CBar {
+  __device__ __forceinline__ static void sync() { asm volatile("bar.sync 1, 224;" ::: "memory"); }
+};
+static_assert(kCC == 224, "CBar counts 224 threads");
+__device__ __forceinline__ void cbar() { CBar::sync(); }
+
+struct alignas(16) CSmem {
+  uint64_t full[kCNSt];
+  uint64_t empty[kCNSt];
+  int64_t srow[kCNSt];
+  sel::Scratch sc;
+  union {
+    uint64_t list[kCCap];       // top-k candidates; top-p crossing elements
+    float hist[kPB * kCC];      // top-p: bin b of compute thread t at b * kCC + t
+    struct {
+      uint64_t lo[kCHalf];
+      uint32_t keys[kCStageVecs];  // top-k: the first stage's vector maxima
+    } tk;
+  } w;
+  double dscan[32];
+  double hb[kPB];
+  float hw[kCW][kPB];
+  uint64_t red2[2][kCW];
+  float redf[3][kCW];
+  int32_t redi[kCW];
+  uint32_t lcnt, tau;
+  int32_t bad, abort_flag, owner, am;
+  float M, S1, uj, uD, vx;
+  int32_t pbi;
+  int32_t gtop, gl, gh;
+  uint64_t res_u, zall, ptarget;
+  double res_d;
+};
+
+// The ragged last vector of a row (n < N valid elements from e0 on), read from global
+// memory and padded with -inf; kept out of line so that the stage loops stay small.
+template <typename E>
+__device__ __noinline__ uint4 ragged_vec(const E* xr, int e0, int n) {
+  uint32_t wv[4] = {SVec<E>::kNegInfWord, SVec<E>::kNegInfWord, SVec<E>::kNegInfWord,
+                    SVec<E>::kNegInfWord};
+  for (int q = 0; q < n; ++q) {
+    if (sizeof(E) == 2) {
+      const uint32_t h = reinterpret_cast<const uint16_t*>(xr)[e0 + q];
+      wv[q >> 1] = (q & 1) ? ((wv[q >> 1] & 0x0000FFFFu) | (h << 16))
+                           : ((wv[q >> 1] & 0xFFFF0000u) | h);
+    } else {
+      wv[q] = reinterpret_cast<const uint32_t*>(xr)[e0 + q];
+    }
+  }
+  return make_uint4(wv[0], wv[1], wv[2], wv[3]);
+}
+
+// two CTAs an SM: their rings and state fit the SM's 228 KB of shared memory (1 KB of it
+// reserved per CTA)
+static_assert(2 * (kCNSt * kCStageBytes + sizeof(CSmem) + 1024) <= 233472, "two CTAs an SM");
+
+// Orders the rows by cost tier (stable within a tier) and clears the per-launch state. A
+// request's rows share its knobs, so the order is built over requests: request b at
+// position p of the order owns the claim positions p R .. p R + R - 1. Each entry holds
+// the row and, in bits 30-31, its number of passes minus one.
+__global__ void __launch_bounds__(1024) k_chain_plan(SampleArgs a) {
+  __shared__ uint32_t cnt[4];
+  __shared__ uint32_t wc[32][4];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t B = a.rows / a.R;
+  if (tid < 4) cnt[tid] = 0u;
+  if (tid == 0) {
+    a.ws.work[0] = 0u;  // top-k candidates collected (all rows)
+    a.ws.work[1] = 0u;  // top-k lists compacted at the end
+    a.ws.work[2] = 0u;  // rows the general path served
+    a.ws.work[3] = 0u;  // row claims
+  }
+  uint32_t c0 = 0u, c1 = 0u, c2 = 0u, c3 = 0u;
+  for (int64_t b = tid; b < B; b += 1024) {
+    a.ws.creq[b] = 0u;
+    a.accept_length[b] = 0;
+    const int t = ctier(cknobs(a, b));
+    c0 += (t == 0);
+    c1 += (t == 1);
+    c2 += (t == 2);
+    c3 += (t == 3);
+  }
+  __syncthreads();
+  if (c0) atomicAdd(&cnt[0], c0);
+  if (c1) atomicAdd(&cnt[1], c1);
+  if (c2) atomicAdd(&cnt[2], c2);
+  if (c3) atomicAdd(&cnt[3], c3);
+  __syncthreads();
+  uint32_t r0 = 0u, r1 = cnt[0], r2 = cnt[0] + cnt[1], r3 = cnt[0] + cnt[1] + cnt[2];
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int64_t bb = 0; bb < B; bb += 1024) {
+    const int64_t b = bb + tid;
+    int t = 4;
+    uint32_t np = 0u;
+    if (b < B) {
+      const CKnobs kn = cknobs(a, b);
+      t = ctier(kn);
+      np = (kn.kind == kCTopP) ? 2u : 0u;  // passes - 1
+    }
+    uint32_t before = 0u;
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t m = __ballot_sync(0xffffffffu, t == q);
+      if (lane == 0) wc[warp][q] = (uint32_t)__popc(m);
+      if (t == q) before = (uint32_t)__popc(m & lt);
+    }
+    __syncthreads();
+    if (t < 4) {
+      uint32_t pos = (t == 0 ? r0 : t == 1 ? r1 : t == 2 ? r2 : r3) + before;
+      for (int w = 0; w < warp; ++w) pos += wc[w][t];
+      for (int32_t jj = 0; jj < a.R; ++jj)
+        a.ws.order[(int64_t)pos * a.R + jj] = (uint32_t)(b * a.R + jj) | (np << 30);
+    }
+    for (int w = 0; w < 32; ++w) {
+      r0 += wc[w][0];
+      r1 += wc[w][1];
+      r2 += wc[w][2];
+      r3 += wc[w][3];
+    }
+    __syncthreads();
+  }
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
+  extern __shared__ __align__(128) unsigned char dsm[];
+  constexpr int N = SVec<E>::N;
+  constexpr int SE = kCStageBytes / (int)sizeof(E);  // elements per stage
+  unsigned char* ring = dsm;
+  CSmem& sm = *reinterpret_cast<CSmem*>(dsm + kCNSt * kCStageBytes);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t V = a.V;
+  const int nst = (int)((V + SE - 1) / SE);  // stages per pass
+  const unsigned long long budget = a.wait_cycles;
+  constexpr bool bf16 = sizeof(E) == 2;
+  constexpr int lowv = bf16 ? 16 : 0;  // value key bits below this follow from the higher ones
+
+  if (tid == 0) {
+    for (int s = 0; s < kCNSt; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], kCW);
+    }
+    fence_mbar_init();
+    sm.abort_flag = 0;
+  }
+  __syncthreads();
+
+  // ---- producer warp: the ring's refills ------------------------------------------------
+  if (warp == kCW) {
+    if (lane == 0) {
+      uint64_t pol_first, pol_last;
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_first));
+      asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_last));
+      auto order_at = [&](uint32_t pos) -> uint32_t {
+        return (pos < (uint64_t)a.rows) ? __ldcg(&a.ws.order[pos]) : kNoRow;
+      };
+      uint32_t gi = 0;  // stages issued
+      // rows are claimed one row ahead, so that the claim's latency is never waited for
+      uint32_t inext = order_at(atomicAdd(&a.ws.work[3], 1u));
+      uint32_t ipos = atomicAdd(&a.ws.work[3], 1u);
+      for (;;) {
+        const uint32_t e = inext;
+        if (e == kNoRow) {  // one last stage tells the consumers to stop
+          const int slot = (int)(gi % kCNSt);
+          const uint32_t use = gi / kCNSt;
+          if ((use > 0 && !cwait(&sm.empty[slot], (use - 1) & 1u, budget, &sm.abort_flag)) ||
+              ld_abort(&sm.abort_flag))
+            break;
+          sm.srow[slot] = -1;
+          mbar_arrive_expect_tx(&sm.full[slot], 0u);
+          ++gi;
+          break;
+        }
+        const int64_t irow = (int64_t)(e & kRowMask);
+        const int inp = (int)(e >> 30) + 1;
+        inext = order_at(ipos);
+        ipos = atomicAdd(&a.ws.work[3], 1u);
+        const unsigned char* src =
+            reinterpret_cast<const unsigned char*>(a.x) + irow * a.ld * (int64_t)sizeof(E);
+        bool ok = true;
+        for (int pass = 0; pass < inp && ok; ++pass) {
+          // top-p rows: the first two passes are kept in L2 for the ones that follow
+          const uint64_t pol = (inp > 1 && pass < 2) ? pol_last : pol_first;
+          for (int c = 0; c < nst; ++c, ++gi) {
+            const int slot = (int)(gi % kCNSt);
+            const uint32_t use = gi / kCNSt;
+            // after an error nothing more is issued (a slot may still be in use)
+            if ((use > 0 && !cwait(&sm.empty[slot], (use - 1) & 1u, budget, &sm.abort_flag)) ||
+                ld_abort(&sm.abort_flag)) {
+              ok = false;
+              break;
+            }
+            const int64_t nc = min((int64_t)SE, V - (int64_t)c * SE);
+            const uint32_t bytes = (uint32_t)((nc * (int64_t)sizeof(E)) & ~(int64_t)15);
+            sm.srow[slot] = irow;
+            mbar_arrive_expect_tx(&sm.full[slot], bytes);
+            if (bytes)
+              bulk_g2s_pol(ring + slot * kCStageBytes, src + (int64_t)c * kCStageBytes, bytes,
+                           &sm.full[slot], pol);
+          }
+        }
+        if (!ok) break;
+      }
+      // no copy of this CTA may still be in flight when it exits: wait for the last use of
+      // every slot (normally complete already)
+      for (uint32_t h = (gi > (uint32_t)kCNSt ? gi - (uint32_t)kCNSt : 0u); h < gi; ++h)
+        cdrain(&sm.full[h % kCNSt], (h / kCNSt) & 1u);
+    }
+    return;
+  }
+
+  // ---- the rows -----------------------------------------------------------------------------
+  const uint4 ninf = make_uint4(SVec<E>::kNegInfWord, SVec<E>::kNegInfWord,
+                                SVec<E>::kNegInfWord, SVec<E>::kNegInfWord);
+  const int64_t nvr = V / N;  // whole vectors of a row; the rest is a scalar tail
+  const int64_t nvall = (V + N - 1) / N;
+  const int vbase = warp * (kCVecs * 32) + lane;  // warp w: a stage's vectors 128 w ..
+  uint32_t g = 0;                                 // the next stage to consume
+
+  auto stage_ptr = [&](uint32_t gg) -> const uint4* {
+    const int slot = (int)(gg % kCNSt);
+    cwait(&sm.full[slot], (gg / kCNSt) & 1u, budget, &sm.abort_flag);
+    return reinterpret_cast<const uint4*>(ring + slot * kCStageBytes);
+  };
+  auto stage_release = [&](uint32_t gg) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[gg % kCNSt]);
+  };
+
+  for (;;) {
+    int64_t row;
+    {
+      const int slot = (int)(g % kCNSt);
+      cwait(&sm.full[slot], (g / kCNSt) & 1u, budget, &sm.abort_flag);
+      row = *reinterpret_cast<volatile int64_t*>(&sm.srow[slot]);
+    }
+    cbar();
+    const bool ab = ld_abort(&sm.abort_flag);
+    if (tid == 0) {
+      sm.lcnt = 0;
+      sm.bad = 0;
+      sm.tau = 0;
+    }
+    cbar();
+    if (ab || row < 0 || row >= a.rows) break;
+
+    const int64_t req = row / a.R;
+    const int32_t j = (int32_t)(row % a.R);
+    const CKnobs kn = cknobs(a, req);
+    const E* xr = reinterpret_cast<const E*>(a.x) + row * a.ld;
+    const uint4* rp = reinterpret_cast<const uint4*>(xr);
+    const int32_t D = a.D;
+    const int32_t x = (j < D) ? a.draft_tokens[req * D + j] : -1;
+    const bool xvalid = x >= 0 && (int64_t)x < V;
+    const float sl2 = (kn.kind == kCGreedy) ? 0.f : __fdiv_rn(kLog2e, kn.T);
+    const float s16 = sl2 * 16.f;  // sixteenths of an octave per logit unit
+    const int32_t k = kn.k;
+    uint64_t* const rowslots = a.ws.cand + row * a.ws.cand_splits * (int64_t)kSTopK;
+    const bool want_lse = a.logprobs != nullptr;
+
+    // vector vi of the stage held at sv (first element c0, nc elements, nvf whole
+    // vectors); the ragged last vector of the row comes from global memory, padded with
+    // -inf
+    auto stage_vec = [&](const uint4* sv, int c0, int nc, int vi) -> uint4 {
+      const int nvf = nc / N;
+      if (vi < nvf) return sv[vi];
+      if (vi > nvf || nc % N == 0) return ninf;
+      return ragged_vec<E>(xr, c0 + vi * N, nc - nvf * N);
+    };
+    auto load_vec = [&](int64_t vi, float* xv) {
+      if (vi < nvr) {
+        SVec<E>::unpack(__ldcg(rp + vi), xv);
+      } else {
+        for (int q = 0; q < N; ++q) {
+          const int64_t i = vi * N + q;
+          xv[q] = (i < V) ? SVec<E>::at(xr, i) : -INFINITY;
+        }
+      }
+    };
+    // The sixteenth-of-an-octave bucket of a logit's weight: floor(v s16), with the
+    // product taken exactly and rounded down, clamped to +-2^22 (monotone in v), from the
+    // bits of v s16 + 1.5 2^23 (one fused multiply-add rounding toward -inf; no
+    // conversion instruction). Its octave is the bucket >> 4.
+    auto six_i = [&](float v) -> int {
+      float t = __fmaf_rd(v, s16, 12582912.f);
+      t = fminf(fmaxf(t, 8388608.f), 16777216.f);
+      return __float_as_int(t) - 0x4B400000;
+    };
+
+    // running statistics of this thread's vectors
+    float bv = -INFINITY;   // maximum
+    int32_t bi = INT32_MAX;  // its first token id
+    float lm = -INFINITY, ls = 0.f, lc = 0.f;  // temperature-1 log-sum-exp (Kahan)
+    auto lse_vec = [&](const uint4& r, float vm) {
+      if (!(vm > -INFINITY)) return;
+      float xv[N];
+      SVec<E>::unpack(r, xv);
+      const float nm = fmaxf(lm, vm);
+      const float f = ex2((lm - nm) * kLog2e);
+      ls *= f;
+      lc *= f;
+      lm = nm;
+      float vs = 0.f;
+#pragma unroll
+      for (int q = 0; q < N; ++q) vs += ex2((xv[q] - nm) * kLog2e);
+      kahan_add(ls, lc, vs);
+    };
+
+    // Keeps the list's candidates at or above the k-th largest value (cnt <= kCCap) and
+    // returns that value's key; the list keeps its order of survivors in each half.
+    auto compact = [&](uint32_t cnt) -> uint32_t {
+      const uint32_t vk = sel::select_bound<kCC, CBar>(
+          (int)cnt, [&](int i) { return (uint32_t)(sm.w.list[i] >> kIdxBits); }, (uint32_t)k,
+          bf16 ? 2 : 4, sm.sc);
+      // in two halves, so that a thread holds at most ceil(2048 / 224) candidates:
+      // survivors of the first half go below 2048, the second half is read before it is
+      // overwritten
+      constexpr int KP = (kCHalf + kCC - 1) / kCC;
+      for (int half = 0; half < 2; ++half) {
+        uint64_t keep[KP];
+#pragma unroll
+        for (int m = 0; m < KP; ++m) {
+          const uint32_t i = (uint32_t)(half * kCHalf + m * kCC + tid);
+          keep[m] = (i < cnt && i < (uint32_t)((half + 1) * kCHalf)) ? sm.w.list[i] : 0ull;
+        }
+        cbar();
+        if (half == 0 && tid == 0) sm.lcnt = 0;
+        cbar();
+#pragma unroll
+        for (int m = 0; m < KP; ++m)
+          if ((uint32_t)(keep[m] >> kIdxBits) >= vk && keep[m] != 0ull)
+            sm.w.list[atomicAdd(&sm.lcnt, 1u)] = keep[m];
+        cbar();
+      }
+      return vk;
+    };
+    uint64_t z1 = 0;  // top-p pass 1: the row's mass in 2^-40 units of 2^(pbi + 1)
+
+    // One pass over the row's stages: the statistics every row keeps, and the kind's own
+    // summary. PASS is the top-p pass (1 for every other kind).
+    auto stream = [&](auto kind_tag, auto pass_tag) {
+      constexpr int KIND = decltype(kind_tag)::value;
+      constexpr int PASS = decltype(pass_tag)::value;
+      for (int c = 0; c < nst; ++c, ++g) {
+        const uint4* sv = stage_ptr(g);
+        const int c0 = c * SE;  // the stage's first element
+        const int nc = min(SE, (int)V - c0);
+        uint4 rv[kCVecs];
+        if (nc == SE) {
+#pragma unroll
+          for (int u = 0; u < kCVecs; ++u) rv[u] = sv[vbase + u * 32];
+        } else {
+#pragma unroll
+          for (int u = 0; u < kCVecs; ++u) rv[u] = stage_vec(sv, c0, nc, vbase + u * 32);
+        }
+        stage_release(g);
+        float vmv[kCVecs];
+#pragma unroll
+        for (int u = 0; u < kCVecs; ++u) vmv[u] = SVec<E>::vmax(rv[u]);
+        if (PASS == 1) {
+          // the thread's maximum and its first token id: the stage's four vector maxima
+          // against the running maximum, searched only when it rises
+          const float m4 = fmaxf(fmaxf(vmv[0], vmv[1]), fmaxf(vmv[2], vmv[3]));
+          if (m4 > bv) {
+            int qb = -1;
+#pragma unroll
+            for (int u = kCVecs - 1; u >= 0; --u) {
+              if (vmv[u] != m4) continue;
+              float xv[N];
+              SVec<E>::unpack(rv[u], xv);
+#pragma unroll
+              for (int q = N - 1; q >= 0; --q)
+                if (xv[q] == m4) qb = (vbase + u * 32) * N + q;
+            }
+            bv = m4;
+            bi = c0 + qb;
+          }
+          if (want_lse) {
+#pragma unroll
+            for (int u = 0; u < kCVecs; ++u) lse_vec(rv[u], vmv[u]);
+          }
+        }
+
+        if constexpr (KIND == kCTopK) {
+          if (c == 0) {
+            // a lower bound of the row's k-th value from the first stage.
+            if (k <= kCMerge) {
+              // the k-th largest vector maximum of the stage
+#pragma unroll
+              for (int u = 0; u < kCVecs; ++u)
+                sm.w.tk.keys[vbase + u * 32] = (vmv[u] > -INFINITY) ? fkey(vmv[u]) : 0u;
+              cbar();
+              const uint32_t t0 = sel::select_bound<kCC, CBar>(
+                  kCStageVecs, [&](int i) { return sm.w.tk.keys[i]; }, (uint32_t)k,
+                  bf16 ? 2 : 4, sm.sc);
+              if (tid == 0) sm.tau = t0;
+              cbar();
+            } else {
+              // the stage's own k-th largest value
+              uint32_t* skeys = reinterpret_cast<uint32_t*>(sm.w.list);
+#pragma unroll
+              for (int u = 0; u < kCVecs; ++u) {
+                float xv[N];
+                SVec<E>::unpack(rv[u], xv);
+#pragma unroll
+                for (int q = 0; q < N; ++q)
+                  skeys[(vbase + u * 32) * N + q] = (xv[q] > -INFINITY) ? fkey(xv[q]) : 0u;
+              }
+              cbar();
+              const uint32_t t0 = sel::select_bound<kCC, CBar>(
+                  nc, [&](int i) { return skeys[i]; }, (uint32_t)k, bf16 ? 2 : 4, sm.sc);
+              if (tid == 0) sm.tau = t0;
+              cbar();
+            }
+          }
+          // the elements at or above the threshold (a key at or below that of -inf keeps
+          // every finite element)
+          const uint32_t tau = sm.tau;
+          const float tf = (tau <= 0x007FFFFFu) ? -INFINITY : key_to_value(tau);
+          // a stage rarely holds a candidate once the bound is set: the warp tests its
+          // stage maximum first
+          const float m4 = fmaxf(fmaxf(vmv[0], vmv[1]), fmaxf(vmv[2], vmv[3]));
+          if (__any_sync(0xffffffffu, m4 > -INFINITY && m4 >= tf)) {
+            uint32_t mk[kCVecs];
+            uint32_t nsel = 0;
+  #pragma unroll
+            for (int u = 0; u < kCVecs; ++u) {
+              mk[u] = 0u;
+              if (vmv[u] > -INFINITY && vmv[u] >= tf) {
+                float xv[N];
+                SVec<E>::unpack(rv[u], xv);
+  #pragma unroll
+                for (int q = 0; q < N; ++q)
+                  if (xv[q] >= tf && xv[q] != -INFINITY) mk[u] |= 1u << q;
+                nsel += (uint32_t)__popc(mk[u]);
+              }
+            }
+            if (__any_sync(0xffffffffu, nsel != 0u)) {
+              uint32_t pos = warp_reserve(&sm.lcnt, nsel, lane);
+  #pragma unroll
+              for (int u = 0; u < kCVecs; ++u) {
+                if (!mk[u]) continue;
+                float xv[N];
+                SVec<E>::unpack(rv[u], xv);
+  #pragma unroll
+                for (int q = 0; q < N; ++q)
+                  if (mk[u] & (1u << q)) {
+                    if (pos < (uint32_t)kCCap)
+                      sm.w.list[pos] = comp_key(fkey(xv[q]),
+                                                (uint32_t)(c0 + (vbase + u * 32) * N + q));
+                    ++pos;
+                  }
+              }
+            }
+          }
+          // k > 128: the list is checked every few stages (and after the last) and compacted
+          // when it passes half its capacity. k <= 128 lists are only checked at the end.
+          if (k > kCMerge && ((c + 1) % 4 == 0 || c == nst - 1)) {
+            cbar();
+            const uint32_t cnt = sm.lcnt;
+            cbar();
+            if (cnt > (uint32_t)kCCap) {
+              if (tid == 0) {
+                sm.bad = 1;
+                sm.tau = 0xFFFFFFFFu;  // stop collecting; the general path takes the row
+                sm.lcnt = 0;
+              }
+              cbar();
+            } else if (cnt > (uint32_t)kCHalf) {
+              const uint32_t vk = compact(cnt);
+              if (tid == 0) sm.tau = max(sm.tau, vk);
+              cbar();
+              if (sm.lcnt > (uint32_t)kCHalf) {  // ties at the k-th value fill the list
+                cbar();
+                if (tid == 0) {
+                  sm.bad = 1;
+                  sm.tau = 0xFFFFFFFFu;
+                  sm.lcnt = 0;
+                }
+              }
+              cbar();
+            }
+          }
+        } else if constexpr (KIND == kCPlain) {
+          // warp w's 128 vectors of the stage: their mass relative to their own maximum,
+          // the draft token left out
+          float em = fmaxf(fmaxf(vmv[0], vmv[1]), fmaxf(vmv[2], vmv[3]));
+          em = warp_max(em);
+          float s = 0.f;
+          if (em > -INFINITY) {
+#pragma unroll
+            for (int u = 0; u < kCVecs; ++u) {
+              const int e0 = c0 + (vbase + u * 32) * N;
+              float xv[N];
+              SVec<E>::unpack(rv[u], xv);
+              float vs = 0.f;
+              if ((unsigned)(x - e0) < (unsigned)N) {
+#pragma unroll
+                for (int q = 0; q < N; ++q)
+                  vs += (e0 + q == x) ? 0.f : ex2((xv[q] - em) * sl2);
+              } else {
+#pragma unroll
+                for (int q = 0; q < N; ++q) vs += ex2((xv[q] - em) * sl2);
+              }
+              s += vs;
+            }
+          }
+          s = warp_sum_f32(s);
+          if (lane == 0)
+            rowslots[c * kCW + warp] =
+                ((uint64_t)__float_as_uint(em) << 32) | __float_as_uint(s);
+        } else if constexpr (KIND == kCTopP && PASS == 1) {
+          // pass 1: weights relative to 2^(pbi + 1), the window top (kPHead octaves above
+          // the first stage's maximum): the row's mass, and octave bins below the window
+          // top (bin d: octave pbi - d; the lowest bin also takes every deeper element),
+          // one column per compute thread (no shared atomics; -inf elements add 0)
+          if (c == 0) {
+            float m = fmaxf(fmaxf(vmv[0], vmv[1]), fmaxf(vmv[2], vmv[3]));
+            m = warp_max(m);
+            if (lane == 0) sm.redf[0][warp] = m;
+#pragma unroll
+            for (int b = 0; b < kPB; ++b) sm.w.hist[b * kCC + tid] = 0.f;
+            cbar();
+            if (tid == 0) {
+              float mm = sm.redf[0][0];
+              for (int w2 = 1; w2 < kCW; ++w2) mm = fmaxf(mm, sm.redf[0][w2]);
+              sm.pbi = (mm > -INFINITY) ? (six_i(mm) >> 4) + kPHead : 0;
+              if (!(mm > -INFINITY)) sm.bad = 1;
+            }
+            cbar();
+          }
+          const int pbi = sm.pbi;
+          const float ptop = (float)(pbi + 1);
+          int dmin = 0;  // negative if an element lies above the window
+          float zs = 0.f;
+#pragma unroll
+          for (int u = 0; u < kCVecs; ++u) {
+            float xv[N];
+            SVec<E>::unpack(rv[u], xv);
+#pragma unroll
+            for (int q = 0; q < N; ++q) {
+              const float v = xv[q];
+              const float wv = ex2(fmaf(v, sl2, -ptop));
+              zs += wv;
+              const int d = pbi - (six_i(v) >> 4);
+              dmin = min(dmin, d);
+              sm.w.hist[min(max(d, 0), kPB - 1) * kCC + tid] += wv;
+            }
+          }
+          if (dmin < 0) sm.bad = 1;
+          z1 += __float2ull_rz(zs * kFx);
+        } else if constexpr (KIND == kCTopP && PASS == 2) {
+          // pass 2 (the row maximum known): sixteenth bins over the window's two octaves,
+          // weights relative to the maximum
+          const float M = sm.M;
+          const int gt = sm.gtop;
+#pragma unroll
+          for (int u = 0; u < kCVecs; ++u) {
+            const bool meets = vmv[u] > -INFINITY && six_i(vmv[u]) >= gt - (kPB - 1) &&
+                               six_i(SVec<E>::vmin(rv[u])) <= gt;
+            if (!__any_sync(0xffffffffu, meets)) continue;  // the warp's vectors miss it
+            float xv[N];
+            SVec<E>::unpack(rv[u], xv);
+#pragma unroll
+            for (int q = 0; q < N; ++q) {
+              const float v = xv[q];
+              const unsigned f = (unsigned)(gt - six_i(v));
+              if (meets && f < (unsigned)kPB) sm.w.hist[f * kCC + tid] += ex2((v - M) * sl2);
+            }
+          }
+        } else if constexpr (KIND == kCTopP && PASS == 3) {
+          // pass 3: per warp range the kept mass above the collected sixteenths (the
+          // draft token left out), and the elements within them
+          const float M = sm.M;
+          const int gh = sm.gh, gl = sm.gl;
+          float s = 0.f;
+          uint32_t mk[kCVecs];
+          uint32_t nsel = 0;
+#pragma unroll
+          for (int u = 0; u < kCVecs; ++u) {
+            mk[u] = 0u;
+            const bool any = vmv[u] > -INFINITY && six_i(vmv[u]) >= gl;
+            if (!__any_sync(0xffffffffu, any)) continue;  // the warp's vectors are lighter
+            const int e0 = c0 + (vbase + u * 32) * N;
+            float xv[N];
+            SVec<E>::unpack(rv[u], xv);
+#pragma unroll
+            for (int q = 0; q < N; ++q) {
+              const float v = xv[q];
+              const int gx = six_i(v);  // -inf: the lowest bucket, below the window
+              const float wv = ex2((v - M) * sl2);
+              s += (any && gx > gh && e0 + q != x) ? wv : 0.f;
+              mk[u] |= (any && gx >= gl && gx <= gh) ? (1u << q) : 0u;
+            }
+            nsel += (uint32_t)__popc(mk[u]);
+          }
+          if (__any_sync(0xffffffffu, nsel != 0u)) {
+            uint32_t pos = warp_reserve(&sm.lcnt, nsel, lane);
+#pragma unroll
+            for (int u = 0; u < kCVecs; ++u) {
+              if (!mk[u]) continue;
+              float xv[N];
+              SVec<E>::unpack(rv[u], xv);
+#pragma unroll
+              for (int q = 0; q < N; ++q)
+                if (mk[u] & (1u << q)) {
+                  if (pos < (uint32_t)kCCap)
+                    sm.w.list[pos] = comp_key(fkey(xv[q]),
+                                              (uint32_t)(c0 + (vbase + u * 32) * N + q));
+                  ++pos;
+                }
+            }
+          }
+          const uint64_t f = warp_sum_u64(__float2ull_rz(s * kFx));
+          if (lane == 0) rowslots[c * kCW + warp] = f;
+        }
+      }
+    };
+
+    // ---- the streaming passes ---------------------------------------------------------------
+    switch (kn.kind) {
+      case kCTopK: stream(KindTag<kCTopK>{}, KindTag<1>{}); break;
+      case kCPlain: stream(KindTag<kCPlain>{}, KindTag<1>{}); break;
+      case kCTopP: stream(KindTag<kCTopP>{}, KindTag<1>{}); break;
+      default: stream(KindTag<kCGreedy>{}, KindTag<1>{}); break;
+    }
+
+    // ---- the row's statistics ---------------------------------------------------------------
+    ls += lc;
+    {
+      float v = bv, m = lm, s = ls;
+      int32_t i = bi;
+      warp_argmax(v, i);
+      if (want_lse) warp_lse(m, s);
+      if (lane == 0) {
+        sm.redf[0][warp] = v;
+        sm.redf[1][warp] = m;
+        sm.redf[2][warp] = s;
+        sm.redi[warp] = i;
+      }
+      cbar();
+      if (warp == 0) {
+        v = lane < kCW ? sm.redf[0][lane] : -INFINITY;
+        m = lane < kCW ? sm.redf[1][lane] : -INFINITY;
+        s = lane < kCW ? sm.redf[2][lane] : 0.f;
+        i = lane < kCW ? sm.redi[lane] : INT32_MAX;
+        warp_argmax(v, i);
+        if (want_lse) warp_lse(m, s);
+        if (lane == 0) {
+          sm.M = v;
+          sm.am = (i == INT32_MAX) ? 0 : i;
+          sm.S1 = s;
+          const uint64_t seed = a.seed ? (uint64_t)a.seed[req] : 0;
+          const uint64_t off = a.offset ? (uint64_t)a.offset[req] : 0;
+          const bool coins = kn.kind != kCGreedy;
+          sm.uj = (coins && j < D) ? (a.uniforms ? a.uniforms[req * a.R + j]
+                                                 : verify_coin(seed, off, (uint32_t)j))
+                                   : 0.f;
+          sm.uD = coins ? (a.uniforms ? a.uniforms[req * a.R + D]
+                                      : verify_coin(seed, off, (uint32_t)D))
+                        : 0.f;
+          sm.vx = xvalid ? SVec<E>::at(xr, x) : 0.f;
+        }
+      }
+      cbar();
+    }
+    const float M = sm.M;
+    const int32_t am = sm.am;
+    const float uj = sm.uj, uD = sm.uD, vx = sm.vx;
+    auto wfn = [&](float v) -> uint64_t { return fixw(ex2((v - M) * sl2)); };
+    auto wcomp = [&](uint64_t cc) -> uint64_t {
+      return wfn(key_to_value((uint32_t)(cc >> kIdxBits)));
+    };
+
+    // ---- top-p: locate the crossing (passes 2 and 3) ------------------------------------------
+    // Sums bin b over the compute threads' columns into sm.hb[b] (warp w, lane b takes the
+    // entries of threads 32w .. 32w + 31 in a skewed order, free of bank conflicts).
+    auto bin_totals = [&]() {
+      float acc = 0.f;
+#pragma unroll 8
+      for (int i = 0; i < 32; ++i) acc += sm.w.hist[lane * kCC + warp * 32 + ((i + lane) & 31)];
+      sm.hw[warp][lane] = acc;
+      cbar();
+      if (warp == 0) {
+        double t = 0.0;
+        for (int w2 = 0; w2 < kCW; ++w2) t += (double)sm.hw[w2][lane];
+        sm.hb[lane] = t;
+      }
+      cbar();
+    };
+    if (kn.kind == kCTopP) {
+      // pass 1's octave bins (weights relative to 2^(pbi + 1)) and the row's mass
+      {
+        const uint64_t z = warp_sum_u64(z1);
+        if (lane == 0) sm.red2[0][warp] = z;
+      }
+      bin_totals();
+      if (warp == 0) {
+        uint64_t zt = 0;
+        for (int w2 = 0; w2 < kCW; ++w2) zt += sm.red2[0][w2];
+        const double zrel = (double)zt * kCInvFx;  // the row's mass, units of 2^(pbi + 1)
+        const double mb = sm.hb[lane];
+        double incl = mb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const double y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const double P1 = (double)kn.tp * zrel;
+        const double before = incl - mb;
+        const unsigned hm = __ballot_sync(0xffffffffu, mb > 0.0 && before < P1 && P1 <= incl);
+        const int bs = hm ? __ffs(hm) - 1 : -1;
+        const double bbefore = __shfl_sync(0xffffffffu, before, bs >= 0 ? bs : 0);
+        const double bmass = __shfl_sync(0xffffffffu, mb, bs >= 0 ? bs : 0);
+        // the fine window: the crossing octave and its neighbour on the nearer side
+        const bool okb = bs >= 0 && bs < kPB - 2;  // else the crossing is in or below the lowest bins
+        const int bt = (okb && (P1 - bbefore) / bmass < 0.5 && bs > 0) ? bs - 1 : (okb ? bs : 0);
+        const double above = __shfl_sync(0xffffffffu, before, bt);  // the bins above bt
+        if (lane == 0) {
+          // 2^40 times the weight of 2^(pbi + 1) relative to the row maximum's
+          const double K =
+              exp2((double)(sm.pbi + 1) - (double)M * (double)sl2) * 1099511627776.0;
+          const double zm = zrel * K;
+          const double want = ceil((double)kn.tp * zm);
+          sm.ptarget = (want >= zm) ? (uint64_t)zm : (uint64_t)want;
+          if (!okb) sm.bad = 1;
+          sm.gtop = 16 * (sm.pbi - bt) + 15;
+          sm.res_d = above * K;  // the mass above the window, 2^-40 units of the maximum
+        }
+      }
+      cbar();
+      const bool bad1 = sm.bad != 0;
+      // pass 2 (its stages are consumed in any case)
+      if (!bad1) {
+#pragma unroll
+        for (int b = 0; b < kPB; ++b) sm.w.hist[b * kCC + tid] = 0.f;
+      }
+      cbar();
+      if (!bad1) {
+        stream(KindTag<kCTopP>{}, KindTag<2>{});
+      } else {
+        for (int c = 0; c < nst; ++c, ++g) {
+          (void)stage_ptr(g);
+          stage_release(g);
+        }
+      }
+      cbar();
+      bin_totals();
+      if (warp == 0 && !bad1) {
+        // sixteenth f (0: the window's highest) in 2^-40 units of the maximum's weight,
+        // after the mass above the window
+        const double mf = sm.hb[lane] * 1099511627776.0;
+        double incl = mf;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const double y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const double P = (double)sm.ptarget;
+        const double before = sm.res_d + incl - mf;
+        const unsigned hm = __ballot_sync(0xffffffffu, mf > 0.0 && before < P && P <= before + mf);
+        const int fs = hm ? __ffs(hm) - 1 : -1;
+        const double fbefore = __shfl_sync(0xffffffffu, before, fs >= 0 ? fs : 0);
+        const double fmass = __shfl_sync(0xffffffffu, mf, fs >= 0 ? fs : 0);
+        if (lane == 0) {
+          if (fs < 0) {
+            sm.bad = 1;
+          } else {
+            // the crossing sixteenth and its neighbour on the nearer side
+            const double frac = (P - fbefore) / fmass;
+            int f0 = fs, f1 = fs;
+            if (frac < 0.5) f0 = (fs > 0) ? fs - 1 : fs;
+            else f1 = (fs < kPB - 1) ? fs + 1 : fs;
+            sm.gh = sm.gtop - f0;
+            sm.gl = sm.gtop - f1;
+          }
+        }
+      }
+      cbar();
+      const bool bad2 = sm.bad != 0;
+      if (tid == 0) sm.lcnt = 0;
+      cbar();
+      if (!bad2) {
+        stream(KindTag<kCTopP>{}, KindTag<3>{});
+      } else {
+        for (int c = 0; c < nst; ++c, ++g) {
+          (void)stage_ptr(g);
+          stage_release(g);
+        }
+      }
+      cbar();
+    }
+
+    // a wait that gave up: leave the row (and the rest) unwritten
+    {
+      const bool ab2 = ld_abort(&sm.abort_flag);
+      cbar();
+      if (ab2) break;
+    }
+    // a top-k list that overflowed goes to the general path; one longer than a warp
+    // takes is compacted to the row's top k first
+    if (kn.kind == kCTopK && sm.bad == 0) {
+      const uint32_t cnt = sm.lcnt;
+      if (tid == 0) {
+        atomicAdd(&a.ws.work[0], cnt);
+        if (cnt > (uint32_t)(32 * kCSmallE)) atomicAdd(&a.ws.work[1], 1u);
+      }
+      if (cnt > (uint32_t)kCCap) {
+        cbar();
+        if (tid == 0) sm.bad = 1;
+      } else if (cnt > (uint32_t)(32 * kCSmallE) && k <= kCMerge) {
+        (void)compact(cnt);
+      }
+      cbar();
+    }
+    const bool bad = sm.bad != 0;
+
+    // records the row; the last row of its request to be recorded writes the chain
+    auto finish_row = [&](int32_t tok_f, int32_t acc_f) {
+      a.ws.rowres[row] = RowRes{M, am, sm.S1, tok_f, acc_f, {0, 0, 0}};
+      __threadfence();
+      const uint32_t prev = atomicAdd(&a.ws.creq[req], 1u);
+      if (prev != (uint32_t)a.R - 1) return;
+      __threadfence();
+      int32_t js = D;
+      for (int32_t jj = 0; jj < D; ++jj)
+        if (!__ldcg(&a.ws.rowres[req * a.R + jj].acc)) {
+          js = jj;
+          break;
+        }
+      for (int32_t jj = 0; jj < a.R; ++jj) {
+        const int64_t rj = req * a.R + jj;
+        int32_t t = -1;
+        if (jj < js) t = a.draft_tokens[req * D + jj];
+        else if (jj == js) t = __ldcg(&a.ws.rowres[rj].tok);
+        a.accepted_tokens[rj] = t;
+        if (a.accept_index) a.accept_index[rj] = (jj <= js) ? (int32_t)rj : -1;
+        if (a.logprobs) {
+          float lp = 0.f;
+          if (jj <= js && t >= 0 && (int64_t)t < V) {
+            const E* xj = reinterpret_cast<const E*>(a.x) + rj * a.ld;
+            lp = (SVec<E>::at(xj, t) - __ldcg(&a.ws.rowres[rj].M)) -
+                 logf(__ldcg(&a.ws.rowres[rj].S));
+          }
+          a.logprobs[rj] = lp;
+        }
+      }
+      a.accept_length[req] = js + 1;
+    };
+    // Warp 0 walks the 32 vectors from row vector v0 (one a lane) and returns the first
+    // element at which the running weight exceeds tf (the last element with weight if
+    // none does, e.g. by rounding; -1 if no element has weight).
+    auto walk_step = [&](int64_t v0, float tf, auto&& wgt) -> int32_t {
+      const int64_t vi = v0 + lane;
+      float xv[N];
+      float vs = 0.f;
+      if (vi < nvall) {
+        load_vec(vi, xv);
+#pragma unroll
+        for (int q = 0; q < N; ++q) vs += wgt(xv[q], vi * N + q);
+      }
+      float inc = vs;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      const unsigned cross = __ballot_sync(0xffffffffu, vs > 0.f && inc > tf);
+      const unsigned nz = __ballot_sync(0xffffffffu, vs > 0.f);
+      const int wl = cross ? __ffs(cross) - 1 : (nz ? 31 - __clz(nz) : -1);
+      int32_t f = -1;
+      if (lane == wl) {
+        float accf = inc - vs;
+        for (int q = 0; q < N; ++q) {
+          const float w = wgt(xv[q], vi * N + q);
+          if (w == 0.f) continue;
+          f = (int32_t)(vi * N + q);
+          accf += w;
+          if (cross && accf > tf) break;
+        }
+      }
+      return (wl >= 0) ? __shfl_sync(0xffffffffu, f, wl) : -1;
+    };
+    // The same over the kCVecs * 32 vectors from v0, a step of 32 at a time.
+    auto walk_range = [&](int64_t v0, float tf, auto&& wgt) -> int32_t {
+      int lastu = -1;
+      for (int u = 0; u < kCVecs; ++u) {
+        const int64_t vi = v0 + u * 32 + lane;
+        float vs = 0.f;
+        if (vi < nvall) {
+          float xv[N];
+          load_vec(vi, xv);
+#pragma unroll
+          for (int q = 0; q < N; ++q) vs += wgt(xv[q], vi * N + q);
+        }
+        const float tot = warp_sum_f32(vs);
+        if (tot > tf) return walk_step(v0 + u * 32, tf, wgt);
+        if (tot > 0.f) {
+          tf -= tot;
+          lastu = u;
+        }
+      }
+      // rounding: the last element with weight
+      return (lastu >= 0) ? walk_step(v0 + lastu * 32, INFINITY, wgt) : -1;
+    };
+    // The draw over per-range masses (stage c, warp w at c * kCW + w; the draft token left
+    // out) with coin uD, then a walk of the chosen range with weights wgt: warp 0 records
+    // the row. Zr is the ranges' total.
+    const int64_t e1max = (int64_t)nst * kCW;  // the row's ranges
+    auto draw_ranges = [&](uint64_t mine, uint64_t ex, uint64_t Zr, int64_t e0, int64_t e1,
+                           int32_t acc, auto&& wgt) {
+      uint64_t t = (uint64_t)((double)uD * (double)Zr);
+      if (t >= Zr) t = Zr - 1;
+      if (mine > 0 && ex <= t && t < ex + mine) {
+        uint64_t accu = ex;
+        int64_t esel = e1 - 1;
+        for (int64_t e = e0; e < e1; ++e) {
+          const uint64_t m = __ldcg(rowslots + e);
+          if (t < accu + m) {
+            esel = e;
+            break;
+          }
+          accu += m;
+        }
+        sm.res_u = (uint64_t)esel;
+        sm.res_d = (double)(t - accu) * kCInvFx;
+      }
+      cbar();
+      if (warp == 0) {
+        const int64_t es = min((int64_t)(sm.res_u % (uint64_t)e1max), e1max - 1);
+        const int64_t v0 = (es / kCW) * (SE / N) + (es % kCW) * (kCVecs * 32);
+        const int32_t tok = walk_range(v0, (float)sm.res_d, wgt);
+        if (lane == 0) finish_row(tok >= 0 ? tok : am, acc);
+      }
+    };
+
+    // The general path for the rows the streamed summaries cannot serve (top_k above
+    // kSTopK, candidate overflow, a top-p crossing outside its windows): radix selections
+    // over the whole row, read again from memory for every digit, in the order top-k,
+    // top-p within it, then the draw in token-id order.
+    auto general = [&]() {
+      if (tid == 0) atomicAdd(&a.ws.work[2], 1u);
+      const int n = (int)V;
+      auto gitem = [&](int i) -> uint64_t {
+        return comp_key(fkey(SVec<E>::at(xr, i)), (uint32_t)i);
+      };
+      auto gmass = [&](uint64_t c0) -> uint64_t {
+        uint64_t sum = 0;
+        for (int i = tid; i < n; i += kCC) {
+          const uint64_t cc = gitem(i);
+          if (cc >= c0) sum += wcomp(cc);
+        }
+        uint64_t tot;
+        (void)sel::excl_scan<kCC, CBar>(sum, sm.sc, tot);
+        return tot;
+      };
+      const bool tk = k > 0 && (int64_t)k < V;
+      uint64_t C = 1;  // every composite key is at least 1
+      if (tk)
+        C = sel::radix_adaptive<kCC, false, CBar>(
+            n, gitem, 1ull, (uint64_t)k, [](uint64_t) { return (uint64_t)1; }, lowv, sm.sc);
+      uint64_t Z = gmass(C);
+      if (kn.tp < 1.f) {
+        const double want = ceil((double)kn.tp * (double)Z);
+        const uint64_t P = (want > (double)Z) ? Z : (uint64_t)want;
+        C = sel::radix_adaptive<kCC, true, CBar>(n, gitem, C, P, wcomp, lowv, sm.sc);
+        Z = gmass(C);
+      }
+      uint64_t wx = 0;
+      if (xvalid && comp_key(fkey(vx), (uint32_t)x) >= C) wx = wfn(vx);
+      const int32_t acc = (j < D) && ((double)uj * (double)Z < (double)wx) ? 1 : 0;
+      const uint64_t Zr = Z - wx;
+      int32_t tok;
+      if (Zr == 0) {
+        tok = (wx > 0) ? x : am;
+      } else {
+        uint64_t t = (uint64_t)((double)uD * (double)Zr);
+        if (t >= Zr) t = Zr - 1;
+        const int idx_sh[3] = {16, 8, 0};
+        uint64_t gsel = 0;
+        (void)sel::radix<kCC, true, CBar>(
+            n, gitem, C, t + 1,
+            [&](uint64_t cc) { return ((int32_t)comp_token(cc) == x) ? 0ull : wcomp(cc); },
+            idx_sh, 3, sm.sc, &gsel);
+        tok = (int32_t)comp_token(gsel);
+      }
+      if (tid == 0) finish_row(tok, acc);
+    };
+
+    // ---- finish the row ---------------------------------------------------------------------
+    if (kn.kind == kCGreedy) {
+      if (tid == 0) finish_row(am, (j < D && x == am) ? 1 : 0);
+    } else if (bad || kn.kind == kCGeneral) {
+      general();
+    } else if (kn.kind == kCTopP) {
+      // the crossing elements resolved exactly; the kept ones join their ranges
+      const uint32_t cnt = sm.lcnt;
+      const int ghi = sm.gh, gli = sm.gl;
+      const int64_t E_ = (int64_t)nst * kCW;
+      const int64_t per = (E_ + kCC - 1) / kCC;
+      const int64_t e0 = min(E_, (int64_t)tid * per), e1 = min(E_, e0 + per);
+      uint64_t mine = 0;
+      for (int64_t e = e0; e < e1; ++e) mine += __ldcg(rowslots + e);
+      uint64_t Zab;
+      (void)sel::excl_scan<kCC, CBar>(mine, sm.sc, Zab);
+      // the draft token's weight if it lies above the collected sixteenths
+      const bool xabove = xvalid && six_i(vx) > ghi;
+      const uint64_t A = Zab + (xabove ? wfn(vx) : 0ull);
+      const uint64_t P = sm.ptarget;
+      uint64_t lmass = 0;
+      for (uint32_t i = tid; i < min(cnt, (uint32_t)kCCap); i += kCC) lmass += wcomp(sm.w.list[i]);
+      uint64_t Lt;
+      (void)sel::excl_scan<kCC, CBar>(lmass, sm.sc, Lt);
+      if (cnt > (uint32_t)kCCap || cnt == 0 || P <= A || P > A + Lt) {
+        general();
+      } else {
+        const uint64_t C = sel::radix_adaptive<kCC, true, CBar>(
+            (int)cnt, [&](int i) { return sm.w.list[i]; }, 1ull, P - A, wcomp, lowv, sm.sc);
+        for (uint32_t i = tid; i < cnt; i += kCC) {
+          const uint64_t cc = sm.w.list[i];
+          const uint32_t gidx = comp_token(cc);
+          if (cc >= C && (int32_t)gidx != x)
+            atomicAdd(reinterpret_cast<unsigned long long*>(
+                          rowslots + (gidx / N) / (kCVecs * 32)),
+                      (unsigned long long)wcomp(cc));
+        }
+        cbar();
+        auto kept = [&](float v, int64_t gidx) -> bool {
+          const int gx = six_i(v);
+          if (gx > ghi) return true;
+          return gx >= gli && comp_key(fkey(v), (uint32_t)gidx) >= C;
+        };
+        uint64_t wx = 0;
+        if (xvalid && kept(vx, x)) wx = wfn(vx);
+        mine = 0;
+        for (int64_t e = e0; e < e1; ++e) mine += __ldcg(rowslots + e);
+        uint64_t Zr;
+        const uint64_t ex = sel::excl_scan<kCC, CBar>(mine, sm.sc, Zr);
+        const int32_t acc = (j < D) && ((double)uj * (double)(Zr + wx) < (double)wx) ? 1 : 0;
+        if (Zr == 0) {
+          if (tid == 0) finish_row((wx > 0) ? x : am, acc);
+        } else {
+          draw_ranges(mine, ex, Zr, e0, e1, acc, [&](float v, int64_t gidx) -> float {
+            if (gidx == (int64_t)x || v == -INFINITY || !kept(v, gidx)) return 0.f;
+            return ex2((v - M) * sl2);
+          });
+        }
+      }
+    } else if (kn.kind == kCTopK && (int)sm.lcnt <= 32 * kCSmallE) {
+      // few candidates: one warp finishes the row. Orders come from counting (compact
+      // loops, so that this code, run once a row, stays small).
+      if (warp == 0) {
+        const int nl = (int)sm.lcnt;
+        uint64_t* srt = sm.w.list + kCHalf;        // the candidates by rank (value order)
+        uint64_t* wid = sm.w.list + kCHalf + 128;  // kept: weight by rank in id order
+        uint32_t* kid = reinterpret_cast<uint32_t*>(sm.w.list + kCHalf + 256);  // kept ids
+        for (int i = lane; i < nl; i += 32) {
+          const uint64_t ci = sm.w.list[i];
+          int r = 0;
+          for (int jj = 0; jj < nl; ++jj) r += (sm.w.list[jj] > ci) ? 1 : 0;
+          srt[r] = ci;  // composites are distinct: ranks are a permutation
+        }
+        __syncwarp();
+        uint64_t v[kCSmallE], w[kCSmallE], incl[kCSmallE];
+#pragma unroll
+        for (int e = 0; e < kCSmallE; ++e) {
+          const int i = e * 32 + lane;  // rank
+          v[e] = (i < nl) ? srt[i] : 0ull;
+          w[e] = (i < nl && i < k) ? wcomp(v[e]) : 0ull;
+          incl[e] = w[e];
+        }
+        const uint64_t Zk = warp_scan_incl(incl);
+        // top-p within the top k: rank r kept iff r = 0 or the mass before it is below P
+        uint64_t P = Zk;
+        if (kn.tp < 1.f) {
+          const double want = ceil((double)kn.tp * (double)Zk);
+          P = (want > (double)Zk) ? Zk : (want > 0.0 ? (uint64_t)want : 0ull);
+        }
+        uint64_t Z = 0, wx = 0;
+        bool kept[kCSmallE];
+#pragma unroll
+        for (int e = 0; e < kCSmallE; ++e) {
+          const int i = e * 32 + lane;
+          kept[e] = i < nl && i < k && (i == 0 || incl[e] - w[e] < P);
+          const uint32_t tk = comp_token(v[e]);
+          if (kept[e]) {
+            Z += w[e];
+            if ((int32_t)tk == x) wx = w[e];
+          }
+          if (i < 128) kid[i] = kept[e] ? tk : 0xFFFFFFFFu;
+        }
+        Z = warp_sum_u64(Z);
+        wx = warp_sum_u64(wx);
+        const int32_t acc = (j < D) && ((double)uj * (double)Z < (double)wx) ? 1 : 0;
+        const uint64_t Zr = Z - wx;
+        int32_t tok = (wx > 0) ? x : (int32_t)comp_token(srt[0]);  // srt[0]: the argmax
+        if (Zr > 0) {
+          uint64_t t = (uint64_t)((double)uD * (double)Zr);
+          if (t >= Zr) t = Zr - 1;
+          __syncwarp();
+          // the kept tokens in id order (their rank among the kept ids), the draft token
+          // without weight
+#pragma unroll
+          for (int e = 0; e < kCSmallE; ++e) {
+            const int i = e * 32 + lane;
+            if (!kept[e]) continue;
+            const uint32_t tk = kid[i];
+            int r = 0;
+            for (int jj = 0; jj < nl && jj < 128; ++jj) r += (kid[jj] < tk) ? 1 : 0;
+            wid[r] = ((int32_t)tk == x) ? 0ull : w[e];
+            kid[128 + r] = tk;
+          }
+          __syncwarp();
+          const int nk = __popc(__ballot_sync(0xffffffffu, kept[0])) +
+                         __popc(__ballot_sync(0xffffffffu, kept[1])) +
+                         __popc(__ballot_sync(0xffffffffu, kept[2])) +
+                         __popc(__ballot_sync(0xffffffffu, kept[3]));
+          uint64_t cw[kCSmallE], ww[kCSmallE];
+#pragma unroll
+          for (int e = 0; e < kCSmallE; ++e) {
+            const int i = e * 32 + lane;
+            ww[e] = (i < nk) ? wid[i] : 0ull;
+            cw[e] = ww[e];
+          }
+          (void)warp_scan_incl(cw);
+          // the first token whose inclusive prefix mass exceeds t
+          int32_t f = INT32_MAX;
+#pragma unroll
+          for (int e = 0; e < kCSmallE; ++e) {
+            const int i = e * 32 + lane;
+            if (i < nk && ww[e] > 0 && cw[e] > t && cw[e] - ww[e] <= t) f = (int32_t)kid[128 + i];
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) f = min(f, __shfl_xor_sync(0xffffffffu, f, o));
+          if (f != INT32_MAX) tok = f;
+        }
+        if (lane == 0) finish_row(tok, acc);
+      }
+    } else if (kn.kind == kCTopK) {
+      const int nl = (int)sm.lcnt;
+      auto item = [&](int i) { return sm.w.list[i]; };
+      const uint64_t Ck = sel::radix_adaptive<kCC, false, CBar>(
+          nl, item, 1ull, (uint64_t)k, [](uint64_t) { return (uint64_t)1; }, lowv, sm.sc);
+      auto mass_from = [&](uint64_t c0) -> uint64_t {
+        uint64_t sum = 0;
+        for (int i = tid; i < nl; i += kCC) {
+          const uint64_t cc = sm.w.list[i];
+          if (cc >= c0) sum += wcomp(cc);
+        }
+        uint64_t tot;
+        (void)sel::excl_scan<kCC, CBar>(sum, sm.sc, tot);
+        return tot;
+      };
+      uint64_t C = Ck, Z = mass_from(Ck);
+      if (kn.tp < 1.f) {
+        const double want = ceil((double)kn.tp * (double)Z);
+        const uint64_t P = (want > (double)Z) ? Z : (want > 0.0 ? (uint64_t)want : 0ull);
+        C = sel::radix_adaptive<kCC, true, CBar>(nl, item, Ck, P, wcomp, lowv, sm.sc);
+        Z = mass_from(C);
+      }
+      uint64_t wx = 0;
+      if (xvalid && comp_key(fkey(vx), (uint32_t)x) >= C) wx = wfn(vx);
+      const int32_t acc = (j < D) && ((double)uj * (double)Z < (double)wx) ? 1 : 0;
+      const uint64_t Zr = Z - wx;
+      int32_t tok;
+      if (Zr == 0) {
+        tok = (wx > 0) ? x : am;
+      } else {
+        uint64_t t = (uint64_t)((double)uD * (double)Zr);
+        if (t >= Zr) t = Zr - 1;
+        const int idx_sh[3] = {16, 8, 0};
+        uint64_t gsel = 0;
+        (void)sel::radix<kCC, true, CBar>(
+            nl, item, C, t + 1,
+            [&](uint64_t cc) { return ((int32_t)comp_token(cc) == x) ? 0ull : wcomp(cc); },
+            idx_sh, 3, sm.sc, &gsel);
+        tok = (int32_t)comp_token(gsel);
+      }
+      if (tid == 0) finish_row(tok, acc);
+    } else {  // kCPlain: the warp ranges scaled to the row maximum, in token order
+      const int64_t E_ = (int64_t)nst * kCW;
+      const int64_t per = (E_ + kCC - 1) / kCC;
+      const int64_t e0 = min(E_, (int64_t)tid * per), e1 = min(E_, e0 + per);
+      auto entry = [&](int64_t e, float* emax) -> double {
+        const uint64_t p = __ldcg(rowslots + e);
+        const float em = __uint_as_float((uint32_t)(p >> 32));
+        *emax = em;
+        if (!(em > -INFINITY)) return 0.0;
+        return (double)__uint_as_float((uint32_t)p) * (double)ex2((em - M) * sl2);
+      };
+      double mine = 0.0;
+      float emd;
+      for (int64_t e = e0; e < e1; ++e) mine += entry(e, &emd);
+      double Zr;
+      const double ex = excl_scan_f64_t<kCW, CBar>(mine, sm.dscan, Zr);
+      const double wx = xvalid ? (double)ex2((vx - M) * sl2) : 0.0;
+      const int32_t acc = (j < D) && ((double)uj * (Zr + wx) < wx) ? 1 : 0;
+      if (!(Zr > 0.0)) {
+        if (tid == 0) finish_row((wx > 0.0) ? x : am, acc);
+      } else {
+        const double t = (double)uD * Zr;
+        if (tid == 0) sm.owner = -1;
+        cbar();
+        if (mine > 0.0 && ex <= t && t < ex + mine) sm.owner = tid;
+        cbar();
+        if (sm.owner < 0) {  // rounding: the last thread with mass
+          if (mine > 0.0) atomicMax(&sm.owner, tid);
+          cbar();
+        }
+        if (tid == sm.owner) {
+          double accd = ex, rs = 0.0, rlast = 0.0;
+          int64_t es = -1, elast = -1;
+          for (int64_t e = e0; e < e1; ++e) {
+            float em;
+            const double m = entry(e, &em);
+            if (m <= 0.0) continue;
+            elast = e;
+            rlast = accd;
+            if (t < accd + m) {
+              es = e;
+              rs = accd;
+              break;
+            }
+            accd += m;
+          }
+          if (es < 0) {
+            es = elast;
+            rs = rlast;
+          }
+          float em;
+          const double m = entry(es, &em);
+          sm.res_u = (uint64_t)es;
+          sm.redf[0][0] = em;
+          // the residual in the range's own weight units (relative to its maximum)
+          sm.res_d = (t - rs) / (m > 0.0 ? (double)ex2((em - M) * sl2) : 1.0);
+        }
+        cbar();
+        if (warp == 0) {
+          const int64_t es = min((int64_t)(sm.res_u % (uint64_t)e1max), e1max - 1);
+          const float em = sm.redf[0][0];
+          const int64_t v0 = (es / kCW) * (SE / N) + (es % kCW) * (kCVecs * 32);
+          const int32_t tok = walk_range(v0, (float)sm.res_d, [&](float v, int64_t gidx) -> float {
+            return (gidx == (int64_t)x || v == -INFINITY) ? 0.f : ex2((v - em) * sl2);
+          });
+          if (lane == 0) finish_row(tok >= 0 ? tok : am, acc);
+        }
+      }
+    }
+    cbar();  // the row's shared state is free for the next row
+  }
+
+}
+
+template <typename E>
+cudaError_t launch_chain_t(const SampleArgs& a, cudaStream_t s) {
+  int dev = 0, nsm = 148;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  k_chain_plan<<<1, 1024, 0, s>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t want = (int64_t)nsm * 2;  // two CTAs an SM
+  const unsigned grid = (unsigned)(a.rows < want ? a.rows : want);
+  const size_t dyn = (size_t)kCNSt * kCStageBytes + sizeof(CSmem);
+  e = cudaFuncSetAttribute(k_chain<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  if (e != cudaSuccess) return e;
+  k_chain<E><<<grid, kCThreads, dyn, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_chain(const SampleArgs& a, cudaStream_t s) {
+  if (a.rows <= 0) return cudaSuccess;
+  return a.bf16 ? launch_chain_t<uint16_t>(a, s) : launch_chain_t<float>(a, s);
+}
+
+cudaError_t chain_read_error(uint32_t* word, int clear) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_chain_err, sizeof(v));
+  if (e != cudaSuccess) return e;
+  *word = v;
+  if (clear && v) {
+    const unsigned int z = 0;
+    e = cudaMemcpyToSymbol(g_chain_err, &z, sizeof(z));
+  }
+  return e;
+}
+
+}  // namespace tsv

@@ -58,7 +58,10 @@ struct Workspace {
   uint64_t* cmass;    // [rows * 8] per-CTA masses of a cluster-staged row
   uint32_t* best;     // [rows] Gumbel-max: the row's best score so far (order key, 0: none)
   uint32_t* work;     // [4] the row kernel's 64-bit next-row counter ([0..1], 8-byte
-                      // aligned) and finished-CTA count ([2])
+                      // aligned) and finished-CTA count ([2]); the chain kernel's count
+                      // of rows served by its general path ([2]) and row claims ([3])
+  uint32_t* order;    // [rows] the chain kernel's rows in claim order (cost tiers)
+  uint32_t* creq;     // [batch] the chain kernel's per-request finished-row counts
   uint64_t* cand;     // [rows * cand_splits * kSTopK] per-row range masses of the row
                       // kernel (vocab > 0 only)
   int64_t cand_splits;
@@ -157,12 +160,21 @@ struct SampleArgs {
   float* logprobs;
   Workspace ws;
   float* out;  // top-k/top-p renorm of probability rows: [rows, V] fp32 (no workspace)
+  uint64_t wait_cycles;  // chain kernel: SM clock cycles a stage wait may take
 };
 
 cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s);
 // The row kernel in its renorm mode (fp32 probability rows, 16-byte aligned).
 cudaError_t launch_renorm_rows(const SampleArgs& a, cudaStream_t s);
 cudaError_t row_read_error(uint32_t* word, int clear);
+
+// ---- chain kernel (ts_chain.cu) -----------------------------------------------------
+
+// Target-only chain sampling from logits (16-byte aligned rows, vocab <= kRowMaxVocab):
+// a planning launch orders the rows by cost tier and clears the per-launch state, then a
+// persistent row-streaming launch serves every row.
+cudaError_t launch_chain(const SampleArgs& a, cudaStream_t s);
+cudaError_t chain_read_error(uint32_t* word, int clear);
 constexpr int64_t kRowMaxVocab = (int64_t)1 << 18;  // the row kernel's exact digit sums
 
 // ---- cluster-staged row kernels (ts_staged.cu) -----------------------------------

@@ -71,6 +71,8 @@ def load():
     L.ts_last_error_message.restype = ctypes.c_char_p
     L.ts_device_error.argtypes = [P, ctypes.c_int]
     L.ts_device_error.restype = st
+    L.ts_set_wait_cycles.argtypes = [ctypes.c_uint64]
+    L.ts_set_wait_cycles.restype = st
     L.ts_softmax_temp.argtypes = [P, ctypes.c_int, i64, i64, i64, P, P, P]
     L.ts_softmax_temp.restype = st
     L.ts_topk_topp_renorm.argtypes = [P, i64, i64, i64, P, P, P, P]
@@ -139,6 +141,11 @@ def device_error(clear: bool = True) -> int:
     if st not in (0, 4):
         _check("ts_device_error", st)
     return int(w.value)
+
+
+def set_wait_cycles(cycles: int) -> None:
+    """Sets the chain kernel's stage-wait budget in SM clock cycles (0: the default)."""
+    _check("ts_set_wait_cycles", load().ts_set_wait_cycles(int(cycles)))
 
 
 def softmax_temp(logits, temperature=None, out=None, stream=None):
