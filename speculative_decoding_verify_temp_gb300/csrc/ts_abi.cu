@@ -3,7 +3,6 @@
 // the kernels of ts_stream.cu, ts_sample.cu and ts_staged.cu.
 #include <stdarg.h>
 #include <stdio.h>
-#include <stdlib.h>
 
 #include <atomic>
 #include <mutex>
@@ -357,9 +356,7 @@ ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t
     sa.logprobs = p->logprobs;
     sa.ws = a.ws;
     sa.wait_cycles = g_wait_cycles.load(std::memory_order_relaxed);
-    if (getenv("TS_CHAIN_KERNEL") && atoi(getenv("TS_CHAIN_KERNEL")) == 2)
-      return launched(tsv::launch_chain(sa, stream), "row-streaming chain launch");
-    return launched(tsv::launch_sample(sa, stream), "row-streaming sampling launch");
+    return launched(tsv::launch_chain(sa, stream), "row-streaming chain launch");
   } else if (p->temperature) {
     // Greedy requests need only the argmax of each row: a streaming pass handles them,
     // and the staged kernel skips them.

@@ -209,6 +209,23 @@ __device__ __noinline__ uint4 ragged_vec(const E* xr, int e0, int n) {
   return make_uint4(wv[0], wv[1], wv[2], wv[3]);
 }
 
+// The largest key C, down to bit lowbit, such that at least k of the warp's keys (E a
+// lane) are >= C: the k-th largest key with its bits below lowbit cleared, or 0 if the
+// warp holds fewer than k keys. Bisection on the bits, one ballot per key and bit.
+template <int E>
+__device__ __forceinline__ uint32_t warp_kth_key(const uint32_t (&key)[E], int k, int lowbit) {
+  uint32_t res = 0u;
+#pragma unroll 1
+  for (int bit = 31; bit >= lowbit; --bit) {
+    const uint32_t cand = res | (1u << bit);
+    int cnt = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) cnt += __popc(__ballot_sync(0xffffffffu, key[e] >= cand));
+    if (cnt >= k) res = cand;
+  }
+  return res;
+}
+
 // two CTAs an SM: their rings and state fit the SM's 228 KB of shared memory (1 KB of it
 // reserved per CTA)
 static_assert(2 * (kCNSt * kCStageBytes + sizeof(CSmem) + 1024) <= 233472, "two CTAs an SM");
@@ -313,11 +330,12 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
         return (pos < (uint64_t)a.rows) ? __ldcg(&a.ws.order[pos]) : kNoRow;
       };
       uint32_t gi = 0;  // stages issued
-      // rows are claimed one row ahead, so that the claim's latency is never waited for
-      uint32_t inext = order_at(atomicAdd(&a.ws.work[3], 1u));
-      uint32_t ipos = atomicAdd(&a.ws.work[3], 1u);
+      // A row is claimed when the previous one has a ring's depth of stages left to issue,
+      // so that the claim's latency is hidden while a CTA holds at most the row it is
+      // streaming and the next one's first stages (the last rows of a step stay spread).
+      uint32_t pend = atomicAdd(&a.ws.work[3], 1u);  // the claim of the next row
       for (;;) {
-        const uint32_t e = inext;
+        const uint32_t e = order_at(pend);
         if (e == kNoRow) {  // one last stage tells the consumers to stop
           const int slot = (int)(gi % kCNSt);
           const uint32_t use = gi / kCNSt;
@@ -331,31 +349,31 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
         }
         const int64_t irow = (int64_t)(e & kRowMask);
         const int inp = (int)(e >> 30) + 1;
-        inext = order_at(ipos);
-        ipos = atomicAdd(&a.ws.work[3], 1u);
+        const int total = inp * nst;
+        const int claim_at = max(0, total - (kCNSt + 1));  // stage index that claims the next row
         const unsigned char* src =
             reinterpret_cast<const unsigned char*>(a.x) + irow * a.ld * (int64_t)sizeof(E);
         bool ok = true;
-        for (int pass = 0; pass < inp && ok; ++pass) {
+        for (int cs = 0; cs < total; ++cs, ++gi) {
+          const int pass = cs / nst, c = cs - pass * nst;
           // top-p rows: the first two passes are kept in L2 for the ones that follow
           const uint64_t pol = (inp > 1 && pass < 2) ? pol_last : pol_first;
-          for (int c = 0; c < nst; ++c, ++gi) {
-            const int slot = (int)(gi % kCNSt);
-            const uint32_t use = gi / kCNSt;
-            // after an error nothing more is issued (a slot may still be in use)
-            if ((use > 0 && !cwait(&sm.empty[slot], (use - 1) & 1u, budget, &sm.abort_flag)) ||
-                ld_abort(&sm.abort_flag)) {
-              ok = false;
-              break;
-            }
-            const int64_t nc = min((int64_t)SE, V - (int64_t)c * SE);
-            const uint32_t bytes = (uint32_t)((nc * (int64_t)sizeof(E)) & ~(int64_t)15);
-            sm.srow[slot] = irow;
-            mbar_arrive_expect_tx(&sm.full[slot], bytes);
-            if (bytes)
-              bulk_g2s_pol(ring + slot * kCStageBytes, src + (int64_t)c * kCStageBytes, bytes,
-                           &sm.full[slot], pol);
+          const int slot = (int)(gi % kCNSt);
+          const uint32_t use = gi / kCNSt;
+          // after an error nothing more is issued (a slot may still be in use)
+          if ((use > 0 && !cwait(&sm.empty[slot], (use - 1) & 1u, budget, &sm.abort_flag)) ||
+              ld_abort(&sm.abort_flag)) {
+            ok = false;
+            break;
           }
+          if (cs == claim_at) pend = atomicAdd(&a.ws.work[3], 1u);
+          const int64_t nc = min((int64_t)SE, V - (int64_t)c * SE);
+          const uint32_t bytes = (uint32_t)((nc * (int64_t)sizeof(E)) & ~(int64_t)15);
+          sm.srow[slot] = irow;
+          mbar_arrive_expect_tx(&sm.full[slot], bytes);
+          if (bytes)
+            bulk_g2s_pol(ring + slot * kCStageBytes, src + (int64_t)c * kCStageBytes, bytes,
+                         &sm.full[slot], pol);
         }
         if (!ok) break;
       }
@@ -541,20 +559,19 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
 
         if constexpr (KIND == kCTopK) {
           if (c == 0) {
-            // a lower bound of the row's k-th value from the first stage.
+            // a lower bound of the row's k-th value from the first stage. k <= 128: every
+            // warp finds the k-th largest of its own 128 vector maxima by bisection on the
+            // key bits
+            // and the row keeps the largest of these (each is the k-th largest of a subset
+            // of the row); one barrier. Larger k: the stage's k-th largest value.
             if (k <= kCMerge) {
-              // the k-th largest vector maximum of the stage
+              uint32_t kv[kCVecs];
 #pragma unroll
-              for (int u = 0; u < kCVecs; ++u)
-                sm.w.tk.keys[vbase + u * 32] = (vmv[u] > -INFINITY) ? fkey(vmv[u]) : 0u;
-              cbar();
-              const uint32_t t0 = sel::select_bound<kCC, CBar>(
-                  kCStageVecs, [&](int i) { return sm.w.tk.keys[i]; }, (uint32_t)k,
-                  bf16 ? 2 : 4, sm.sc);
-              if (tid == 0) sm.tau = t0;
+              for (int u = 0; u < kCVecs; ++u) kv[u] = (vmv[u] > -INFINITY) ? fkey(vmv[u]) : 0u;
+              const uint32_t mykey = warp_kth_key(kv, k, lowv);
+              if (lane == 0 && mykey) atomicMax(&sm.tau, mykey);
               cbar();
             } else {
-              // the stage's own k-th largest value
               uint32_t* skeys = reinterpret_cast<uint32_t*>(sm.w.list);
 #pragma unroll
               for (int u = 0; u < kCVecs; ++u) {
@@ -613,7 +630,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
           }
           // k > 128: the list is checked every few stages (and after the last) and compacted
           // when it passes half its capacity. k <= 128 lists are only checked at the end.
-          if (k > kCMerge && ((c + 1) % 4 == 0 || c == nst - 1)) {
+          if (k > kCMerge && ((c + 1) % 8 == 0 || c == nst - 1)) {
             cbar();
             const uint32_t cnt = sm.lcnt;
             cbar();

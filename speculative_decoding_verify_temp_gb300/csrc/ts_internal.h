@@ -137,9 +137,9 @@ cudaError_t launch_logprobs_probs(const float* p, int64_t ld, int64_t V, int64_t
 
 // ---- row-streaming kernel (ts_sample.cu) -----------------------------------------
 
-// Target-only chain sampling from logits: a persistent row-streaming kernel that serves
-// every row (greedy ones included). Requires 16-byte aligned rows and vocab <=
-// kRowMaxVocab.
+// Arguments of the row-streaming kernels: the renorm of probability rows (ts_sample.cu)
+// and target-only chain sampling from logits (ts_chain.cu). Both require 16-byte aligned
+// rows and vocab <= kRowMaxVocab.
 struct SampleArgs {
   const void* x;
   int32_t bf16;
@@ -163,7 +163,6 @@ struct SampleArgs {
   uint64_t wait_cycles;  // chain kernel: SM clock cycles a stage wait may take
 };
 
-cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s);
 // The row kernel in its renorm mode (fp32 probability rows, 16-byte aligned).
 cudaError_t launch_renorm_rows(const SampleArgs& a, cudaStream_t s);
 cudaError_t row_read_error(uint32_t* word, int clear);

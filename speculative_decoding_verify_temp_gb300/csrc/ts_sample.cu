@@ -1,31 +1,25 @@
-// Row-streaming kernel for target-only chain sampling from logits (TokenSpeed
-// flashinfer.py verify(): sampling_argmax for greedy requests; softmax with temperature,
-// fused top-k/top-p renorm and chain_speculative_sampling_target_only for the others),
-// and, in its renorm mode, for top-k/top-p renormalisation of probability rows
-// (fused_topk_topp_renorm).
+// Row-streaming kernel for the top-k/top-p renormalisation of probability rows (TokenSpeed
+// flashinfer.py verify(): fused_topk_topp_renorm). Its row machinery was first written for
+// chain sampling as well; chain sampling from logits now runs in ts_chain.cu, and only
+// the renorm mode (RN = true) is instantiated.
 //
-// A persistent CTA (2 an SM) takes one row after another: chain rows from a shared
-// counter that runs over the rows in four cost tiers, longest kind first; renorm rows
-// (no workspace) from a tiered order that every CTA computes alike. A producer warp
-// streams each row through a ring of kRNSt shared-memory stages of 16 KB (bulk copies
-// completing on mbarriers, the next row's stages already in flight while a row is
-// finished); 8 consumer warps copy their vectors of a stage to registers, free the slot,
-// keep running row state, and finish the row after its last stage:
-//  - every row: maximum, argmax (lowest id), temperature-1 log-sum-exp;
+// A persistent CTA (2 an SM) takes one row after another from a tiered order that every
+// CTA computes alike (large top-k and general rows, then top-p rows, then the rest; no
+// workspace). A producer warp streams each row through a ring of kRNSt shared-memory
+// stages of 16 KB (bulk copies completing on mbarriers, the next row's stages already in
+// flight while a row is finished); 8 consumer warps copy their vectors of a stage to
+// registers, free the slot, keep running row state, and finish the row after its last
+// stage:
 //  - top-k (k <= kSTopK): a candidate list in shared memory above a running threshold:
 //    first a lower bound of the row's k-th value from the first stage (its k-th largest
 //    vector maximum, or for k > 256 its k-th largest value), later the k-th largest
-//    candidate value whenever the list fills; at the end the row's top k, the top-p
-//    prefix within it, and the draw in token-id order by a radix walk over the ids;
-//  - neither knob: the mass of every warp's 128 vectors of a stage relative to their
-//    maximum; at the end these ranges, scaled to the row maximum, locate the draw, and
-//    only that range is read again;
-//  - top-p alone: a histogram over sixteenth-of-an-octave buckets on fixed edges
-//    (multiples of T ln 2 / 16) of the weights relative to their bucket's upper edge, so
-//    that no maximum is needed while streaming (probabilities: linear buckets from the
-//    float's exponent and leading mantissa bits); at the end the bucket where the ordered
-//    mass crosses top_p, one more read of the row for the whole-bucket masses per range
-//    and the crossing bucket's elements (resolved exactly), then the draw.
+//    candidate value whenever the list fills; at the end the row's top k and the top-p
+//    prefix within it;
+//  - neither knob: the row's exact mass;
+//  - top-p alone: a histogram over linear buckets (the float's exponent and leading
+//    mantissa bits) of the probabilities relative to their bucket's upper edge; at the
+//    end the bucket where the ordered mass crosses top_p, one more read of the row for the
+//    mass above it and the crossing bucket's elements (resolved exactly).
 // Renorm rows are read once more through the ring to write max(p, 0) / Z or 0. Rows the
 // summaries cannot serve (top_k above kSTopK, candidate overflow, a row maximum far
 // above the first stage's, an oversized crossing bucket) take a general path: radix
@@ -1450,11 +1444,6 @@ cudaError_t launch_row_kernel(const SampleArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 }  // namespace
-
-cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s) {
-  if (a.rows <= 0) return cudaSuccess;
-  return a.bf16 ? launch_row_kernel<uint16_t, false>(a, s) : launch_row_kernel<float, false>(a, s);
-}
 
 cudaError_t launch_renorm_rows(const SampleArgs& a, cudaStream_t s) {
   if (a.rows <= 0 || a.bf16 || !a.out) return cudaErrorInvalidValue;
