@@ -207,17 +207,17 @@ ts_status ts_gather_logprobs(const void* x, ts_dtype dt, int32_t is_probs, int64
 /* Greedy chain verification that allocates nothing and takes no workspace. The pages
  * have no counterpart: this entry point exists for callers that cannot give the library
  * device memory, such as a host binding the C ABI without a device allocator of its own,
- * or code running where cudaMalloc is not allowed (inside CUDA stream capture, or under a
- * memory budget owned by another allocator). Same arguments, outputs and semantics as
- * ts_verify_chain_greedy, minus workspace/ws_bytes.
- * Scratch: a file-scope device array of 4 MiB that every GPU loading the library holds
- * until the process exits. Calls with batch*(D+1) > TS_STATIC_MAX_ROWS are rejected with
- * TS_ERR_INVALID_ARG. The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) once for that device; make that first call before any stream
- * capture. Each call clears the array's arrival counters on `stream` (cudaMemsetAsync)
- * and calls no allocating routine. All calls share the one array: calls that may overlap
- * on the GPU (different streams, or devices sharing it) race and must be serialised by
- * the caller. */
+ * or code whose device memory is a fixed budget owned by another allocator. Same
+ * arguments, outputs and semantics as ts_verify_chain_greedy, minus workspace/ws_bytes.
+ * Scratch: a file-scope device array of 4 MiB; every GPU that loads the library holds
+ * its own copy until the process exits. Calls with batch*(D+1) > TS_STATIC_MAX_ROWS are
+ * rejected with TS_ERR_INVALID_ARG. Each call looks up the array's device address on the
+ * current device (cudaGetSymbolAddress, which allocates nothing); the first call on a
+ * device also loads the library's device code there, so make that first call before any
+ * stream capture. Each call clears the array's arrival counters on `stream`
+ * (cudaMemsetAsync) and calls no allocating routine. All calls on one device share that
+ * device's copy of the array: calls that may overlap on the same device (different
+ * streams or host threads) race and must be serialised by the caller. */
 #define TS_STATIC_MAX_ROWS 2048
 ts_status ts_verify_chain_greedy_static(const void* target_logits, ts_dtype dt, int64_t batch,
                                         int32_t D, int64_t vocab, int64_t ld,

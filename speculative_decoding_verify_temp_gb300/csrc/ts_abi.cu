@@ -5,7 +5,6 @@
 #include <stdio.h>
 
 #include <atomic>
-#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -447,9 +446,9 @@ ts_status ts_gather_logprobs(const void* x, ts_dtype dt, int32_t is_probs, int64
 // Greedy chain verification without a caller workspace.
 //
 // Some callers cannot hand the library device memory: a host that binds the C ABI
-// without any device allocator of its own, or code that runs where cudaMalloc is not
-// allowed (inside stream capture, where it would break the capture, or under a fixed
-// memory budget owned by another allocator). For them this variant keeps its scratch
+// without any device allocator of its own, or code whose device memory is a fixed budget
+// owned by another allocator that the library may not draw from. For them this variant
+// keeps its scratch
 // (arrival counters and per-split partials) in a file-scope device array that every GPU
 // loading the library holds until the process exits. Its size is fixed, so the number
 // of rows it can serve is capped.
@@ -459,27 +458,16 @@ namespace {
 constexpr size_t kStaticScratchBytes = (size_t)4 << 20;  // 4 MiB per device
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-constexpr int kStaticMaxDevices = 64;
-std::mutex g_static_mu;
-void* g_static_ptr[kStaticMaxDevices];  // device address of g_static_scratch, per device
-
-// The device address of the scratch array on the current device, looked up once per
-// device. (In host code the array's name is only a host-side handle, never a device
-// pointer.)
+// The device address of the scratch array on the current device. (In host code the
+// array's name is only a host-side handle, never a device pointer.) Looked up on every
+// call: the lookup allocates nothing and launches nothing, and a cached address could
+// outlive the context it was taken in (after cudaDeviceReset, say). The first lookup on
+// a device loads the library's device code there.
 ts_status static_scratch(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kStaticMaxDevices)
-    return fail(TS_ERR_INVALID_ARG, "device ordinal %d beyond %d", dev, kStaticMaxDevices);
-  std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-    g_static_ptr[dev] = p;
-  }
-  *out = g_static_ptr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+  *out = p;
   return TS_OK;
 }
 

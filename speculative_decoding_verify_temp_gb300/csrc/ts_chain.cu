@@ -117,15 +117,29 @@ __device__ __forceinline__ bool ld_abort(const int32_t* f) {
   return *reinterpret_cast<const volatile int32_t*>(f) != 0;
 }
 
+// One non-blocking probe of the phase of `bar` with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 "
+      "%0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of `bar` with the given parity; gives up after `budget` cycles of
 // this SM's clock or as soon as the CTA's abort flag is up, raising it (and the sticky
-// error word). Returns whether the phase completed.
+// error word). Returns whether the phase completed. Budgets below 2^20 cycles poll
+// without suspending (a suspended probe may outlast a short budget).
 __device__ __forceinline__ bool cwait(uint64_t* bar, uint32_t parity, unsigned long long budget,
                                       int32_t* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+  const bool short_budget = budget < (1ull << 20);
+  if (short_budget ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (short_budget ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 0u &&
         (ld_abort(abort_flag) || (unsigned long long)(clock64() - t0) > budget)) {
       *reinterpret_cast<volatile int32_t*>(abort_flag) = 1;

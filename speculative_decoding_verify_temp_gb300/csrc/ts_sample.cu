@@ -28,8 +28,10 @@
 // Weights are 2^((x - M) log2(e) / T) for the row maximum M (probabilities: p); masses
 // that decide a selection are sums of floor(w * 2^40); composite keys order tokens by
 // value, then by lowest id. Every wait on an mbarrier is bounded by the SM clock; a wait
-// that gives up sets an error word (ts_device_error reports it), after which the
-// producer issues no more copies and waits for those in flight before the CTA exits.
+// that gives up raises the CTA's abort flag and sets the reported error word
+// (ts_device_error); the producer then issues no more copies and waits for those in
+// flight, and the consumers leave the rows they have not written, all at the next row
+// boundary, before the CTA exits. A later launch starts clean.
 #include <stdint.h>
 
 #include "ts_common.cuh"
@@ -100,17 +102,22 @@ __device__ __forceinline__ float rn_edge(float b) {
   return __uint_as_float(((uint32_t)b + 1u) << 19);
 }
 
-__device__ __forceinline__ bool row_error() { return *(volatile unsigned int*)&g_row_err != 0; }
+// The CTA's abort flag: raised by a wait that gave up. It is the CTA's own, so that one
+// launch's error never reaches a later launch (the global word only reports).
+__device__ __forceinline__ bool row_error(const int32_t* ab) {
+  return *reinterpret_cast<const volatile int32_t*>(ab) != 0;
+}
 
-// Waits for the phase of `bar` with the given parity; gives up (setting the error word)
-// after kRWaitCycles of this SM's clock (monotonic) or once any thread has given up.
-// Returns whether the phase completed.
-__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity) {
+// Waits for the phase of `bar` with the given parity; gives up after kRWaitCycles of this
+// SM's clock (monotonic) or once the CTA has aborted, raising the CTA's abort flag and
+// setting the reported error word. Returns whether the phase completed.
+__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, int32_t* ab) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && (clock64() - t0 > kRWaitCycles || row_error())) {
+    if ((it & 63u) == 0 && (clock64() - t0 > kRWaitCycles || row_error(ab))) {
+      *reinterpret_cast<volatile int32_t*>(ab) = 1;
       atomicOr(&g_row_err, 1u);
       return false;
     }
@@ -167,6 +174,7 @@ struct RowSmem {
   int32_t redi[kRWarps];
   uint32_t lcnt, tau;
   int32_t bad;
+  int32_t abort_flag;
   float base;
   float M, S1;
   int32_t am;
@@ -197,6 +205,7 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
       mbar_init(&sm.empty[s], kRWarps);
     }
     fence_mbar_init();
+    sm.abort_flag = 0;
   }
   if (tid < 16) {
     sm.tab[tid] = exp2(-(double)tid / 16.0);
@@ -286,7 +295,7 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
         if (row < 0) {  // one last stage tells the consumers to stop
           const int slot = (int)(g % kRNSt);
           const uint32_t use = g / kRNSt;
-          if ((use > 0 && !bounded_wait(&sm.empty[slot], (use - 1) & 1u)) || row_error()) break;
+          if ((use > 0 && !bounded_wait(&sm.empty[slot], (use - 1) & 1u, &sm.abort_flag)) || row_error(&sm.abort_flag)) break;
           sm.srow[slot] = -1;
           mbar_arrive_expect_tx(&sm.full[slot], 0u);
           ++g;  // (the marker is the latest use of its slot)
@@ -302,7 +311,7 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
           const int slot = (int)(g % kRNSt);
           const uint32_t use = g / kRNSt;
           // after an error nothing more is issued (a slot may still be in use)
-          if ((use > 0 && !bounded_wait(&sm.empty[slot], (use - 1) & 1u)) || row_error()) {
+          if ((use > 0 && !bounded_wait(&sm.empty[slot], (use - 1) & 1u, &sm.abort_flag)) || row_error(&sm.abort_flag)) {
             ok = false;
             break;
           }
@@ -338,9 +347,13 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
     int64_t row;
     {
       const int slot = (int)(g % kRNSt);
-      bounded_wait(&sm.full[slot], (g / kRNSt) & 1u);
-      row = sm.srow[slot];
-      if (row < 0 || row >= a.rows) {
+      bounded_wait(&sm.full[slot], (g / kRNSt) & 1u, &sm.abort_flag);
+      row = *reinterpret_cast<volatile int64_t*>(&sm.srow[slot]);
+      // every consumer takes the same decision: the flag is read between two barriers
+      cbar();
+      const bool ab = row_error(&sm.abort_flag);
+      cbar();
+      if (ab || row < 0 || row >= a.rows) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[slot]);
         break;
@@ -419,7 +432,7 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
     // ---- the stages of the row -------------------------------------------------------
     for (int c = 0; c < nst; ++c, ++g) {
       const int slot = (int)(g % kRNSt);
-      bounded_wait(&sm.full[slot], (g / kRNSt) & 1u);
+      bounded_wait(&sm.full[slot], (g / kRNSt) & 1u, &sm.abort_flag);
       const uint4* sv = reinterpret_cast<const uint4*>(ring + slot * kRStageBytes);
       const int64_t c0 = (int64_t)c * SE;  // the stage's first element
       const int nc = (int)min((int64_t)SE, V - c0);
@@ -931,7 +944,7 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
         uint64_t zab = 0;
         for (int c = 0; c < nst; ++c, ++g) {
           const int slot = (int)(g % kRNSt);
-          bounded_wait(&sm.full[slot], (g / kRNSt) & 1u);
+          bounded_wait(&sm.full[slot], (g / kRNSt) & 1u, &sm.abort_flag);
           const int64_t c0 = (int64_t)c * SE;
           uint4 rv[kRVecs];
           if (active) {
@@ -1031,13 +1044,20 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
       } else {  // no knobs: everything is kept
         (void)sel::excl_scan<kRCons, sel::ConsumerBar>(zsum, sm.sc, Z);
       }
+      // a wait that gave up: the row (and the rest) is left unwritten
+      {
+        cbar();
+        const bool ab = row_error(&sm.abort_flag);
+        cbar();
+        if (ab) break;
+      }
       // the write pass
       const float scale = (Z > 0) ? __fdiv_rn(kFx, __ull2float_rn(Z)) : 0.f;
       float* orow = a.out + row * V;
       const bool vout = ((reinterpret_cast<uintptr_t>(orow) & 15) == 0);
       for (int c = 0; c < nst; ++c, ++g) {
         const int slot = (int)(g % kRNSt);
-        bounded_wait(&sm.full[slot], (g / kRNSt) & 1u);
+        bounded_wait(&sm.full[slot], (g / kRNSt) & 1u, &sm.abort_flag);
         const uint4* sv = reinterpret_cast<const uint4*>(ring + slot * kRStageBytes);
         const int64_t c0 = (int64_t)c * SE;
         const int nc = (int)min((int64_t)SE, V - c0);
@@ -1120,7 +1140,7 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
       const float fb = (float)bstar;
       for (int c = 0; c < nst; ++c, ++g) {
         const int slot = (int)(g % kRNSt);
-        bounded_wait(&sm.full[slot], (g / kRNSt) & 1u);
+        bounded_wait(&sm.full[slot], (g / kRNSt) & 1u, &sm.abort_flag);
         if (active) {
           const uint4* sv = reinterpret_cast<const uint4*>(ring + slot * kRStageBytes);
           const int64_t c0 = (int64_t)c * SE;

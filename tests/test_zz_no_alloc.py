@@ -1,9 +1,9 @@
 """The greedy verification entry point that allocates nothing.
 
 Callers that cannot give the library device memory (a host binding the C ABI without a
-device allocator, or code running where cudaMalloc is not allowed, such as inside
-stream capture) use ts_verify_chain_greedy_static, whose scratch is a fixed array inside
-the library. This checks it, through the C ABI, against the workspace entry point on two
+device allocator, or code whose device memory is a fixed budget owned by another
+allocator) use ts_verify_chain_greedy_static, whose scratch is a fixed array inside the
+library. This checks it, through the C ABI, against the workspace entry point on two
 calls in a row with different inputs (the second call must not see the first call's
 scratch), and that it rejects a call larger than its fixed scratch. The file is named to
 be collected last.
