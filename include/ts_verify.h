@@ -149,7 +149,9 @@ typedef struct ts_chain_args {
   const int32_t* top_k;      /* [batch] or NULL; logits only */
   const float* top_p;        /* [batch] or NULL; logits only */
   const float* draft_probs;  /* [batch*D, ld_draft] fp32, or NULL: target-only (the draft
-                                is a point mass on the drafted token) */
+                                is a point mass on the drafted token). With logit targets
+                                the rows must be 16-byte aligned and vocab <= 2^18 (else
+                                TS_ERR_INVALID_ARG) */
   int64_t ld_draft;
   const int32_t* draft_tokens; /* [batch, D]; ids outside [0, vocab) are never accepted */
   const int64_t* seed;       /* [batch] Philox key (two's-complement bits) */
@@ -175,7 +177,10 @@ typedef struct ts_chain_args {
  * drawn from p_D. The draw uses u_D: the smallest token id whose inclusive prefix mass,
  * in token-id order, exceeds u_D times the total mass. With explicit probabilities the
  * accept test is evaluated in fp32 (one rounded product); the residual max(p - q, 0) is
- * formed elementwise in fp32.
+ * formed elementwise in fp32. With logits and draft probabilities, p is the filtered
+ * distribution of the logits (temperature, top-k, top-p), the accept test compares
+ * u q(x) with p(x) in double, and the residual max(p - q, 0) of the rejected row is formed
+ * elementwise in fp32 from p's fixed-point weights.
  * Coins: uniforms if given, else Philox4x32-10 keyed by seed[b] with counter
  * (j, 0xFFFFFFFF, lo32(offset[b]), hi32(offset[b])), word 0 mapped to
  * (2*(w >> 9) + 1) * 2^-24.

@@ -303,9 +303,6 @@ ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t
     a.logprobs = p->logprobs;
     return launched(tsv::launch_draw_probs(a, stream), "probability-row chain launch");
   }
-  if (p->draft_probs)
-    return fail(TS_ERR_INVALID_ARG,
-                "logit targets with explicit draft probabilities are not supported by this build");
   if (p->vocab > tsv::staged_max_vocab(p->target_dtype == TS_BF16))
     return fail(TS_ERR_INVALID_ARG, "vocab %lld above the staged limit %d", (long long)p->vocab,
                 tsv::staged_max_vocab(p->target_dtype == TS_BF16));
@@ -355,8 +352,16 @@ ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t
     sa.logprobs = p->logprobs;
     sa.ws = a.ws;
     sa.wait_cycles = g_wait_cycles.load(std::memory_order_relaxed);
+    sa.q = p->draft_probs;
+    sa.ld_q = p->ld_draft;
     return launched(tsv::launch_chain(sa, stream), "row-streaming chain launch");
-  } else if (p->temperature) {
+  }
+  if (p->draft_probs)
+    return fail(TS_ERR_INVALID_ARG,
+                "logit targets with draft probabilities need 16-byte aligned rows and vocab "
+                "<= %lld",
+                (long long)tsv::kRowMaxVocab);
+  if (p->temperature) {
     // Greedy requests need only the argmax of each row: a streaming pass handles them,
     // and the staged kernel skips them.
     tsv::RowStatArgs g{};

@@ -198,7 +198,7 @@ struct alignas(16) CSmem {
   int32_t redi[kCW];
   uint32_t lcnt, tau;
   int32_t bad, abort_flag, owner, am;
-  float M, S1, uj, uD, vx;
+  float M, S1, uj, uD, vx, qx;
   int32_t pbi;
   int32_t gtop, gl, gh;
   uint64_t res_u, zall, ptarget;
@@ -849,6 +849,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
                                       : verify_coin(seed, off, (uint32_t)D))
                         : 0.f;
           sm.vx = xvalid ? SVec<E>::at(xr, x) : 0.f;
+          sm.qx = (a.q && j < D && xvalid) ? a.q[(req * D + j) * a.ld_q + x] : 0.f;
         }
       }
       cbar();
@@ -1004,9 +1005,26 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
     }
     const bool bad = sm.bad != 0;
 
+    // The accept test on the kept mass Z (the draft token's weight wx included):
+    // target-only u < p(x), with draft probabilities u q(x) < p(x).
+    const bool qmode = a.q != nullptr;
+    const float qx = sm.qx;
+    auto accept = [&](double Z, double wx) -> int32_t {
+      if (j >= D) return 0;
+      return (qmode ? (double)uj * (double)qx * Z < wx : (double)uj * Z < wx) ? 1 : 0;
+    };
+    // With draft probabilities the residual draw of a rejected row needs the draft row:
+    // rows before the last record their kept set and leave the draw to k_chain_resid.
+    const bool skip_draw = qmode && j < D;
     // records the row; the last row of its request to be recorded writes the chain
-    auto finish_row = [&](int32_t tok_f, int32_t acc_f) {
-      a.ws.rowres[row] = RowRes{M, am, sm.S1, tok_f, acc_f, {0, 0, 0}};
+    auto finish_row = [&](int32_t tok_f, int32_t acc_f, int32_t kset = 0, uint64_t Cf = 0,
+                          uint64_t Zf = 0) {
+      RowRes rr{M, am, sm.S1, tok_f, acc_f, {0, 0, 0}, Cf, Zf, 0, 0, kset, 0};
+      if (kset == 3) {
+        rr.gh = sm.gh;
+        rr.gl = sm.gl;
+      }
+      a.ws.rowres[row] = rr;
       __threadfence();
       const uint32_t prev = atomicAdd(&a.ws.creq[req], 1u);
       if (prev != (uint32_t)a.R - 1) return;
@@ -1022,6 +1040,10 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
         int32_t t = -1;
         if (jj < js) t = a.draft_tokens[req * D + jj];
         else if (jj == js) t = __ldcg(&a.ws.rowres[rj].tok);
+        if (qmode && jj == js && js < D) {  // the residual kernel writes this position
+          if (a.accept_index) a.accept_index[rj] = (int32_t)rj;
+          continue;
+        }
         a.accepted_tokens[rj] = t;
         if (a.accept_index) a.accept_index[rj] = (jj <= js) ? (int32_t)rj : -1;
         if (a.logprobs) {
@@ -1157,7 +1179,11 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
       }
       uint64_t wx = 0;
       if (xvalid && comp_key(fkey(vx), (uint32_t)x) >= C) wx = wfn(vx);
-      const int32_t acc = (j < D) && ((double)uj * (double)Z < (double)wx) ? 1 : 0;
+      const int32_t acc = accept((double)Z, (double)wx);
+      if (skip_draw) {
+        if (tid == 0) finish_row(-1, acc, 1, C, Z);
+        return;
+      }
       const uint64_t Zr = Z - wx;
       int32_t tok;
       if (Zr == 0) {
@@ -1173,7 +1199,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
             idx_sh, 3, sm.sc, &gsel);
         tok = (int32_t)comp_token(gsel);
       }
-      if (tid == 0) finish_row(tok, acc);
+      if (tid == 0) finish_row(tok, acc, 1, C, Z);
     };
 
     // ---- finish the row ---------------------------------------------------------------------
@@ -1225,8 +1251,10 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
         for (int64_t e = e0; e < e1; ++e) mine += __ldcg(rowslots + e);
         uint64_t Zr;
         const uint64_t ex = sel::excl_scan<kCC, CBar>(mine, sm.sc, Zr);
-        const int32_t acc = (j < D) && ((double)uj * (double)(Zr + wx) < (double)wx) ? 1 : 0;
-        if (Zr == 0) {
+        const int32_t acc = accept((double)(Zr + wx), (double)wx);
+        if (skip_draw) {
+          if (tid == 0) finish_row(-1, acc, 3, C, Zr + wx);
+        } else if (Zr == 0) {
           if (tid == 0) finish_row((wx > 0) ? x : am, acc);
         } else {
           draw_ranges(mine, ex, Zr, e0, e1, acc, [&](float v, int64_t gidx) -> float {
@@ -1280,9 +1308,19 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
         }
         Z = warp_sum_u64(Z);
         wx = warp_sum_u64(wx);
-        const int32_t acc = (j < D) && ((double)uj * (double)Z < (double)wx) ? 1 : 0;
-        const uint64_t Zr = Z - wx;
-        int32_t tok = (wx > 0) ? x : (int32_t)comp_token(srt[0]);  // srt[0]: the argmax
+        const int32_t acc = accept((double)Z, (double)wx);
+        // the kept set is a prefix of the value order: its smallest composite bounds it
+        uint64_t Cmin = ~0ull;
+#pragma unroll
+        for (int e = 0; e < kCSmallE; ++e)
+          if (kept[e] && v[e] < Cmin) Cmin = v[e];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const uint64_t y = __shfl_xor_sync(0xffffffffu, Cmin, o);
+          Cmin = y < Cmin ? y : Cmin;
+        }
+        const uint64_t Zr = skip_draw ? 0ull : Z - wx;
+        int32_t tok = skip_draw ? -1 : ((wx > 0) ? x : (int32_t)comp_token(srt[0]));  // srt[0]: the argmax
         if (Zr > 0) {
           uint64_t t = (uint64_t)((double)uD * (double)Zr);
           if (t >= Zr) t = Zr - 1;
@@ -1323,7 +1361,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
           for (int o = 16; o > 0; o >>= 1) f = min(f, __shfl_xor_sync(0xffffffffu, f, o));
           if (f != INT32_MAX) tok = f;
         }
-        if (lane == 0) finish_row(tok, acc);
+        if (lane == 0) finish_row(tok, acc, 1, Cmin, Z);
       }
     } else if (kn.kind == kCTopK) {
       const int nl = (int)sm.lcnt;
@@ -1349,10 +1387,11 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
       }
       uint64_t wx = 0;
       if (xvalid && comp_key(fkey(vx), (uint32_t)x) >= C) wx = wfn(vx);
-      const int32_t acc = (j < D) && ((double)uj * (double)Z < (double)wx) ? 1 : 0;
-      const uint64_t Zr = Z - wx;
-      int32_t tok;
-      if (Zr == 0) {
+      const int32_t acc = accept((double)Z, (double)wx);
+      const uint64_t Zr = skip_draw ? 0ull : Z - wx;
+      int32_t tok = -1;
+      if (skip_draw) {
+      } else if (Zr == 0) {
         tok = (wx > 0) ? x : am;
       } else {
         uint64_t t = (uint64_t)((double)uD * (double)Zr);
@@ -1365,7 +1404,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
             idx_sh, 3, sm.sc, &gsel);
         tok = (int32_t)comp_token(gsel);
       }
-      if (tid == 0) finish_row(tok, acc);
+      if (tid == 0) finish_row(tok, acc, 1, C, Z);
     } else {  // kCPlain: the warp ranges scaled to the row maximum, in token order
       const int64_t E_ = (int64_t)nst * kCW;
       const int64_t per = (E_ + kCC - 1) / kCC;
@@ -1383,8 +1422,10 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
       double Zr;
       const double ex = excl_scan_f64_t<kCW, CBar>(mine, sm.dscan, Zr);
       const double wx = xvalid ? (double)ex2((vx - M) * sl2) : 0.0;
-      const int32_t acc = (j < D) && ((double)uj * (Zr + wx) < wx) ? 1 : 0;
-      if (!(Zr > 0.0)) {
+      const int32_t acc = accept(Zr + wx, wx);
+      if (skip_draw) {
+        if (tid == 0) finish_row(-1, acc, 2, 1ull, (uint64_t)((Zr + wx) * 1099511627776.0));
+      } else if (!(Zr > 0.0)) {
         if (tid == 0) finish_row((wx > 0.0) ? x : am, acc);
       } else {
         const double t = (double)uD * Zr;
@@ -1440,6 +1481,126 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
 
 }
 
+
+// With draft probabilities, the residual draw of every request rejected before its last
+// row (TensorRT-LLM rejection_sampling_one_model: at the first rejection j*, a token from
+// norm(max(p - q, 0))): p''_j* is recomputed from the row's recorded kept set (its
+// weights over the recorded kept mass), the residual max(p'' - q, 0) is formed
+// elementwise in fp32 and summed in 2^-40 fixed point, and the draw is the smallest token
+// id whose inclusive prefix mass exceeds u_D times the total (a zero residual draws from
+// p''). One CTA per request; it writes accepted_tokens[b, j*] and its logprob.
+template <typename E>
+__global__ void __launch_bounds__(256) k_chain_resid(SampleArgs a) {
+  __shared__ uint64_t tot[8];
+  __shared__ int32_t s_tok;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t b = blockIdx.x;
+  const int32_t D = a.D, R = a.R;
+  const int32_t L = __ldcg(&a.accept_length[b]);
+  if (L < 1 || L > D) return;  // every draft accepted (the bonus is drawn), or unfinished
+  const int32_t js = L - 1;
+  const int64_t row = b * R + js;
+  const RowRes* rp = a.ws.rowres + row;
+  const float M = __ldcg(&rp->M);
+  const int32_t am = __ldcg(&rp->am);
+  const int32_t kind = __ldcg(&rp->kind);
+  const E* xr = reinterpret_cast<const E*>(a.x) + row * a.ld;
+  int32_t tok = am;
+  if (kind != 0) {
+    const CKnobs kn = cknobs(a, b);
+    const float sl2 = __fdiv_rn(kLog2e, kn.T);
+    const float s16 = sl2 * 16.f;
+    const uint64_t C = __ldcg(&rp->C), Zk = __ldcg(&rp->Zk);
+    const int32_t gh = __ldcg(&rp->gh), gl = __ldcg(&rp->gl);
+    const float invZ = (float)(1.0 / (double)(Zk ? Zk : 1ull));
+    const float* qr = a.q + (b * D + js) * a.ld_q;
+    const int64_t V = a.V;
+    auto six_i = [&](float v) -> int {
+      float t = __fmaf_rd(v, s16, 12582912.f);
+      t = fminf(fmaxf(t, 8388608.f), 16777216.f);
+      return __float_as_int(t) - 0x4B400000;
+    };
+    // p''_i, and the residual weight of token i in fixed point
+    auto pw = [&](int64_t i) -> float {
+      const float v = SVec<E>::at(xr, i);
+      if (v == -INFINITY) return 0.f;
+      bool kept = kind == 2;
+      if (kind == 1) kept = comp_key(fkey(v), (uint32_t)i) >= C;
+      if (kind == 3) {
+        const int g = six_i(v);
+        kept = g > gh || (g >= gl && comp_key(fkey(v), (uint32_t)i) >= C);
+      }
+      if (!kept) return 0.f;
+      return __ull2float_rn(fixw(ex2((v - M) * sl2))) * invZ;
+    };
+    auto rw = [&](int64_t i, bool from_p) -> uint64_t {
+      const float p = pw(i);
+      const float r = from_p ? p : fmaxf(p - qr[i], 0.f);
+      return __float2ull_rz(r * kFx);
+    };
+    const int64_t Lw = ((V + 8 * 32 - 1) / (8 * 32)) * 32;  // a warp's contiguous block
+    const int64_t w0 = min(V, (int64_t)warp * Lw), w1 = min(V, w0 + Lw);
+    bool from_p = false;
+    uint64_t Zr = 0;
+    for (int round = 0; round < 2; ++round) {
+      uint64_t wt = 0;
+      for (int64_t i = w0 + lane; i < w1; i += 32) wt += rw(i, from_p);
+      wt = warp_sum_u64(wt);
+      if (lane == 0) tot[warp] = wt;
+      __syncthreads();
+      Zr = 0;
+      for (int w2 = 0; w2 < 8; ++w2) Zr += tot[w2];
+      if (Zr > 0 || from_p) break;
+      from_p = true;  // a zero residual draws from p''
+      __syncthreads();
+    }
+    if (Zr > 0) {
+      const uint64_t seed = a.seed ? (uint64_t)a.seed[b] : 0;
+      const uint64_t off = a.offset ? (uint64_t)a.offset[b] : 0;
+      const float uD = a.uniforms ? a.uniforms[b * R + D] : verify_coin(seed, off, (uint32_t)D);
+      uint64_t t = (uint64_t)((double)uD * (double)Zr);
+      if (t >= Zr) t = Zr - 1;
+      uint64_t acc = 0;
+      int ws = 7;
+      for (int w2 = 0; w2 < 8; ++w2) {
+        if (t < acc + tot[w2]) {
+          ws = w2;
+          break;
+        }
+        acc += tot[w2];
+      }
+      if (warp == ws) {
+        int32_t found = -1;
+        for (int64_t s0 = w0; s0 < w1 && found < 0; s0 += 32) {
+          const int64_t i = s0 + lane;
+          const uint64_t wi = (i < w1) ? rw(i, from_p) : 0ull;
+          uint64_t inc = wi;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+          }
+          const unsigned hit = __ballot_sync(0xffffffffu, wi > 0 && acc + inc > t);
+          if (hit) found = (int32_t)(s0 + __ffs(hit) - 1);
+          acc += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) s_tok = found;
+      }
+      __syncthreads();
+      if (s_tok >= 0) tok = s_tok;
+    }
+  }
+  if (tid == 0) {
+    a.accepted_tokens[row] = tok;
+    if (a.logprobs) {
+      float lp = 0.f;
+      if (tok >= 0 && (int64_t)tok < a.V)
+        lp = (SVec<E>::at(xr, tok) - M) - logf(__ldcg(&a.ws.rowres[row].S));
+      a.logprobs[row] = lp;
+    }
+  }
+}
+
 template <typename E>
 cudaError_t launch_chain_t(const SampleArgs& a, cudaStream_t s) {
   int dev = 0, nsm = 148;
@@ -1456,6 +1617,9 @@ cudaError_t launch_chain_t(const SampleArgs& a, cudaStream_t s) {
   e = cudaFuncSetAttribute(k_chain<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
   if (e != cudaSuccess) return e;
   k_chain<E><<<grid, kCThreads, dyn, s>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !a.q) return e;
+  k_chain_resid<E><<<(unsigned)(a.rows / a.R), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

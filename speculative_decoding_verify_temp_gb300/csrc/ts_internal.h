@@ -33,13 +33,19 @@ struct alignas(16) Part {
 };
 
 // Per-row result handed from the row kernels to the request-level chain writer.
-struct alignas(32) RowRes {
+struct alignas(64) RowRes {
   float M;       // row maximum (raw logits)
   int32_t am;    // row argmax
   float S;       // sum exp(x - M) at temperature 1 (logprobs), or 0
   int32_t tok;   // drawn token of this row (residual or bonus draw), -1 if none
   int32_t acc;   // 1 if the draft of this row was accepted
   int32_t pad[3];
+  // the chain kernel's kept set, for a residual draw against draft probabilities:
+  uint64_t C;    // threshold composite (a token is kept iff its composite >= C)
+  uint64_t Zk;   // kept mass in 2^-40 units of the maximum's weight
+  int32_t gh, gl;  // top-p rows: sixteenths above gh are kept, gl..gh by C
+  int32_t kind;    // 0 greedy (the argmax), 1 by C, 2 every token, 3 top-p window + C
+  int32_t pad2;
 };
 
 // Per-request partial of the streaming draw: residual mass and base mass.
@@ -161,6 +167,8 @@ struct SampleArgs {
   Workspace ws;
   float* out;  // top-k/top-p renorm of probability rows: [rows, V] fp32 (no workspace)
   uint64_t wait_cycles;  // chain kernel: SM clock cycles a stage wait may take
+  const float* q;        // chain kernel: draft probabilities [B*D, ld_q] fp32, or NULL
+  int64_t ld_q;
 };
 
 // The row kernel in its renorm mode (fp32 probability rows, 16-byte aligned).

@@ -552,3 +552,59 @@ def test_selection_routes(V, dtype, k, p, T):
     ok = marg > BOUNDARY
     np.testing.assert_array_equal(got[ok] > 0, want[ok] > 0)
     np.testing.assert_allclose(got[ok], want[ok], rtol=1e-5, atol=1e-6)
+
+
+# ---- logits with explicit draft probabilities --------------------------------------------
+
+def _draws(rng, q):
+    """One draw per row of q (input preparation: the drafts are sampled from q)."""
+    c = np.cumsum(q.astype(np.float64), axis=-1)
+    u = rng.random(c.shape[0]) * c[:, -1]
+    return np.minimum((c < u[:, None]).sum(-1), q.shape[-1] - 1).astype(np.int32)
+
+
+@pytest.mark.parametrize("B,D,V,dtype", [(4, 3, 1024, "f32"), (32, 3, 50000, "bf16"),
+                                         (16, 7, 151936, "f32"), (24, 2, 8195, "bf16")])
+def test_logits_with_draft_probs(B, D, V, dtype):
+    # the target distribution is the filtered softmax of the logits (temperature, top-k,
+    # top-p); drafts are drawn from q, the softmax of noisy target logits; the accept test
+    # uses q(x) and a rejected row draws from norm(max(p'' - q, 0))
+    rng = np.random.default_rng(B * 7 + V)
+    R = D + 1
+    d = _rand_logits(rng, B * R, V, dtype, sigma=2.5, zipf=V > 2000)
+    lg = d["logits"].reshape(B, R, V)[:, :D].astype(np.float64)
+    noisy = lg + rng.standard_normal(lg.shape) * 0.7
+    e = np.exp(noisy - noisy.max(-1, keepdims=True))
+    q = (e / e.sum(-1, keepdims=True)).astype(np.float32)
+    drafts = _draws(rng, q.reshape(B * D, V)).reshape(B, D)
+    T = rng.choice(np.array([0.0, 0.7, 1.0, 1.3], np.float32), B)
+    k = rng.choice(np.array([0, 20, 500], np.int32), B).astype(np.int32)
+    tp = rng.choice(np.array([1.0, 0.9], np.float32), B).astype(np.float32)
+    seed = synth.request_seeds(B)
+    off = np.arange(B, dtype=np.int64)
+    x = dev_logits(d)
+    if V % 8:  # a ragged vocabulary in rows padded to 16-byte multiples (the kernel's route)
+        ld = (V + 7) // 8 * 8
+        full = torch.zeros((B * R, ld), dtype=x.dtype, device=x.device)
+        full[:, :V] = x
+        x = full[:, :V]
+    g = tv.chain_spec_sampling(x, True, D, dev(drafts), draft_probs=dev(q),
+                               temperature=dev(T), top_k=dev(k), top_p=dev(tp), seed=dev(seed),
+                               offset=dev(off), logprobs=True)
+    ref = oracle.chain_spec_sampling(d["logits"], True, D, drafts, draft_probs=q, temperature=T,
+                                     top_k=k, top_p=tp, seed=seed, offset=off)
+    compare_chain(g, ref, dtype)
+    # both outcomes occur: some requests reject before their last row (the residual draw)
+    alen = g["accept_length"].cpu().numpy()
+    assert (alen <= D).any()
+
+
+def test_logits_with_draft_probs_unaligned_rows_are_refused():
+    V, D, B = 1001, 2, 3
+    x = torch.zeros((B * (D + 1), V + 1), dtype=torch.bfloat16, device="cuda")[:, :V]
+    q = torch.full((B * D, V), 1.0 / V, device="cuda")
+    drafts = torch.zeros((B, D), dtype=torch.int32, device="cuda")
+    seed = torch.zeros(B, dtype=torch.int64, device="cuda")
+    with pytest.raises(tv.TsError) as e:
+        tv.chain_spec_sampling(x, True, D, drafts, draft_probs=q, seed=seed, offset=seed)
+    assert e.value.status == 1
