@@ -1,5 +1,8 @@
 """Helpers for the GPU parity tests: device tensors from the seeded inputs, and the
 comparison rules (exact for integers; boundary decisions counted, not failed)."""
+import multiprocessing
+import os
+
 import numpy as np
 import torch
 
@@ -48,3 +51,54 @@ def compare_chain(gpu: dict, ref: dict, dtype: str = "f32", max_boundary_frac: f
         lp = gpu["logprobs"].cpu().numpy()
         np.testing.assert_allclose(lp[ok], ref["logprobs"][ok], **TOL[dtype])
     return nb
+
+
+# ---- the oracle over whole launches, on every host core --------------------------------
+
+def _oracle_worker(task):
+    """One slice of requests through the oracle (runs in a spawned process)."""
+    import oracle
+    from speculative_decoding_verify_temp_gb300 import synth
+
+    fn, rows, bf16, args, kw = task
+    x = synth.f32_from_bf16_bits(rows) if bf16 else rows
+    return getattr(oracle, fn)(x, *args, **kw)
+
+
+def _slices(n, parts):
+    step = max(1, -(-n // parts))
+    return [(i, min(n, i + step)) for i in range(0, n, step)]
+
+
+def oracle_all(fn, rows, bf16, R, args=(), per_request=None, static=None, procs=None):
+    """oracle.<fn>(x, *args, **kw) over every request of a launch, the requests split over
+    the host cores (the method is per request: each request's coins come from its own seed
+    and offset, so the slices are independent). rows: the launch's [B*R, V] values as bf16
+    bits (bf16=True) or fp32. args: positional arguments, each (array, "row" | "req" |
+    None) - sliced by rows, by requests, or passed whole; per_request: keyword arrays of
+    one entry per request (None allowed); static: keyword arguments passed as they are.
+    Dict results (the chain calls) and tuple results are concatenated."""
+    B = rows.shape[0] // R
+    procs = procs or max(1, min(os.cpu_count() or 1, 32))
+    per_request = per_request or {}
+    tasks = []
+    for b0, b1 in _slices(B, procs):
+        a = []
+        for arr, by in args:
+            a.append(arr[b0 * R:b1 * R] if by == "row" else arr[b0:b1] if by == "req" else arr)
+        kw = {k: (None if v is None else v[b0:b1]) for k, v in per_request.items()}
+        kw.update(static or {})
+        tasks.append((fn, np.ascontiguousarray(rows[b0 * R:b1 * R]), bf16, tuple(a), kw))
+    with multiprocessing.get_context("spawn").Pool(len(tasks)) as pool:
+        parts = pool.map(_oracle_worker, tasks)
+    if isinstance(parts[0], dict):
+        # accept_index holds flat row numbers b*R + j: each slice counts from its own first
+        # request
+        bases = [b0 for b0, _ in _slices(B, procs)]
+        for p, b0 in zip(parts, bases):
+            if p.get("accept_index") is not None:
+                ai = p["accept_index"]
+                p["accept_index"] = np.where(ai >= 0, ai + b0 * R, ai)
+        return {k: (None if parts[0][k] is None else np.concatenate([p[k] for p in parts]))
+                for k in parts[0]}
+    return tuple(np.concatenate([p[i] for p in parts]) for i in range(len(parts[0])))

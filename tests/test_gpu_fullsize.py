@@ -1,8 +1,10 @@
 """GPU parity at the benchmark configurations' full sizes, in the launch configuration
-bench.py times (the same calls, workspaces and outputs). Every output is checked against
-the invariants of the method; a sample of requests (or rows) covering every knob kind is
-checked against the oracle, computed for those requests alone (the method is per
-request: coins come from each request's own seed and offset)."""
+bench.py times (the same calls, workspaces and outputs). Every request of every chain
+launch (and every Gumbel row) is checked against the oracle, which runs over the host
+cores in slices of requests (the method is per request: coins come from each request's
+own seed and offset); logprobs are on. The softmax and renorm legs, whose outputs are
+whole rows of probabilities, are checked on a sample of rows. Boundary requests (a
+decision within 1e-6 of flipping) are counted and printed, not failed."""
 import numpy as np
 import pytest
 import torch
@@ -10,7 +12,7 @@ import torch
 import oracle
 from speculative_decoding_verify_temp_gb300 import synth
 from speculative_decoding_verify_temp_gb300 import tsverify as tv
-from tests.gpu_util import BOUNDARY, TOL, compare_chain, dev
+from tests.gpu_util import BOUNDARY, TOL, compare_chain, dev, oracle_all
 
 pytestmark = pytest.mark.gpu
 
@@ -36,30 +38,6 @@ def step():
     return d
 
 
-def _rows_f32(d, reqs, R):
-    """fp32 logits of the rows of the given requests (widened from the bf16 bits)."""
-    rows = np.concatenate([np.arange(b * R, (b + 1) * R) for b in reqs])
-    return synth.f32_from_bf16_bits(np.ascontiguousarray(d["logits_bits"][rows])), rows
-
-
-def _sample(d, per_kind=5, seed=0):
-    """Requests of every kind: greedy, no knobs, top-p alone, small top-k, large top-k."""
-    T, k, p = d["temperature"], d["top_k"], d["top_p"]
-    kinds = [T < 1e-5,
-             (T >= 1e-5) & (k == 0) & (p >= 1),
-             (T >= 1e-5) & (k == 0) & (p < 1),
-             (T >= 1e-5) & (k > 0) & (k <= 256),
-             (T >= 1e-5) & (k > 256)]
-    rng = np.random.default_rng(seed)
-    out = []
-    for m in kinds:  # (a workload may have no request of a kind)
-        idx = np.flatnonzero(m)
-        if len(idx):
-            out.extend(rng.choice(idx, min(per_kind, len(idx)), replace=False).tolist())
-    assert len(out) >= per_kind
-    return np.array(sorted(out))
-
-
 def _chain_invariants(acc, alen, drafts, D, V):
     R = D + 1
     assert alen.min() >= 1 and alen.max() <= R
@@ -77,26 +55,27 @@ def test_verify_step_fullsize(step):
     d = step
     B, D, V = d["B"], d["D"], d["V"]
     R = D + 1
-    kw = dict(temperature=dev(d["temperature"]), top_k=dev(d["top_k"]), top_p=dev(d["top_p"]),
-              seed=dev(d["seed"]), offset=dev(d["offset"]),
-              workspace=tv.make_workspace(B, R, V, torch.device("cuda")),
-              outputs=tv._chain_outputs(B, R, torch.device("cuda"), False, False))
-    g = tv.chain_spec_sampling(d["dev_logits"], True, D, dev(d["draft_tokens"]), **kw)
-    acc = g["accepted_tokens"].cpu().numpy()
-    alen = g["accept_length"].cpu().numpy()
-    _chain_invariants(acc, alen, d["draft_tokens"], D, V)
-    # a second call on the same workspace gives the same bits
-    g2 = tv.chain_spec_sampling(d["dev_logits"], True, D, dev(d["draft_tokens"]), **kw)
-    np.testing.assert_array_equal(g2["accepted_tokens"].cpu().numpy(), acc)
-    reqs = _sample(d)
-    x, _ = _rows_f32(d, reqs, R)
-    ref = oracle.chain_spec_sampling(x, True, D, d["draft_tokens"][reqs],
-                                     temperature=d["temperature"][reqs], top_k=d["top_k"][reqs],
-                                     top_p=d["top_p"][reqs], seed=d["seed"][reqs],
-                                     offset=d["offset"][reqs], logprobs=False)
-    sub = {"accepted_tokens": torch.from_numpy(acc[reqs]),
-           "accept_length": torch.from_numpy(alen[reqs])}
-    compare_chain(sub, ref, "bf16", max_boundary_frac=0.1, check_logprobs=False)
+    kn = dict(temperature=dev(d["temperature"]), top_k=dev(d["top_k"]), top_p=dev(d["top_p"]),
+              seed=dev(d["seed"]), offset=dev(d["offset"]))
+    ws = tv.make_workspace(B, R, V, torch.device("cuda"))
+    # the bench's call (no logprobs, no accept_index) ...
+    g0 = tv.chain_spec_sampling(d["dev_logits"], True, D, dev(d["draft_tokens"]), **kn,
+                                workspace=ws,
+                                outputs=tv._chain_outputs(B, R, torch.device("cuda"), False, False))
+    acc0 = g0["accepted_tokens"].cpu().numpy()
+    alen0 = g0["accept_length"].cpu().numpy()
+    _chain_invariants(acc0, alen0, d["draft_tokens"], D, V)
+    # ... and the same call with every output on: the same decisions, on the same workspace
+    g = tv.chain_spec_sampling(d["dev_logits"], True, D, dev(d["draft_tokens"]), **kn,
+                               workspace=ws, logprobs=True)
+    np.testing.assert_array_equal(g["accepted_tokens"].cpu().numpy(), acc0)
+    np.testing.assert_array_equal(g["accept_length"].cpu().numpy(), alen0)
+    ref = oracle_all("chain_spec_sampling", d["logits_bits"], True, R,
+                     args=[(True, None), (D, None), (d["draft_tokens"], "req")],
+                     per_request=dict(temperature=d["temperature"], top_k=d["top_k"],
+                                      top_p=d["top_p"], seed=d["seed"], offset=d["offset"]))
+    nb = compare_chain(g, ref, "bf16", max_boundary_frac=0.05)
+    print(f"\nverify step B={B} D={D} V={V}: {B} requests checked, {nb} boundary")
 
 
 def test_greedy_verify_fullsize(step):
@@ -108,12 +87,11 @@ def test_greedy_verify_fullsize(step):
     acc = g["accepted_tokens"].cpu().numpy()
     alen = g["accept_length"].cpu().numpy()
     _chain_invariants(acc, alen, d["draft_tokens"], D, V)
-    reqs = np.arange(0, B, 17)
-    x, _ = _rows_f32(d, reqs, R)
-    ref = oracle.verify_chain_greedy(x, D, d["draft_tokens"][reqs])
-    np.testing.assert_array_equal(alen[reqs], ref["accept_length"])
-    np.testing.assert_array_equal(acc[reqs], ref["accepted_tokens"])
-    np.testing.assert_allclose(g["logprobs"].cpu().numpy()[reqs], ref["logprobs"], **TOL["bf16"])
+    ref = oracle_all("verify_chain_greedy", d["logits_bits"], True, R,
+                     args=[(D, None), (d["draft_tokens"], "req")])
+    np.testing.assert_array_equal(alen, ref["accept_length"])
+    np.testing.assert_array_equal(acc, ref["accepted_tokens"])
+    np.testing.assert_allclose(g["logprobs"].cpu().numpy(), ref["logprobs"], **TOL["bf16"])
 
 
 def test_gumbel_fullsize(step):
@@ -124,11 +102,12 @@ def test_gumbel_fullsize(step):
     tok = tv.gumbel_max_sample(d["dev_logits"], R, dev(Trow), dev(d["seed"]), dev(d["offset"]),
                                tv.make_workspace(B, R, V, torch.device("cuda"))).cpu().numpy()
     assert ((tok >= 0) & (tok < d["real_vocab"])).all()  # -inf pads never win
-    reqs = np.arange(3, B, 41)
-    x, rows = _rows_f32(d, reqs, R)
-    want, marg = oracle.gumbel_max_sample(x, R, Trow[rows], d["seed"][reqs], d["offset"][reqs])
+    want, marg = oracle_all("gumbel_max_sample", d["logits_bits"], True, R,
+                            args=[(R, None), (Trow, "row"), (d["seed"], "req"),
+                                  (d["offset"], "req")])
     ok = marg > BOUNDARY
-    np.testing.assert_array_equal(tok[rows][ok], want[ok])
+    np.testing.assert_array_equal(tok[ok], want[ok])
+    print(f"\nGumbel B={B} N={R} V={V}: {B * R} rows checked, {int((~ok).sum())} boundary")
 
 
 def test_softmax_fullsize(step):
@@ -156,19 +135,16 @@ def test_target_only_leg_fullsize():
                                top_p=dev(c["top_p"]), seed=dev(c["seed"]),
                                offset=dev(c["offset"]),
                                workspace=tv.make_workspace(B, R, V, torch.device("cuda")),
-                               outputs=tv._chain_outputs(B, R, torch.device("cuda"), False, False))
+                               logprobs=True)
     acc = g["accepted_tokens"].cpu().numpy()
     alen = g["accept_length"].cpu().numpy()
     _chain_invariants(acc, alen, c["draft_tokens"], D, V)
-    reqs = _sample(c, per_kind=4, seed=1)
-    x, _ = _rows_f32(c, reqs, R)
-    ref = oracle.chain_spec_sampling(x, True, D, c["draft_tokens"][reqs],
-                                     temperature=c["temperature"][reqs], top_k=c["top_k"][reqs],
-                                     top_p=c["top_p"][reqs], seed=c["seed"][reqs],
-                                     offset=c["offset"][reqs], logprobs=False)
-    sub = {"accepted_tokens": torch.from_numpy(acc[reqs]),
-           "accept_length": torch.from_numpy(alen[reqs])}
-    compare_chain(sub, ref, "bf16", max_boundary_frac=0.1, check_logprobs=False)
+    ref = oracle_all("chain_spec_sampling", c["logits_bits"], True, R,
+                     args=[(True, None), (D, None), (c["draft_tokens"], "req")],
+                     per_request=dict(temperature=c["temperature"], top_k=c["top_k"],
+                                      top_p=c["top_p"], seed=c["seed"], offset=c["offset"]))
+    nb = compare_chain(g, ref, "bf16", max_boundary_frac=0.05)
+    print(f"\ntarget-only B={B} D={D} V={V}: {B} requests checked, {nb} boundary")
 
 
 def test_rejection_and_renorm_legs_fullsize():
@@ -180,21 +156,18 @@ def test_rejection_and_renorm_legs_fullsize():
     g = tv.chain_spec_sampling(rp, False, D, dev(r["draft_tokens"]), draft_probs=rq,
                                seed=dev(r["seed"]), offset=dev(r["offset"]),
                                workspace=tv.make_workspace(B, R, V, torch.device("cuda")),
-                               outputs=tv._chain_outputs(B, R, torch.device("cuda"), False, True))
+                               outputs=tv._chain_outputs(B, R, torch.device("cuda"), True, True))
     acc = g["accepted_tokens"].cpu().numpy()
     alen = g["accept_length"].cpu().numpy()
     _chain_invariants(acc, alen, r["draft_tokens"], D, V)
-    reqs = np.arange(0, B, 23)
-    rows = np.concatenate([np.arange(b * R, (b + 1) * R) for b in reqs])
-    qrows = np.concatenate([np.arange(b * D, (b + 1) * D) for b in reqs])
-    q2 = r["draft_probs"].reshape(B * D, V)
-    ref = oracle.chain_spec_sampling(r["target_probs"][rows], False, D, r["draft_tokens"][reqs],
-                                     draft_probs=q2[qrows], seed=r["seed"][reqs],
-                                     offset=r["offset"][reqs])
-    sub = {"accepted_tokens": torch.from_numpy(acc[reqs]),
-           "accept_length": torch.from_numpy(alen[reqs]),
-           "logprobs": g["logprobs"][torch.from_numpy(reqs).cuda()]}
-    compare_chain(sub, ref, "f32", max_boundary_frac=0.1)
+    ref = oracle_all("chain_spec_sampling", r["target_probs"], False, R,
+                     args=[(False, None), (D, None), (r["draft_tokens"], "req")],
+                     per_request=dict(draft_probs=r["draft_probs"], seed=r["seed"],
+                                      offset=r["offset"]))
+    # the residual draws here are over 151936 tokens of nearly flat mass: a coin lands
+    # within 1e-6 of one of their CDF edges for several percent of the requests
+    nb = compare_chain(g, ref, "f32", max_boundary_frac=0.15)
+    print(f"\nrejection B={B} D={D} V={V}: {B} requests checked, {nb} boundary")
     # the renorm leg: the same probabilities with the target-only knob mix
     rrows = B * R
     rng = np.random.default_rng(1)
