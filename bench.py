@@ -44,7 +44,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-legs", action="store_true")
-    ap.add_argument("--cpu-sample", type=int, default=48, help="requests in the CPU baseline sample")
+    ap.add_argument("--cpu-sample", type=int, default=48,
+                    help="requests in the single-core CPU baseline sample "
+                         "(0: no CPU baseline, for profiling runs)")
     ap.add_argument("--knobs", default=None,
                     help="T,top_k,top_p applied to every request (profiling one selection route)")
     ap.add_argument("--batch", type=int, default=512,
@@ -175,9 +177,11 @@ class ClockSampler:
                 "power_w_max": max((num(r[2]) or 0.0) for r in rows)}
 
 
-def time_device(fn, steps: int, warmup: int, device):
+def time_device(fn, steps: int, warmup: int, device, per_step: bool = False):
     """Mean device time of one fn() call over `steps` timed calls (CUDA events on the
-    launching stream, barrier + synchronize on both sides, max over ranks)."""
+    launching stream, barrier + synchronize on both sides, max over ranks). With per_step,
+    also the 10th, 50th and 90th percentiles of the per-call times (an event between
+    consecutive calls)."""
     import torch
 
     for _ in range(warmup):
@@ -185,15 +189,22 @@ def time_device(fn, steps: int, warmup: int, device):
     torch.cuda.synchronize()
     barrier()
     s = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s)
-    for _ in range(steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1 if per_step else 2)]
+    ev[0].record(s)
+    for i in range(steps):
         fn()
-    e1.record(s)
+        if per_step:
+            ev[i + 1].record(s)
+    if not per_step:
+        ev[1].record(s)
     torch.cuda.synchronize()
     barrier()
-    ms = e0.elapsed_time(e1) / steps
-    return max_over_ranks(ms, device)
+    ms = max_over_ranks(ev[0].elapsed_time(ev[-1]) / steps, device)
+    if not per_step:
+        return ms
+    each = np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(steps)])
+    return ms, {"p10": float(np.percentile(each, 10)), "p50": float(np.percentile(each, 50)),
+                "p90": float(np.percentile(each, 90))}
 
 
 # ---- the workload -----------------------------------------------------------------------
@@ -210,8 +221,35 @@ def main_workload(batch: int = 512, knobs=None):
     return d
 
 
-def cpu_baseline(d, nreq: int):
-    """The oracle, as it stands, on the first nreq requests of the workload (1 core)."""
+def _oracle_slice(task):
+    """One slice of requests through the oracle (runs in a spawned process)."""
+    import oracle
+    from speculative_decoding_verify_temp_gb300 import synth
+
+    bits, D, drafts, kw = task
+    return oracle.chain_spec_sampling(synth.f32_from_bf16_bits(bits), True, D, drafts,
+                                      logprobs=False, **kw)
+
+
+def _cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                if k.strip() in ("model name", "Model", "CPU part"):
+                    return v.strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def cpu_baseline(d, nreq: int, gpu_out=None):
+    """The oracle, as it stands, on the host cores: on one core over the first nreq
+    requests, and over every core (requests in slices, one spawned process each) over the
+    whole step. The whole-step run also checks the GPU's outputs of the same step request
+    by request (exact tokens and lengths outside the boundary band)."""
+    import multiprocessing
+
     import oracle
     from speculative_decoding_verify_temp_gb300 import synth
 
@@ -219,16 +257,38 @@ def cpu_baseline(d, nreq: int):
     B, D, V = d["B"], d["D"], d["V"]
     R = D + 1
     nreq = min(nreq, B)
+    keys = ("temperature", "top_k", "top_p", "seed", "offset")
     x = synth.f32_from_bf16_bits(d["logits_bits"][: nreq * R])
     t0 = time.perf_counter()
-    oracle.chain_spec_sampling(x, True, D, d["draft_tokens"][:nreq],
-                               temperature=d["temperature"][:nreq], top_k=d["top_k"][:nreq],
-                               top_p=d["top_p"][:nreq], seed=d["seed"][:nreq],
-                               offset=d["offset"][:nreq], logprobs=False)
-    dt = time.perf_counter() - t0
-    return {"value": nreq * R / dt, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {nreq} requests ({nreq * R} rows) of the workload, "
-                      f"{dt:.1f} s single-threaded C"}
+    oracle.chain_spec_sampling(x, True, D, d["draft_tokens"][:nreq], logprobs=False,
+                               **{k: d[k][:nreq] for k in keys})
+    dt1 = time.perf_counter() - t0
+    single = {"value": nreq * R / dt1, "unit": "rows/s", "cores": 1,
+              "sample": f"first {nreq} requests ({nreq * R} rows), {dt1:.1f} s"}
+    procs = max(1, os.cpu_count() or 1)
+    step = -(-B // procs)
+    tasks = [(np.ascontiguousarray(d["logits_bits"][b * R:min(B, b + step) * R]), D,
+              np.ascontiguousarray(d["draft_tokens"][b:b + step]),
+              {k: d[k][b:b + step] for k in keys}) for b in range(0, B, step)]
+    with multiprocessing.get_context("spawn").Pool(len(tasks)) as pool:
+        pool.map(_oracle_slice, [(t[0][:R], D, t[2][:1], {k: v[:1] for k, v in t[3].items()})
+                                 for t in tasks])  # warm the workers (imports, builds)
+        t0 = time.perf_counter()
+        parts = pool.map(_oracle_slice, tasks)
+        dtn = time.perf_counter() - t0
+    ref = {k: np.concatenate([p[k] for p in parts]) for k in ("accepted_tokens", "accept_length",
+                                                               "margin")}
+    out = {"value": B * R / dtn, "unit": "rows/s", "cores": procs, "kind": "oracle",
+           "sample": f"the whole step ({B} requests, {B * R} rows) in {len(tasks)} slices over "
+                     f"{procs} processes, {dtn:.1f} s",
+           "cpu_model": _cpu_model(), "single_core": single}
+    if gpu_out is not None:
+        ok = ref["margin"] > 1e-6
+        acc, alen = gpu_out
+        mism = int(((acc != ref["accepted_tokens"]).any(axis=1) | (alen != ref["accept_length"]))[ok].sum())
+        out["parity"] = {"requests": int(B), "mismatches_outside_boundary": mism,
+                         "boundary_requests": int((~ok).sum()), "boundary": "margin <= 1e-6"}
+    return out
 
 
 def run_reference(args):
@@ -309,8 +369,9 @@ def run_ours(args):
 
     alg_bytes = rows * V * 2  # the logits, read once
     with ClockSampler(local) as clk:
-        ms = time_device(step, args.steps, args.warmup, device)
+        ms, pct = time_device(step, args.steps, args.warmup, device, per_step=True)
     clocks = clk.summary()
+    gpu_out = (outs[0].cpu().numpy(), outs[1].cpu().numpy())  # the last timed step's
     value = world * rows / (ms / 1e3)
     achieved = alg_bytes / (ms / 1e3) / 1e9
 
@@ -344,11 +405,12 @@ def run_ours(args):
 
     if rank != 0:
         return
-    cpu = cpu_baseline(d, args.cpu_sample)
-    traffic = ncu_traffic("k_row", "verify_step") if B == 512 else None
+    cpu = cpu_baseline(d, args.cpu_sample, gpu_out) if args.cpu_sample > 0 else None
+    traffic = ncu_traffic("k_chain", "verify_step") if B == 512 else None
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "ms_per_step_percentiles": pct,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": WORKLOAD if B == 512 else WORKLOAD.replace("B=512", f"B={B}"),
@@ -362,11 +424,13 @@ def run_ours(args):
         "hbm_gbs": achieved, "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": traffic, "kernel": "k_row<bf16> (one launch per step)",
+                     "traffic": traffic,
+                     "kernel": "k_chain<bf16> (the step: a one-CTA planning launch, then it)",
+                     "timed": "the whole step (both launches) with CUDA events",
                      "algorithmic_bytes_per_launch": alg_bytes},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "legs": legs,
     }
@@ -404,6 +468,46 @@ def run_legs(args, d, logits, device, tv, synth, peak):
     ms = time_device(lambda: tv.gumbel_max_sample(logits, R, Trow, seed, off, wsg, out=tok),
                      steps, warm, device)
     rec("gumbel_B512_N4_V201088_bf16", ms, rows, rows * V * 2)
+    # the verify step with every output on (logprobs at temperature 1, accept_index)
+    kw = dict(temperature=torch.from_numpy(d["temperature"]).to(device),
+              top_k=torch.from_numpy(d["top_k"]).to(device),
+              top_p=torch.from_numpy(d["top_p"]).to(device), seed=seed, offset=off,
+              workspace=tv.make_workspace(B, R, V, device),
+              outputs=tv._chain_outputs(B, R, device, True, True))
+    ms = time_device(lambda: tv.chain_spec_sampling(logits, True, D, drafts, **kw), steps, warm,
+                     device)
+    rec("verify_step_with_logprobs_B512_D3_V201088_bf16", ms, rows, rows * V * 2, launches=2)
+    # the Gumbel-max vocabulary sweep: V in {32000, 128256, 201088} x B in {1, 32, 512}, N = 4
+    # (the 201088 logits are the step's; the others are generated by the same recipe)
+    for Vs in (32000, 128256, 201088):
+        if Vs == V:
+            gl, Trs, gseed, goff = logits, Trow, seed, off
+        else:
+            gsw = synth.gumbel(B=512, N=4, V=Vs, real_vocab=min(Vs, 200019), want_f32=False)
+            gl = torch.from_numpy(np.ascontiguousarray(gsw["logits_bits"]).view(np.int16)).to(
+                device).view(torch.bfloat16)
+            Trs = torch.from_numpy(gsw["temperature"]).to(device)
+            gseed = torch.from_numpy(gsw["seed"]).to(device)
+            goff = torch.from_numpy(gsw["offset"]).to(device)
+        for Bs in (1, 32, 512):
+            # the smaller batches take successive slices of the 2048-row buffer, call by
+            # call, so that consecutive calls do not read the same (L2-resident) rows
+            nr = Bs * 4
+            wss = tv.make_workspace(Bs, 4, Vs, device)
+            toks = torch.empty(nr, dtype=torch.int32, device=device)
+            nsl = 512 // Bs
+            sl = [(gl[i * nr:(i + 1) * nr], Trs[i * nr:(i + 1) * nr], gseed[i * Bs:(i + 1) * Bs],
+                   goff[i * Bs:(i + 1) * Bs]) for i in range(nsl)]
+            cur = [0]
+
+            def call():
+                xs, ts, ss, os_ = sl[cur[0] % nsl]
+                cur[0] += 1
+                tv.gumbel_max_sample(xs, 4, ts, ss, os_, wss, out=toks)
+
+            ms = time_device(call, max(steps, 20), warm, device)
+            rec(f"gumbel_sweep_B{Bs}_N4_V{Vs}_bf16", ms, nr, nr * Vs * 2)
+        del gl, sl
     # softmax with temperature, fp32 probabilities out
     out = torch.empty((rows, V), dtype=torch.float32, device=device)
     ms = time_device(lambda: tv.softmax_temp(logits, Trow, out=out), steps, warm, device)
