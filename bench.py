@@ -44,6 +44,12 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-legs", action="store_true")
+    ap.add_argument("--legs-only", action="store_true",
+                    help="time only the legs (no headline step, no CPU baseline): profiling")
+    ap.add_argument("--leg", default=None,
+                    help="run only the legs whose name contains this string")
+    ap.add_argument("--no-parity", action="store_true",
+                    help="skip the oracle checks of the legs' outputs (boundary counts)")
     ap.add_argument("--cpu-sample", type=int, default=48,
                     help="requests in the single-core CPU baseline sample "
                          "(0: no CPU baseline, for profiling runs)")
@@ -99,6 +105,16 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_entry(kernel: str, workload: str):
+    """The whole record of an ncu capture of this kernel and workload (or None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f).get(f"{kernel}|{workload}")
+    except Exception:
+        return None
 
 
 def ncu_traffic(kernel: str, workload: str):
@@ -177,11 +193,12 @@ class ClockSampler:
                 "power_w_max": max((num(r[2]) or 0.0) for r in rows)}
 
 
-def time_device(fn, steps: int, warmup: int, device, per_step: bool = False):
+def time_device(fn, steps: int, warmup: int, device, per_step: bool = False, flush=None):
     """Mean device time of one fn() call over `steps` timed calls (CUDA events on the
     launching stream, barrier + synchronize on both sides, max over ranks). With per_step,
     also the 10th, 50th and 90th percentiles of the per-call times (an event between
-    consecutive calls)."""
+    consecutive calls). With flush (a device buffer larger than L2), the buffer is written
+    before every call, outside the events, so each call starts with a cold L2."""
     import torch
 
     for _ in range(warmup):
@@ -189,6 +206,22 @@ def time_device(fn, steps: int, warmup: int, device, per_step: bool = False):
     torch.cuda.synchronize()
     barrier()
     s = torch.cuda.current_stream()
+    if flush is not None:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(s)
+            fn()
+            ev[i][1].record(s)
+        torch.cuda.synchronize()
+        barrier()
+        each = np.array([a.elapsed_time(b) for a, b in ev])
+        ms = max_over_ranks(float(each.mean()), device)
+        if not per_step:
+            return ms
+        return ms, {"p10": float(np.percentile(each, 10)), "p50": float(np.percentile(each, 50)),
+                    "p90": float(np.percentile(each, 90))}
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1 if per_step else 2)]
     ev[0].record(s)
     for i in range(steps):
@@ -367,6 +400,12 @@ def run_ours(args):
     def step():
         tv.chain_spec_sampling(logits, True, D, drafts, **kw)
 
+    if args.legs_only:
+        legs = run_legs(args, d, logits, device, tv, synth, peak)
+        if rank == 0:
+            print(json.dumps({"legs": legs}))
+        return
+
     alg_bytes = rows * V * 2  # the logits, read once
     with ClockSampler(local) as clk:
         ms, pct = time_device(step, args.steps, args.warmup, device, per_step=True)
@@ -437,8 +476,83 @@ def run_ours(args):
     print(json.dumps(line))
 
 
+_POOL = None
+
+
+def _oracle_pool():
+    """One spawned process per host core for the oracle checks of the legs."""
+    global _POOL
+    if _POOL is None:
+        import multiprocessing
+
+        _POOL = multiprocessing.get_context("spawn").Pool(max(1, os.cpu_count() or 1))
+    return _POOL
+
+
+def _oracle_task(task):
+    """One slice of rows or requests through the oracle (runs in a spawned process)."""
+    import oracle
+    from speculative_decoding_verify_temp_gb300 import synth
+
+    kind, x, is_bits, args, kw = task
+    x = synth.f32_from_bf16_bits(x) if is_bits else x
+    if kind == "gumbel":
+        return oracle.gumbel_max_sample(x, *args, **kw)
+    if kind == "greedy":
+        return oracle.verify_chain_greedy(x, *args, **kw)
+    return oracle.chain_spec_sampling(x, *args, **kw)
+
+
+def leg_parity(kind, x, is_bits, R, args_req, kw_req, gpu, extra=None):
+    """Check a leg's outputs (from its last timed call) against the oracle over every
+    request, in slices across the host cores: exact tokens and lengths on every request
+    whose decision margin exceeds 1e-6; the others are counted as boundary requests.
+    args_req / kw_req: per-request arrays (sliced) and scalars (kept) for the oracle."""
+    B = x.shape[0] // R
+    procs = max(1, os.cpu_count() or 1)
+    step = -(-B // procs)
+
+    def cut(v, b0, b1, per_row):
+        if isinstance(v, np.ndarray) and v.ndim >= 1 and v.shape[0] in (B, B * R):
+            lo, hi = (b0 * R, b1 * R) if (per_row or v.shape[0] == B * R) else (b0, b1)
+            return np.ascontiguousarray(v[lo:hi])
+        return v
+
+    tasks = []
+    for b0 in range(0, B, step):
+        b1 = min(B, b0 + step)
+        xa = np.ascontiguousarray(x[b0 * R:b1 * R])
+        a = [cut(v, b0, b1, False) for v in args_req]
+        k = {n: cut(v, b0, b1, False) for n, v in kw_req.items()}
+        if extra is not None:
+            # draft-side rows: [B, D, V] or [B * D, V]
+            k.update({n: np.ascontiguousarray(v[b0:b1] if v.shape[0] == B
+                                              else v[b0 * (R - 1):b1 * (R - 1)])
+                      for n, v in extra.items()})
+        tasks.append((kind, xa, is_bits, a, k))
+    parts = _oracle_pool().map(_oracle_task, tasks)
+    if kind == "gumbel":
+        want = np.concatenate([p[0] for p in parts])
+        marg = np.concatenate([p[1] for p in parts])
+        ok = marg > 1e-6
+        mism = int((gpu[0] != want)[ok].sum())
+        return {"rows": int(len(want)), "mismatches_outside_boundary": mism,
+                "boundary_rows": int((~ok).sum()), "boundary": "margin <= 1e-6"}
+    acc = np.concatenate([p["accepted_tokens"] for p in parts])
+    alen = np.concatenate([p["accept_length"] for p in parts])
+    if kind == "greedy":
+        mism = int(((gpu[0] != acc).any(axis=1) | (gpu[1] != alen)).sum())
+        return {"requests": int(B), "mismatches": mism}
+    ok = np.concatenate([p["margin"] for p in parts]) > 1e-6
+    mism = int((((gpu[0] != acc).any(axis=1)) | (gpu[1] != alen))[ok].sum())
+    return {"requests": int(B), "mismatches_outside_boundary": mism,
+            "boundary_requests": int((~ok).sum()), "boundary": "margin <= 1e-6"}
+
+
 def run_legs(args, d, logits, device, tv, synth, peak):
-    """The other calls, each on its own workload (mean device time per call)."""
+    """The other calls, each on its own workload (mean device time per call), with the
+    oracle's check of each leg's outputs (boundary counts per configuration) unless
+    --no-parity."""
     import torch
 
     legs = {}
@@ -446,40 +560,73 @@ def run_legs(args, d, logits, device, tv, synth, peak):
     B, D, V = d["B"], d["D"], d["V"]
     R = D + 1
     rows = B * R
+    parity = not args.no_parity
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # > the 129 MB L2
 
-    def rec(name, ms, nrows, nbytes, launches=1):
+    def want(name):
+        return args.leg is None or args.leg in name
+
+    def rec(name, ms, nrows, nbytes, launches=1, **more):
         legs[name] = {"ms": ms, "rows_per_s": nrows / (ms / 1e3),
                       "hbm_gbs": nbytes / (ms / 1e3) / 1e9,
                       "frac_of_peak": nbytes / (ms / 1e3) / 1e9 / peak, "launches": launches}
+        legs[name].update(more)
 
-    # greedy chain verification on the same logits (the greedy gate)
+    def host(t):
+        return t.cpu().numpy()
+
+    bits = d["logits_bits"]
     drafts = torch.from_numpy(d["draft_tokens"]).to(device)
-    ws = tv.make_workspace(B, R, V, device)
-    outs = tv._chain_outputs(B, R, device, False, False)
-    ms = time_device(lambda: tv.verify_chain_greedy(logits, D, drafts, ws, outputs=outs),
-                     steps, warm, device)
-    rec("greedy_verify_B512_D3_V201088_bf16", ms, rows, rows * V * 2)
-    # Gumbel-max on the same logits as 512 requests x 4 rows, greedy rows included
-    Trow = torch.from_numpy(np.repeat(d["temperature"], R)).to(device)
+    Trow_np = np.repeat(d["temperature"], R).astype(np.float32)
+    Trow = torch.from_numpy(Trow_np).to(device)
     seed = torch.from_numpy(d["seed"]).to(device)
     off = torch.from_numpy(d["offset"]).to(device)
-    wsg = tv.make_workspace(B, R, V, device)
-    tok = torch.empty(rows, dtype=torch.int32, device=device)
-    ms = time_device(lambda: tv.gumbel_max_sample(logits, R, Trow, seed, off, wsg, out=tok),
-                     steps, warm, device)
-    rec("gumbel_B512_N4_V201088_bf16", ms, rows, rows * V * 2)
+    # greedy chain verification on the same logits (the greedy gate)
+    name = "greedy_verify_B512_D3_V201088_bf16"
+    if want(name):
+        ws = tv.make_workspace(B, R, V, device)
+        outs = tv._chain_outputs(B, R, device, False, False)
+        ms = time_device(lambda: tv.verify_chain_greedy(logits, D, drafts, ws, outputs=outs),
+                         steps, warm, device)
+        rec(name, ms, rows, rows * V * 2)
+        if parity:
+            legs[name]["parity"] = leg_parity("greedy", bits, True, R, [D, d["draft_tokens"]], {},
+                                              (host(outs[0]), host(outs[1])))
+    # Gumbel-max on the same logits as 512 requests x 4 rows, greedy rows included
+    name = "gumbel_B512_N4_V201088_bf16"
+    if want(name):
+        wsg = tv.make_workspace(B, R, V, device)
+        tok = torch.empty(rows, dtype=torch.int32, device=device)
+        ms = time_device(lambda: tv.gumbel_max_sample(logits, R, Trow, seed, off, wsg, out=tok),
+                         steps, warm, device)
+        alu = ncu_entry("k_gumbel", "gumbel_B512")
+        rec(name, ms, rows, rows * V * 2, alu=alu)
+        if parity:
+            legs[name]["parity"] = leg_parity("gumbel", bits, True, R,
+                                              [R, Trow_np, d["seed"], d["offset"]], {},
+                                              (host(tok),))
     # the verify step with every output on (logprobs at temperature 1, accept_index)
-    kw = dict(temperature=torch.from_numpy(d["temperature"]).to(device),
-              top_k=torch.from_numpy(d["top_k"]).to(device),
-              top_p=torch.from_numpy(d["top_p"]).to(device), seed=seed, offset=off,
-              workspace=tv.make_workspace(B, R, V, device),
-              outputs=tv._chain_outputs(B, R, device, True, True))
-    ms = time_device(lambda: tv.chain_spec_sampling(logits, True, D, drafts, **kw), steps, warm,
-                     device)
-    rec("verify_step_with_logprobs_B512_D3_V201088_bf16", ms, rows, rows * V * 2, launches=2)
+    name = "verify_step_with_logprobs_B512_D3_V201088_bf16"
+    if want(name):
+        outs = tv._chain_outputs(B, R, device, True, True)
+        kw = dict(temperature=torch.from_numpy(d["temperature"]).to(device),
+                  top_k=torch.from_numpy(d["top_k"]).to(device),
+                  top_p=torch.from_numpy(d["top_p"]).to(device), seed=seed, offset=off,
+                  workspace=tv.make_workspace(B, R, V, device), outputs=outs)
+        ms = time_device(lambda: tv.chain_spec_sampling(logits, True, D, drafts, **kw), steps,
+                         warm, device)
+        rec(name, ms, rows, rows * V * 2, launches=2)
+        if parity:
+            legs[name]["parity"] = leg_parity(
+                "chain", bits, True, R, [True, D, d["draft_tokens"]],
+                {k: d[k] for k in ("temperature", "top_k", "top_p", "seed", "offset")} |
+                {"logprobs": False}, (host(outs[0]), host(outs[1])))
     # the Gumbel-max vocabulary sweep: V in {32000, 128256, 201088} x B in {1, 32, 512}, N = 4
     # (the 201088 logits are the step's; the others are generated by the same recipe)
     for Vs in (32000, 128256, 201088):
+        if not want(f"gumbel_sweep_B1_N4_V{Vs}") and not want(f"gumbel_sweep_B32_N4_V{Vs}") \
+                and not want(f"gumbel_sweep_B512_N4_V{Vs}"):
+            continue
         if Vs == V:
             gl, Trs, gseed, goff = logits, Trow, seed, off
         else:
@@ -490,8 +637,11 @@ def run_legs(args, d, logits, device, tv, synth, peak):
             gseed = torch.from_numpy(gsw["seed"]).to(device)
             goff = torch.from_numpy(gsw["offset"]).to(device)
         for Bs in (1, 32, 512):
+            name = f"gumbel_sweep_B{Bs}_N4_V{Vs}_bf16"
+            if not want(name):
+                continue
             # the smaller batches take successive slices of the 2048-row buffer, call by
-            # call, so that consecutive calls do not read the same (L2-resident) rows
+            # call, so that consecutive calls do not read the same rows
             nr = Bs * 4
             wss = tv.make_workspace(Bs, 4, Vs, device)
             toks = torch.empty(nr, dtype=torch.int32, device=device)
@@ -505,75 +655,116 @@ def run_legs(args, d, logits, device, tv, synth, peak):
                 cur[0] += 1
                 tv.gumbel_max_sample(xs, 4, ts, ss, os_, wss, out=toks)
 
-            ms = time_device(call, max(steps, 20), warm, device)
-            rec(f"gumbel_sweep_B{Bs}_N4_V{Vs}_bf16", ms, nr, nr * Vs * 2)
-        del gl, sl
+            ms = time_device(call, max(steps, 50), warm, device)
+            more = {}
+            if Bs < 512:
+                more["ms_l2_flushed"] = time_device(call, max(steps, 50), warm, device,
+                                                    flush=flush)
+            rec(name, ms, nr, nr * Vs * 2, **more)
+        del gl
     # softmax with temperature, fp32 probabilities out
-    out = torch.empty((rows, V), dtype=torch.float32, device=device)
-    ms = time_device(lambda: tv.softmax_temp(logits, Trow, out=out), steps, warm, device)
-    rec("softmax_B512_R4_V201088_bf16", ms, rows, rows * V * 6)
-    del out
-    # greedy verification, small batch (latency-bound)
-    g = synth.greedy_verify()
-    gl = torch.from_numpy(np.ascontiguousarray(g["logits_bits"]).view(np.int16)).to(device).view(
-        torch.bfloat16)
-    gd = torch.from_numpy(g["draft_tokens"]).to(device)
-    gws = tv.make_workspace(g["B"], g["D"] + 1, g["V"], device)
-    gouts = tv._chain_outputs(g["B"], g["D"] + 1, device, False, False)
-    ms = time_device(lambda: tv.verify_chain_greedy(gl, g["D"], gd, gws, outputs=gouts),
-                     max(50, steps), 10, device)
-    grows = g["B"] * (g["D"] + 1)
-    rec("greedy_verify_B64_D3_V32000_bf16", ms, grows, grows * g["V"] * 2)
+    name = "softmax_B512_R4_V201088_bf16"
+    if want(name):
+        out = torch.empty((rows, V), dtype=torch.float32, device=device)
+        ms = time_device(lambda: tv.softmax_temp(logits, Trow, out=out), steps, warm, device)
+        rec(name, ms, rows, rows * V * 6)
+        del out
+    # greedy verification, small batch (latency-bound; L2-resident unless flushed)
+    name = "greedy_verify_B64_D3_V32000_bf16"
+    if want(name):
+        g = synth.greedy_verify()
+        gl = torch.from_numpy(np.ascontiguousarray(g["logits_bits"]).view(np.int16)).to(
+            device).view(torch.bfloat16)
+        gd = torch.from_numpy(g["draft_tokens"]).to(device)
+        gws = tv.make_workspace(g["B"], g["D"] + 1, g["V"], device)
+        gouts = tv._chain_outputs(g["B"], g["D"] + 1, device, False, False)
+
+        def gcall():
+            tv.verify_chain_greedy(gl, g["D"], gd, gws, outputs=gouts)
+
+        ms = time_device(gcall, max(50, steps), 10, device)
+        msf = time_device(gcall, max(50, steps), 10, device, flush=flush)
+        grows = g["B"] * (g["D"] + 1)
+        rec(name, ms, grows, grows * g["V"] * 2, ms_l2_flushed=msf)
+        if parity:
+            legs[name]["parity"] = leg_parity("greedy", g["logits_bits"], True, g["D"] + 1,
+                                              [g["D"], g["draft_tokens"]], {},
+                                              (host(gouts[0]), host(gouts[1])))
     # target-only chain sampling, B=128 D=4 V=128256
-    c = synth.target_only()
-    cl = torch.from_numpy(np.ascontiguousarray(c["logits_bits"]).view(np.int16)).to(device).view(
-        torch.bfloat16)
-    ca = dict(temperature=torch.from_numpy(c["temperature"]).to(device),
-              top_k=torch.from_numpy(c["top_k"]).to(device),
-              top_p=torch.from_numpy(c["top_p"]).to(device),
-              seed=torch.from_numpy(c["seed"]).to(device),
-              offset=torch.from_numpy(c["offset"]).to(device),
-              workspace=tv.make_workspace(c["B"], c["D"] + 1, c["V"], device),
-              outputs=tv._chain_outputs(c["B"], c["D"] + 1, device, False, False))
-    cd = torch.from_numpy(c["draft_tokens"]).to(device)
-    ms = time_device(lambda: tv.chain_spec_sampling(cl, True, c["D"], cd, **ca), steps, warm, device)
-    crows = c["B"] * (c["D"] + 1)
-    rec("target_only_B128_D4_V128256_bf16", ms, crows, crows * c["V"] * 2)
-    del cl
-    # rejection sampling with draft probabilities, B=256 D=7 V=151936 (fp32 probs)
-    r = synth.rejection()
-    rp = torch.from_numpy(r["target_probs"]).to(device)
-    rq = torch.from_numpy(r["draft_probs"]).to(device)
-    ra = dict(draft_probs=rq, seed=torch.from_numpy(r["seed"]).to(device),
-              offset=torch.from_numpy(r["offset"]).to(device),
-              workspace=tv.make_workspace(r["B"], r["D"] + 1, r["V"], device),
-              outputs=tv._chain_outputs(r["B"], r["D"] + 1, device, False, True))
-    rd = torch.from_numpy(r["draft_tokens"]).to(device)
-    res = tv.chain_spec_sampling(rp, False, r["D"], rd, **ra)
-    alen = res["accept_length"].cpu().numpy()
-    rrows = r["B"] * (r["D"] + 1)
-    # algorithmic bytes: the row the draw needs (p, plus q for a rejection) and the
-    # accepted-prefix scalars
-    need = sum((2 if L <= r["D"] else 1) for L in alen) * r["V"] * 4
-    ms = time_device(lambda: tv.chain_spec_sampling(rp, False, r["D"], rd, **ra), steps, warm,
-                     device)
-    rec("rejection_B256_D7_V151936_f32", ms, rrows, need)
+    name = "target_only_B128_D4_V128256_bf16"
+    if want(name):
+        c = synth.target_only()
+        cl = torch.from_numpy(np.ascontiguousarray(c["logits_bits"]).view(np.int16)).to(
+            device).view(torch.bfloat16)
+        couts = tv._chain_outputs(c["B"], c["D"] + 1, device, False, False)
+        ca = dict(temperature=torch.from_numpy(c["temperature"]).to(device),
+                  top_k=torch.from_numpy(c["top_k"]).to(device),
+                  top_p=torch.from_numpy(c["top_p"]).to(device),
+                  seed=torch.from_numpy(c["seed"]).to(device),
+                  offset=torch.from_numpy(c["offset"]).to(device),
+                  workspace=tv.make_workspace(c["B"], c["D"] + 1, c["V"], device), outputs=couts)
+        cd = torch.from_numpy(c["draft_tokens"]).to(device)
+        ms = time_device(lambda: tv.chain_spec_sampling(cl, True, c["D"], cd, **ca), steps, warm,
+                         device)
+        crows = c["B"] * (c["D"] + 1)
+        rec(name, ms, crows, crows * c["V"] * 2, launches=2)
+        if parity:
+            legs[name]["parity"] = leg_parity(
+                "chain", c["logits_bits"], True, c["D"] + 1, [True, c["D"], c["draft_tokens"]],
+                {k: c[k] for k in ("temperature", "top_k", "top_p", "seed", "offset")} |
+                {"logprobs": False}, (host(couts[0]), host(couts[1])))
+        del cl
+    # rejection sampling with draft probabilities, B=256 D=7 V=151936 (fp32 probs), and the
     # top-k/top-p renorm of the same probabilities with the target-only knob mix
-    rng = np.random.default_rng(1)
-    kk = torch.from_numpy(rng.choice(np.array(synth.TOPK_CHOICES, np.int32), rrows)).to(device)
-    pp = torch.from_numpy(rng.choice(np.array(synth.TOPP_CHOICES, np.float32), rrows)).to(device)
-    ro = torch.empty_like(rp)
-    ms = time_device(lambda: tv.topk_topp_renorm(rp, kk, pp, out=ro), steps, warm, device)
-    rec("renorm_R2048_V151936_f32", ms, rrows, rrows * r["V"] * 8)
+    if want("rejection_B256_D7_V151936_f32") or want("renorm_R2048_V151936_f32"):
+        r = synth.rejection()
+        rp = torch.from_numpy(r["target_probs"]).to(device)
+        rrows = r["B"] * (r["D"] + 1)
+    name = "rejection_B256_D7_V151936_f32"
+    if want(name):
+        rq = torch.from_numpy(r["draft_probs"]).to(device)
+        routs = tv._chain_outputs(r["B"], r["D"] + 1, device, False, True)
+        ra = dict(draft_probs=rq, seed=torch.from_numpy(r["seed"]).to(device),
+                  offset=torch.from_numpy(r["offset"]).to(device),
+                  workspace=tv.make_workspace(r["B"], r["D"] + 1, r["V"], device), outputs=routs)
+        rd = torch.from_numpy(r["draft_tokens"]).to(device)
+        res = tv.chain_spec_sampling(rp, False, r["D"], rd, **ra)
+        alen = res["accept_length"].cpu().numpy()
+        # algorithmic bytes: the row the draw needs (p, plus q for a rejection) and the
+        # accepted-prefix scalars
+        need = sum((2 if L <= r["D"] else 1) for L in alen) * r["V"] * 4
+        ms = time_device(lambda: tv.chain_spec_sampling(rp, False, r["D"], rd, **ra), steps, warm,
+                         device)
+        rec(name, ms, rrows, need)
+        if parity:
+            legs[name]["parity"] = leg_parity(
+                "chain", r["target_probs"], False, r["D"] + 1, [False, r["D"], r["draft_tokens"]],
+                {"seed": r["seed"], "offset": r["offset"], "logprobs": False},
+                (host(routs[0]), host(routs[1])), extra={"draft_probs": r["draft_probs"]})
+        del rq
+    name = "renorm_R2048_V151936_f32"
+    if want(name):
+        rng = np.random.default_rng(1)
+        kk = torch.from_numpy(rng.choice(np.array(synth.TOPK_CHOICES, np.int32), rrows)).to(device)
+        pp = torch.from_numpy(rng.choice(np.array(synth.TOPP_CHOICES, np.float32), rrows)).to(
+            device)
+        ro = torch.empty_like(rp)
+        ms = time_device(lambda: tv.topk_topp_renorm(rp, kk, pp, out=ro), steps, warm, device)
+        rec(name, ms, rrows, rrows * r["V"] * 8)
     return legs
 
 
 def main():
     args = parse()
-    if args.impl == "reference":
-        run_reference(args)
-    else:
-        run_ours(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args)
+        else:
+            run_ours(args)
+    finally:
+        if _POOL is not None:
+            _POOL.close()
+            _POOL.join()
 
 
 if __name__ == "__main__":

@@ -15,7 +15,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtsverify.so")
-SOURCES = ["ts_abi.cu", "ts_stream.cu", "ts_sample.cu", "ts_staged.cu", "ts_chain.cu"]
+SOURCES = ["ts_abi.cu", "ts_stream.cu", "ts_sample.cu", "ts_staged.cu", "ts_chain.cu",
+           "ts_gumbel.cu"]
 HEADERS = ["ts_common.cuh", "ts_internal.h", "ts_select.cuh", "ts_rowutil.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]

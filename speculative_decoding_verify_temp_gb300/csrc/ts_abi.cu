@@ -4,6 +4,7 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include <cuda_runtime.h>
@@ -400,14 +401,44 @@ ts_status ts_gumbel_max_sample(const void* logits, ts_dtype dt, int64_t batch,
   if ((st = check_common(batch * (int64_t)n_per_req, vocab, ld)) != TS_OK) return st;
   if (!logits || !temperature || !seed || !offset || !tokens_out)
     return fail(TS_ERR_INVALID_ARG, "logits, temperature, seed, offset and tokens_out are required");
+  tsv::Workspace ws{};
+  if ((st = take_workspace(batch, n_per_req, vocab, workspace, ws_bytes, &ws)) != TS_OK) return st;
+  const int esize = dt == TS_BF16 ? 2 : 4;
+  if (aligned16(logits, ld, esize)) {
+    // a chunk is one warp's claim: 128 to 1024 vectors, about two a warp over the whole
+    // call, and no more than kMaxSplits a row
+    tsv::GumbelArgs g{};
+    const int64_t rows = batch * n_per_req;
+    const int64_t nv = vocab / (16 / esize);
+    const int64_t ctas = (int64_t)sm_count() * tsv::gumbel_ctas_per_sm(dt == TS_BF16);
+    int64_t cv = (rows * nv + 2 * 8 * ctas - 1) / (2 * 8 * ctas);
+    cv = std::min<int64_t>(std::max<int64_t>(cv, 128), 1024);
+    cv = std::max<int64_t>(cv, (nv + tsv::kMaxSplits - 1) / tsv::kMaxSplits);
+    const int64_t cpr = std::max<int64_t>(1, (nv + cv - 1) / cv);
+    g.x = logits;
+    g.ld = ld;
+    g.V = vocab;
+    g.rows = rows;
+    g.n_per_req = n_per_req;
+    g.temperature = temperature;
+    g.seed = seed;
+    g.offset = offset;
+    g.tokens_out = tokens_out;
+    g.chunk_vecs = cv;
+    g.cpr = (int32_t)cpr;
+    g.total_chunks = (uint32_t)(rows * cpr);
+    g.grid = (int32_t)std::min<int64_t>(ctas, (rows * cpr + 7) / 8);
+    g.ws = ws;
+    return launched(tsv::launch_gumbel(g, dt == TS_BF16, stream), "Gumbel launch");
+  }
   tsv::RowStatArgs a{};
-  if ((st = take_workspace(batch, n_per_req, vocab, workspace, ws_bytes, &a.ws)) != TS_OK) return st;
+  a.ws = ws;
   a.x = logits;
   a.ld = ld;
   a.V = vocab;
   a.rows = batch * n_per_req;
   choose_splits(a.rows, vocab, 2048, &a.splits, &a.split_len);
-  a.vec = aligned16(logits, ld, dt == TS_BF16 ? 2 : 4);
+  a.vec = 0;
   a.kind = 2;
   a.temperature = temperature;
   a.seed = seed;

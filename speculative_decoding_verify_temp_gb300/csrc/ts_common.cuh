@@ -61,17 +61,53 @@ __device__ __forceinline__ uint64_t fixw(float e) { return __float2ull_rz(e * kF
 // Philox4x32-10 (Salmon et al., SC'11): ten rounds of the two-multiplier round
 // function with a Weyl-bumped 2x32 key.
 
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// The ten round keys of one stream: the key bumped by the two Weyl constants each round.
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+};
+
+__device__ __forceinline__ PhiloxKeys philox_keys(uint32_t k0, uint32_t k1) {
+  PhiloxKeys k;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    k.k0[r] = k0;
+    k.k1[r] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return k;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys& k) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
     const uint32_t m0 = 0xD2511F53u, m1 = 0xCD9E8D57u;
     const uint32_t h0 = __umulhi(m0, c.x), l0 = m0 * c.x;
     const uint32_t h1 = __umulhi(m1, c.z), l1 = m1 * c.z;
-    c = make_uint4(h1 ^ c.y ^ k0, l1, h0 ^ c.w ^ k1, l0);
+    c = make_uint4(h1 ^ c.y ^ k.k0[r], l1, h0 ^ c.w ^ k.k1[r], l0);
+  }
+  return c;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+  return philox4x32_10(c, philox_keys(k0, k1));
+}
+
+// Two blocks of one stream computed side by side (the same rounds as above, written so
+// that the two dependency chains interleave).
+__device__ __forceinline__ void philox4x32_10_x2(uint4& a, uint4& b, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t m0 = 0xD2511F53u, m1 = 0xCD9E8D57u;
+    const uint64_t pa0 = (uint64_t)m0 * a.x, pa1 = (uint64_t)m1 * a.z;
+    const uint64_t pb0 = (uint64_t)m0 * b.x, pb1 = (uint64_t)m1 * b.z;
+    a = make_uint4((uint32_t)(pa1 >> 32) ^ a.y ^ k0, (uint32_t)pa1,
+                   (uint32_t)(pa0 >> 32) ^ a.w ^ k1, (uint32_t)pa0);
+    b = make_uint4((uint32_t)(pb1 >> 32) ^ b.y ^ k0, (uint32_t)pb1,
+                   (uint32_t)(pb0 >> 32) ^ b.w ^ k1, (uint32_t)pb0);
     k0 += 0x9E3779B9u;
     k1 += 0xBB67AE85u;
   }
-  return c;
 }
 
 // A 32-bit word to (2*(w >> 9) + 1) * 2^-24: exact in fp32, inside (0, 1).

@@ -111,6 +111,26 @@ struct RowStatArgs {
 
 cudaError_t launch_rowstat(const RowStatArgs& a, int bf16, cudaStream_t s);
 
+// ---- Gumbel-max over 16-byte aligned rows (ts_gumbel.cu) -----------------------------
+
+struct GumbelArgs {
+  const void* x;
+  int64_t ld, V, rows;
+  int32_t n_per_req;
+  const float* temperature;  // [rows]
+  const int64_t* seed;       // [rows / n_per_req]
+  const int64_t* offset;     // [rows / n_per_req]
+  int32_t* tokens_out;       // [rows]
+  int64_t chunk_vecs;        // 16-byte vectors a chunk (the last chunk of a row may be shorter)
+  int32_t cpr;               // chunks a row (<= kMaxSplits); the last also takes the ragged tail
+  uint32_t total_chunks;     // rows * cpr
+  int32_t grid;              // persistent CTAs
+  Workspace ws;              // rowcnt, part, best (left zero) and work[0] (claims)
+};
+
+cudaError_t launch_gumbel(const GumbelArgs& a, int bf16, cudaStream_t s);
+int gumbel_ctas_per_sm(int bf16);
+
 struct DrawArgs {
   const float* p;
   int64_t ld, V, B;

@@ -496,6 +496,54 @@ def test_gumbel(B, N, V, dtype):
     assert (got < V - 50).all() or V <= 100
 
 
+def _strided(t, ld):
+    """A copy of the 2-D tensor t in rows of ld elements (the first t.shape[1] hold t)."""
+    buf = torch.full((t.shape[0], ld), float("-inf"), dtype=t.dtype, device=t.device)
+    buf[:, :t.shape[1]] = t
+    return buf[:, :t.shape[1]]
+
+
+@pytest.mark.parametrize("B,N,V,dtype,ld", [(8, 4, 8195, "bf16", 8200), (5, 3, 50001, "f32", 50004),
+                                            (1, 4, 32000, "bf16", 32000),
+                                            (64, 4, 4099, "f32", 4100),
+                                            (3, 4, 200003, "bf16", 200008),
+                                            (2, 1, 5, "bf16", 8)])
+def test_gumbel_chunked(B, N, V, dtype, ld):
+    """The chunked kernel (16-byte aligned rows, ragged tails, few and many chunks a row)
+    against the oracle, and token for token equal to the per-split route that serves
+    unaligned rows: the two compute the same scores, so every row must agree, boundary
+    rows included. Rows with ties, an all -inf row and greedy rows are in the mix."""
+    rng = np.random.default_rng(B * 7 + V)
+    d = _rand_logits(rng, B * N, V, dtype)
+    x = d["logits"]
+    if V > 64:
+        x[0] = np.float32(1.5)  # every logit equal
+        x[1, V // 3:] = -np.inf
+    if B * N > 3:
+        x[3] = -np.inf
+    if dtype == "bf16":
+        d["logits_bits"] = synth.bf16_bits_from_f32(x)
+        d["logits"] = x = synth.f32_from_bf16_bits(d["logits_bits"])
+    T = np.repeat(rng.uniform(0.3, 1.5, B), N).astype(np.float32)
+    if B > 1:
+        T[N:2 * N] = 0.0
+    seed = synth.request_seeds(B)
+    off = (np.arange(B, dtype=np.int64) + (1 << 33)).astype(np.int64)
+    t = dev_logits(d)
+    aligned = _strided(t, ld)
+    unaligned = _strided(t, ld + 1)
+    args = (N, dev(T), dev(seed), dev(off))
+    got = tv.gumbel_max_sample(aligned, *args).cpu().numpy()
+    alt = tv.gumbel_max_sample(unaligned, *args).cpu().numpy()
+    np.testing.assert_array_equal(got, alt)
+    ref, marg = oracle.gumbel_max_sample(x, N, T, seed, off)
+    ok = marg > BOUNDARY
+    assert (~ok).sum() <= 1
+    np.testing.assert_array_equal(got[ok], ref[ok])
+    if B * N > 3:
+        assert got[3] == 0  # no finite logit: token 0
+
+
 # ---- argument validation through the ABI (no launch) --------------------------------------------
 
 def test_invalid_arguments_raise():
