@@ -69,6 +69,14 @@ def _load():
                                               P, i64, P, P, P, P, P, P, P, P, P]
         L.orc_gumbel_max_sample.argtypes = [P, i64, i32, i64, i64, P, P, P, P, P]
         L.orc_gather_logprobs.argtypes = [P, ctypes.c_int, i64, i64, i64, P, P]
+        L.orc_filter_row_ex.argtypes = [P, i64, ctypes.c_int, f32, i32, f32, f32, ctypes.c_int,
+                                        P, P]
+        L.orc_filter_row_ex.restype = ctypes.c_double
+        L.orc_chain_spec_sampling_ex.argtypes = [P, ctypes.c_int, i64, i32, i64, i64, P, P, P,
+                                                 P, f32, f32, P, i64, P, P, P, P, P, P, P, P,
+                                                 P]
+        L.orc_sample_from_logits.argtypes = [P, i64, i32, i64, i64, P, P, P, P, ctypes.c_int,
+                                             P, P, P, P, P, P, P]
         _lib = L
     return _lib
 
@@ -120,13 +128,19 @@ def argmax(x) -> int:
     return int(_load().orc_argmax(_ptr(x), x.shape[-1]))
 
 
-def filter_row(vals, is_logits: bool, T: float = 1.0, top_k: int = 0, top_p: float = 1.0):
-    """p'' of one row and the top-p margin."""
+def filter_row(vals, is_logits: bool, T: float = 1.0, top_k: int = 0, top_p: float = 1.0,
+               min_p: float = 0.0, joint: bool = False):
+    """p'' of one row and the decision margin (top-k first unless joint; min_p last)."""
     v = _f32(vals).reshape(-1)
     out = np.zeros(v.shape[0], dtype=np.float64)
     am = ctypes.c_int64(0)
-    m = _load().orc_filter_row(_ptr(v), v.shape[0], int(is_logits), T, int(top_k),
-                               float(top_p), _ptr(out), ctypes.byref(am))
+    if min_p == 0.0 and not joint:
+        m = _load().orc_filter_row(_ptr(v), v.shape[0], int(is_logits), T, int(top_k),
+                                   float(top_p), _ptr(out), ctypes.byref(am))
+    else:
+        m = _load().orc_filter_row_ex(_ptr(v), v.shape[0], int(is_logits), T, int(top_k),
+                                      float(top_p), float(min_p), int(joint), _ptr(out),
+                                      ctypes.byref(am))
     return out, m
 
 
@@ -167,8 +181,9 @@ def verify_chain_greedy(logits, D: int, draft_tokens, logprobs: bool = True) -> 
 
 def chain_spec_sampling(target, target_is_logits: bool, D: int, draft_tokens, *,
                         draft_probs=None, temperature=None, top_k=None, top_p=None,
-                        seed=None, offset=None, uniforms=None,
-                        logprobs: bool = True) -> dict:
+                        seed=None, offset=None, uniforms=None, logprobs: bool = True,
+                        min_p=None, threshold_single: float = 1.0,
+                        threshold_acc: float = 1.0) -> dict:
     x = _f32(target)
     rows, V = x.shape
     R = D + 1
@@ -185,13 +200,42 @@ def chain_spec_sampling(target, target_is_logits: bool, D: int, draft_tokens, *,
     lp = np.zeros((B, R), np.float64) if logprobs else None
     marg = np.zeros(B, np.float64)
     uni = None if uniforms is None else _f32(uniforms).reshape(B, R)
-    _load().orc_chain_spec_sampling(
-        _ptr(x), int(target_is_logits), B, D, V, V, _ptr(_f32(temperature)),
-        _ptr(_i32(top_k)), _ptr(_f32(top_p)), _ptr(q), V, _ptr(dt), _ptr(_i64(seed)),
-        _ptr(_i64(offset)), _ptr(uni), _ptr(acc), _ptr(alen), _ptr(aidx), _ptr(lp),
-        _ptr(marg))
+    if min_p is None and threshold_single == 1.0 and threshold_acc == 1.0:
+        _load().orc_chain_spec_sampling(
+            _ptr(x), int(target_is_logits), B, D, V, V, _ptr(_f32(temperature)),
+            _ptr(_i32(top_k)), _ptr(_f32(top_p)), _ptr(q), V, _ptr(dt), _ptr(_i64(seed)),
+            _ptr(_i64(offset)), _ptr(uni), _ptr(acc), _ptr(alen), _ptr(aidx), _ptr(lp),
+            _ptr(marg))
+    else:
+        _load().orc_chain_spec_sampling_ex(
+            _ptr(x), int(target_is_logits), B, D, V, V, _ptr(_f32(temperature)),
+            _ptr(_i32(top_k)), _ptr(_f32(top_p)), _ptr(_f32(min_p)), float(threshold_single),
+            float(threshold_acc), _ptr(q), V, _ptr(dt), _ptr(_i64(seed)), _ptr(_i64(offset)),
+            _ptr(uni), _ptr(acc), _ptr(alen), _ptr(aidx), _ptr(lp), _ptr(marg))
     return dict(accepted_tokens=acc, accept_length=alen, accept_index=aidx, logprobs=lp,
                 margin=marg)
+
+
+def sample_from_logits(logits, n_per_req: int = 1, *, temperature=None, top_k=None,
+                       top_p=None, min_p=None, joint: bool = False, seed=None, offset=None,
+                       uniforms=None, probs: bool = False) -> dict:
+    """Single-step sampling of every row (knobs per row; seed and offset per request of
+    n_per_req rows). Returns tokens, logprobs, margin and, with probs, the kept
+    distributions."""
+    x = _f32(logits)
+    rows, V = x.shape
+    B = rows // n_per_req
+    if uniforms is None and (seed is None or offset is None):
+        raise ValueError("either uniforms or seed and offset are required")
+    tok = np.zeros(rows, np.int32)
+    lp = np.zeros(rows, np.float64)
+    marg = np.zeros(rows, np.float64)
+    pr = np.zeros((rows, V), np.float64) if probs else None
+    _load().orc_sample_from_logits(
+        _ptr(x), B, n_per_req, V, V, _ptr(_f32(temperature)), _ptr(_i32(top_k)),
+        _ptr(_f32(top_p)), _ptr(_f32(min_p)), int(joint), _ptr(_i64(seed)), _ptr(_i64(offset)),
+        _ptr(_f32(uniforms)), _ptr(tok), _ptr(pr), _ptr(lp), _ptr(marg))
+    return dict(tokens=tok, logprobs=lp, margin=marg, probs=pr)
 
 
 def gumbel_max_sample(logits, n_per_req: int, temperature, seed, offset):

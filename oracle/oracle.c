@@ -61,6 +61,30 @@ static double dmin(double a, double b) { return a < b ? a : b; }
  */
 double orc_filter_row(const float* vals, int64_t V, int is_logits, float T,
                       int32_t top_k, float top_p, double* out, int64_t* argmax_out) {
+  return orc_filter_row_ex(vals, V, is_logits, T, top_k, top_p, 0.0f, 0, out, argmax_out);
+}
+
+/*
+ * orc_filter_row with the two variations of the single-step samplers:
+ *
+ *  joint (TokenSpeed sample(): top_k_top_p_sampling_from_probs with
+ *  filter_apply_order="joint"): top-k and top-p are both measured on the
+ *  unfiltered p. The top-p set is then the shortest prefix of the order whose mass
+ *  reaches top_p times the whole row's mass, and the kept set is its intersection
+ *  with the top-k prefix. With joint == 0 the nucleus is measured on the top-k
+ *  renormalised p' (step 3 above). The two differ only when both knobs are active.
+ *
+ *  min_p (TensorRT-LLM fused_sample_from_logits(..., min_ps, ...)): of the tokens
+ *  the two knobs keep, only those whose weight is at least min_p times the largest
+ *  weight stay (min_p is clamped to [0, 1], so the argmax always stays). The test is
+ *  a ratio of weights, so it reads the same before or after any renormalisation.
+ *
+ * The margin adds, for min_p, the log-ratio distance of the last kept and the first
+ * dropped token from ln(min_p), over max(1, |ln min_p|).
+ */
+double orc_filter_row_ex(const float* vals, int64_t V, int is_logits, float T,
+                         int32_t top_k, float top_p, float min_p, int joint, double* out,
+                         int64_t* argmax_out) {
   int64_t am = orc_argmax(vals, V);
   if (argmax_out) *argmax_out = am;
   for (int64_t i = 0; i < V; ++i) out[i] = 0.0;
@@ -84,11 +108,17 @@ double orc_filter_row(const float* vals, int64_t V, int is_logits, float T,
   int64_t nk = (top_k > 0 && (int64_t)top_k < V) ? (int64_t)top_k : V;
   double Zk = 0.0;
   for (int64_t r = 0; r < nk; ++r) Zk += w[it[r].i];
+  /* the mass top_p is a fraction of: the top-k mass, or the whole row's (joint) */
+  double Zref = Zk;
+  if (joint) {
+    Zref = 0.0;
+    for (int64_t r = 0; r < V; ++r) Zref += w[it[r].i];
+  }
 
   double margin = INFINITY;
   int64_t nkeep = nk;
   if (top_p < 1.0f) {
-    double P = (double)top_p * Zk;
+    double P = (double)top_p * Zref;
     double S = 0.0;
     int64_t r = 0;
     for (; r < nk; ++r) {
@@ -101,8 +131,20 @@ double orc_filter_row(const float* vals, int64_t V, int is_logits, float T,
     nkeep = r;
     int64_t rl = nkeep - 1;
     double S_before = S - w[it[rl].i];
-    if (rl > 0) margin = dmin(margin, fabs(P - S_before) / Zk);
-    if (nkeep < nk) margin = dmin(margin, fabs(S - P) / Zk);
+    if (rl > 0) margin = dmin(margin, fabs(P - S_before) / Zref);
+    if (nkeep < nk) margin = dmin(margin, fabs(S - P) / Zref);
+  }
+  if (min_p > 0.0f) {
+    double mp = min_p < 1.0f ? (double)min_p : 1.0;
+    double w0 = w[it[0].i];
+    double thr = mp * w0;
+    int64_t r = 1;
+    while (r < nkeep && w[it[r].i] >= thr) ++r;
+    double lmp = log(mp), scale = fabs(lmp) > 1.0 ? fabs(lmp) : 1.0;
+    if (r > 1) margin = dmin(margin, fabs(log(w[it[r - 1].i] / w0) - lmp) / scale);
+    if (r < nkeep && w[it[r].i] > 0.0)
+      margin = dmin(margin, fabs(log(w[it[r].i] / w0) - lmp) / scale);
+    nkeep = r;
   }
   double Z = 0.0;
   for (int64_t r = 0; r < nkeep; ++r) Z += w[it[r].i];
@@ -200,7 +242,36 @@ void orc_chain_spec_sampling(const float* target, int target_is_logits, int64_t 
                              const float* uniforms, int32_t* accepted_tokens,
                              int32_t* accept_length, int32_t* accept_index,
                              double* logprobs, double* margin_out) {
+  orc_chain_spec_sampling_ex(target, target_is_logits, B, D, V, ld, temperature, top_k, top_p,
+                             NULL, 1.0f, 1.0f, draft_probs, ld_draft, draft_tokens, seed, offset,
+                             uniforms, accepted_tokens, accept_length, accept_index, logprobs,
+                             margin_out);
+}
+
+/*
+ * orc_chain_spec_sampling with min_p filtering of the target rows (logits only; see
+ * orc_filter_row_ex) and relaxed acceptance (TokenSpeed verify() passes threshold_single
+ * and threshold_acc to chain_speculative_sampling_target_only; the pages give no
+ * formula, and this is the reading taken): in target-only mode draft x is accepted iff
+ *     p(x) >= threshold_single   or   u * threshold_acc < p(x),
+ * so thresholds of 1 give plain rejection sampling (u < p(x)) and smaller ones accept
+ * more. A threshold outside (0, 1) means 1. With draft probabilities both must be 1.
+ * The margin adds |u * threshold_acc - p(x)| and |p(x) - threshold_single| for each
+ * relaxed test.
+ */
+void orc_chain_spec_sampling_ex(const float* target, int target_is_logits, int64_t B,
+                                int32_t D, int64_t V, int64_t ld, const float* temperature,
+                                const int32_t* top_k, const float* top_p, const float* min_p,
+                                float threshold_single, float threshold_acc,
+                                const float* draft_probs, int64_t ld_draft,
+                                const int32_t* draft_tokens, const int64_t* seed,
+                                const int64_t* offset, const float* uniforms,
+                                int32_t* accepted_tokens, int32_t* accept_length,
+                                int32_t* accept_index, double* logprobs, double* margin_out) {
   const int64_t R = (int64_t)D + 1;
+  const float ts = (threshold_single > 0.0f && threshold_single < 1.0f) ? threshold_single : 1.0f;
+  const float ta = (threshold_acc > 0.0f && threshold_acc < 1.0f) ? threshold_acc : 1.0f;
+  const int relaxed = (ts < 1.0f || ta < 1.0f) && !draft_probs;
   double* dist = (double*)malloc(sizeof(double) * (size_t)V);
   double* w = (double*)malloc(sizeof(double) * (size_t)V);
   float* u = (float*)malloc(sizeof(float) * (size_t)R);
@@ -208,6 +279,7 @@ void orc_chain_spec_sampling(const float* target, int target_is_logits, int64_t 
     float T = temperature ? temperature[b] : 1.0f;
     int32_t k = top_k ? top_k[b] : 0;
     float p = top_p ? top_p[b] : 1.0f;
+    float mp = min_p ? min_p[b] : 0.0f;
     int greedy_row = target_is_logits && is_greedy(T); /* p is one-hot at the argmax */
     for (int64_t j = 0; j < R; ++j)
       u[j] = uniforms ? uniforms[b * R + j]
@@ -220,7 +292,7 @@ void orc_chain_spec_sampling(const float* target, int target_is_logits, int64_t 
       int valid = (x >= 0 && (int64_t)x < V);
       int acc;
       if (target_is_logits) {
-        margin = dmin(margin, orc_filter_row(row, V, 1, T, k, p, dist, NULL));
+        margin = dmin(margin, orc_filter_row_ex(row, V, 1, T, k, p, mp, 0, dist, NULL));
         double px = valid ? dist[x] : 0.0;
         int exact = greedy_row || px == 0.0; /* one-hot rows and unkept tokens */
         if (draft_probs) {
@@ -228,6 +300,10 @@ void orc_chain_spec_sampling(const float* target, int target_is_logits, int64_t 
           double lhs = (double)u[j] * qx;
           acc = lhs < px;
           if (!exact) margin = dmin(margin, fabs(lhs - px));
+        } else if (relaxed) {
+          double lhs = (double)u[j] * (double)ta;
+          acc = px >= (double)ts || lhs < px;
+          if (!exact) margin = dmin(margin, dmin(fabs(lhs - px), fabs(px - (double)ts)));
         } else {
           acc = (double)u[j] < px;
           if (!exact) margin = dmin(margin, fabs((double)u[j] - px));
@@ -238,6 +314,9 @@ void orc_chain_spec_sampling(const float* target, int target_is_logits, int64_t 
           float qxf = valid ? draft_probs[(b * D + j) * ld_draft + x] : 0.0f;
           volatile float prod = u[j] * qxf; /* one fp32 multiply, rounded to nearest */
           acc = prod < pxf;
+        } else if (relaxed) {
+          volatile float lhs = u[j] * ta; /* one fp32 multiply, rounded to nearest */
+          acc = pxf >= ts || lhs < pxf;
         } else {
           acc = u[j] < pxf;
         }
@@ -251,7 +330,7 @@ void orc_chain_spec_sampling(const float* target, int target_is_logits, int64_t 
     /* The final draw from row js. */
     const float* row = target + (b * R + js) * ld;
     if (target_is_logits) {
-      double m = orc_filter_row(row, V, 1, T, k, p, dist, NULL);
+      double m = orc_filter_row_ex(row, V, 1, T, k, p, mp, 0, dist, NULL);
       if (js == D) margin = dmin(margin, m); /* rows < D were counted above */
     } else {
       for (int64_t i = 0; i < V; ++i) dist[i] = (double)row[i];
@@ -328,6 +407,74 @@ void orc_chain_spec_sampling(const float* target, int target_is_logits, int64_t 
   free(dist);
   free(w);
   free(u);
+}
+
+/*
+ * Single-step sampling from logits (TokenSpeed sample(): softmax with temperature,
+ * then top_k_top_p_sampling_from_probs(..., filter_apply_order="joint", seed, offset);
+ * TensorRT-LLM advanced_sample_draft / advanced_sample_draft_block:
+ * fused_sample_from_logits_with_probs(logits, temperatures, top_ks, top_ps, min_ps, seed,
+ * offset), whose probabilities are stored for the next verify step).
+ *
+ * Row r = b * n_per_req + j (knobs per row, seed and offset per request b) is filtered
+ * by orc_filter_row_ex (joint or top-k-first order, min_p) and one token is drawn from
+ * the kept distribution by the inverse CDF in token-id order: the smallest token whose
+ * inclusive prefix mass exceeds u times the total, with the coin u of position j of the
+ * request's verify stream (or uniforms[r]). A greedy row takes its argmax. probs_out
+ * receives the kept distribution (0 outside it), logprobs_out the temperature-1
+ * log-softmax of the chosen token, margin_out the smallest decision margin (filter cuts
+ * and the draw).
+ */
+void orc_sample_from_logits(const float* logits, int64_t B, int32_t n_per_req, int64_t V,
+                            int64_t ld, const float* temperature, const int32_t* top_k,
+                            const float* top_p, const float* min_p, int joint,
+                            const int64_t* seed, const int64_t* offset, const float* uniforms,
+                            int32_t* tokens_out, double* probs_out, double* logprobs_out,
+                            double* margin_out) {
+  const int64_t rows = B * (int64_t)n_per_req;
+  double* dist = (double*)malloc(sizeof(double) * (size_t)V);
+  for (int64_t r = 0; r < rows; ++r) {
+    const float* x = logits + r * ld;
+    int64_t b = r / n_per_req;
+    uint32_t j = (uint32_t)(r % n_per_req);
+    float T = temperature ? temperature[r] : 1.0f;
+    int32_t k = top_k ? top_k[r] : 0;
+    float p = top_p ? top_p[r] : 1.0f;
+    float mp = min_p ? min_p[r] : 0.0f;
+    int64_t am = 0;
+    double margin = orc_filter_row_ex(x, V, 1, T, k, p, mp, joint, dist, &am);
+    float u = uniforms ? uniforms[r] : orc_verify_coin((uint64_t)seed[b], (uint64_t)offset[b], j);
+    int64_t nnz = 0;
+    double Z = 0.0;
+    for (int64_t i = 0; i < V; ++i) {
+      nnz += (dist[i] > 0.0);
+      Z += dist[i];
+    }
+    double t = (double)u * Z;
+    int64_t tok = -1, last_pos = -1;
+    double S = 0.0;
+    for (int64_t i = 0; i < V; ++i) {
+      if (dist[i] > 0.0) {
+        last_pos = i;
+        if (S + dist[i] > t) {
+          tok = i;
+          if (nnz > 1) margin = dmin(margin, dmin(t - S, S + dist[i] - t) / Z);
+          break;
+        }
+        S += dist[i];
+      }
+    }
+    if (tok < 0) {
+      tok = (last_pos >= 0) ? last_pos : am;
+      margin = 0.0;
+    }
+    tokens_out[r] = (int32_t)tok;
+    if (probs_out)
+      for (int64_t i = 0; i < V; ++i) probs_out[r * V + i] = dist[i];
+    if (logprobs_out) logprobs_out[r] = logprob_from_logits(x, V, tok);
+    if (margin_out) margin_out[r] = margin;
+  }
+  free(dist);
 }
 
 /* Temperature-only draw by Gumbel-max (_sample_sharded_temperature: argmax of

@@ -52,6 +52,9 @@ float orc_gumbel_u01(uint64_t seed, uint64_t offset, uint32_t n, uint32_t v);
 int64_t orc_argmax(const float* x, int64_t V);
 double orc_filter_row(const float* vals, int64_t V, int is_logits, float T,
                       int32_t top_k, float top_p, double* out, int64_t* argmax_out);
+double orc_filter_row_ex(const float* vals, int64_t V, int is_logits, float T,
+                         int32_t top_k, float top_p, float min_p, int joint, double* out,
+                         int64_t* argmax_out);
 
 /* ---- The six operations -------------------------------------------------- */
 void orc_softmax_temp(const float* logits, int64_t rows, int64_t V, int64_t ld,
@@ -78,6 +81,23 @@ void orc_gumbel_max_sample(const float* logits, int64_t B, int32_t n_per_req,
                            int32_t* tokens_out, double* margin_out);
 void orc_gather_logprobs(const float* x, int is_probs, int64_t rows, int64_t V,
                          int64_t ld, const int32_t* tokens, double* out);
+
+/* ---- The next rows: single-step sampling, min_p, relaxed acceptance ------ */
+void orc_chain_spec_sampling_ex(const float* target, int target_is_logits, int64_t B,
+                                int32_t D, int64_t V, int64_t ld, const float* temperature,
+                                const int32_t* top_k, const float* top_p, const float* min_p,
+                                float threshold_single, float threshold_acc,
+                                const float* draft_probs, int64_t ld_draft,
+                                const int32_t* draft_tokens, const int64_t* seed,
+                                const int64_t* offset, const float* uniforms,
+                                int32_t* accepted_tokens, int32_t* accept_length,
+                                int32_t* accept_index, double* logprobs, double* margin_out);
+void orc_sample_from_logits(const float* logits, int64_t B, int32_t n_per_req, int64_t V,
+                            int64_t ld, const float* temperature, const int32_t* top_k,
+                            const float* top_p, const float* min_p, int joint,
+                            const int64_t* seed, const int64_t* offset, const float* uniforms,
+                            int32_t* tokens_out, double* probs_out, double* logprobs_out,
+                            double* margin_out);
 
 #ifdef __cplusplus
 }
