@@ -164,6 +164,15 @@ typedef struct ts_chain_args {
   float* logprobs;           /* [batch, D+1] out, or NULL: logits: log-softmax at T = 1 of
                                 the raw row; probabilities: ln p(token); 0 after the last
                                 emitted token */
+  /* Added knobs; a zero-initialised struct keeps the plain method. Both need logit
+   * targets with 16-byte aligned rows and vocab <= 2^18 (else TS_ERR_INVALID_ARG). */
+  const float* min_p;        /* [batch] or NULL: of the tokens top-k and top-p keep, only
+                                those with p_i >= min_p * max_i p_i stay (min_p clamped to
+                                [0, 1]; TRT-IF fused_sample_from_logits min_ps) */
+  float threshold_single;    /* relaxed acceptance (TS-FI verify() threshold_single and */
+  float threshold_acc;       /* threshold_acc), target-only: accept iff p(x) >= t_single
+                                or u * t_acc < p(x). Values outside (0, 1) mean 1 (plain
+                                rejection sampling); not allowed with draft_probs. */
 } ts_chain_args;
 
 /* Chain speculative sampling [TRT-IF rejection_sampling_one_model; TS-FI verify():
@@ -187,6 +196,49 @@ typedef struct ts_chain_args {
  * Outputs as ts_verify_chain_greedy. */
 ts_status ts_chain_spec_sampling(const ts_chain_args* args, void* workspace,
                                  size_t ws_bytes, cudaStream_t stream);
+
+/* Arguments of ts_sample_from_logits. rows = batch * n_per_req; row r belongs to request
+ * r / n_per_req as its row j = r % n_per_req. */
+#define TS_FILTER_TOP_K_FIRST 0 /* top-p measured on the top-k renormalised distribution */
+#define TS_FILTER_JOINT 1       /* top-k and top-p both measured on the unfiltered one */
+typedef struct ts_sample_args {
+  const void* logits;        /* [rows, ld], dtype */
+  int32_t dtype;             /* ts_dtype */
+  int32_t n_per_req;         /* rows of a request (>= 1) */
+  int64_t batch;
+  int64_t vocab;
+  int64_t ld;
+  const float* temperature;  /* [rows] or NULL (1); below TS_GREEDY_T: the argmax */
+  const int32_t* top_k;      /* [rows] or NULL */
+  const float* top_p;        /* [rows] or NULL */
+  const float* min_p;        /* [rows] or NULL (see ts_chain_args.min_p) */
+  int32_t filter_order;      /* TS_FILTER_TOP_K_FIRST or TS_FILTER_JOINT */
+  int32_t reserved0;
+  const int64_t* seed;       /* [batch] Philox key */
+  const int64_t* offset;     /* [batch] Philox counter base */
+  const float* uniforms;     /* [rows] explicit coins in (0, 1) replacing Philox, or NULL */
+  int32_t* tokens;           /* [rows] out */
+  float* logprobs;           /* [rows] out, or NULL: log-softmax at T = 1 of the raw row */
+  float* probs;              /* out, or NULL: row r's kept distribution (0 outside it, fp32)
+                                at probs + dst * ld_probs, dst = probs_row ? probs_row[r] : r */
+  int64_t ld_probs;          /* >= vocab */
+  const int64_t* probs_row;  /* [rows] destination rows, or NULL */
+} ts_sample_args;
+
+/* Single-step sampling from logits [TS-FI sample(): softmax(logits, temperature), then
+ * top_k_top_p_sampling_from_probs(..., filter_apply_order="joint", seed, offset);
+ * TRT-IF advanced_sample_draft / advanced_sample_draft_block:
+ * fused_sample_from_logits_with_probs(logits, temperatures, top_ks, top_ps, min_ps, seed,
+ * offset), the probabilities stored for the next verify step]. Each row's distribution
+ * is filtered as ts_chain_spec_sampling's p (in filter_order; min_p last) and one token
+ * is drawn by the inverse CDF in token-id order with coin u: uniforms[r], else the coin
+ * of position j of request b's stream as in ts_chain_spec_sampling (Philox keyed by
+ * seed[b], counter (j, 0xFFFFFFFF, lo32(offset[b]), hi32(offset[b]))). Draft-side calls
+ * and the verify call that checks their drafts must therefore use different offsets.
+ * Rows must be 16-byte aligned and vocab <= 2^18 (else TS_ERR_INVALID_ARG). Workspace:
+ * ts_workspace_size(batch * n_per_req, 1, vocab). */
+ts_status ts_sample_from_logits(const ts_sample_args* args, void* workspace, size_t ws_bytes,
+                                cudaStream_t stream);
 
 /* Temperature-only sampling by Gumbel-max [TRT-IF _sample_sharded_temperature: the
  * argmax of x/T plus Gumbel noise is an exact sample of softmax(x/T); rows below the

@@ -58,6 +58,10 @@ void choose_splits(int64_t units, int64_t V, int64_t min_len, int32_t* splits, i
   *splits = (int32_t)((V + l - 1) / l);
 }
 
+// A threshold in (0, 1) relaxes the accept test; any other value (0 from a
+// zero-initialised struct, 1, NaN) means 1.
+float unit_threshold(float t) { return (t > 0.f && t < 1.f) ? t : 1.f; }
+
 ts_status check_common(int64_t rows, int64_t V, int64_t ld) {
   if (rows < 1) return fail(TS_ERR_INVALID_ARG, "rows/batch must be >= 1 (got %lld)", (long long)rows);
   if (V < 1 || V > TS_MAX_VOCAB)
@@ -112,6 +116,7 @@ size_t workspace_layout(int64_t batch, int32_t R, int64_t vocab, void* base, Wor
   w.work = reinterpret_cast<uint32_t*>(take(4 * 4));
   w.order = reinterpret_cast<uint32_t*>(take(rows * 4));
   w.creq = reinterpret_cast<uint32_t*>(take((size_t)batch * 4));
+  w.slen = reinterpret_cast<int32_t*>(take(rows * 4));
   if (vocab > 0) {
     // sized for fp32 rows, which have the most chunks (at most kMaxSplits)
     int64_t chunk = 0;
@@ -280,6 +285,13 @@ ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t
   if (p->draft_probs && p->ld_draft < p->vocab)
     return fail(TS_ERR_INVALID_ARG, "ld_draft must be >= vocab");
   const int32_t R = p->D + 1;
+  const float thr_s = unit_threshold(p->threshold_single), thr_a = unit_threshold(p->threshold_acc);
+  const bool relaxed = thr_s < 1.f || thr_a < 1.f;
+  if (relaxed && p->draft_probs)
+    return fail(TS_ERR_INVALID_ARG, "relaxed acceptance thresholds are target-only");
+  const bool next_knobs = relaxed || p->min_p != nullptr;
+  if (next_knobs && !p->target_is_logits)
+    return fail(TS_ERR_INVALID_ARG, "min_p and relaxed thresholds need logit targets");
   if (!p->target_is_logits) {
     if (p->target_dtype != TS_F32)
       return fail(TS_ERR_UNSUPPORTED_DTYPE, "probability targets must be fp32");
@@ -355,8 +367,15 @@ ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t
     sa.wait_cycles = g_wait_cycles.load(std::memory_order_relaxed);
     sa.q = p->draft_probs;
     sa.ld_q = p->ld_draft;
+    sa.min_p = p->min_p;
+    sa.thr_single = thr_s;
+    sa.thr_acc = thr_a;
     return launched(tsv::launch_chain(sa, stream), "row-streaming chain launch");
   }
+  if (next_knobs)
+    return fail(TS_ERR_INVALID_ARG,
+                "min_p and relaxed thresholds need 16-byte aligned rows and vocab <= %lld",
+                (long long)tsv::kRowMaxVocab);
   if (p->draft_probs)
     return fail(TS_ERR_INVALID_ARG,
                 "logit targets with draft probabilities need 16-byte aligned rows and vocab "
@@ -388,6 +407,59 @@ ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t
   }
   const char* why = "target-only chain launch";
   return launched(tsv::launch_staged(a, stream, &why), why);
+}
+
+ts_status ts_sample_from_logits(const ts_sample_args* p, void* workspace, size_t ws_bytes,
+                                cudaStream_t stream) {
+  if (!p) return fail(TS_ERR_INVALID_ARG, "args is NULL");
+  ts_status st;
+  if ((st = check_dtype(p->dtype)) != TS_OK) return st;
+  if (p->n_per_req < 1) return fail(TS_ERR_INVALID_ARG, "n_per_req must be >= 1");
+  if (p->batch < 1) return fail(TS_ERR_INVALID_ARG, "batch must be >= 1");
+  const int64_t rows = p->batch * (int64_t)p->n_per_req;
+  if ((st = check_common(rows, p->vocab, p->ld)) != TS_OK) return st;
+  if (!p->logits || !p->tokens) return fail(TS_ERR_INVALID_ARG, "logits and tokens are required");
+  if (!p->uniforms && (!p->seed || !p->offset))
+    return fail(TS_ERR_INVALID_ARG, "seed and offset are required when uniforms is NULL");
+  if (p->filter_order != TS_FILTER_TOP_K_FIRST && p->filter_order != TS_FILTER_JOINT)
+    return fail(TS_ERR_INVALID_ARG, "filter_order must be TS_FILTER_TOP_K_FIRST or TS_FILTER_JOINT");
+  if (p->probs && p->ld_probs < p->vocab) return fail(TS_ERR_INVALID_ARG, "ld_probs must be >= vocab");
+  const int esize = p->dtype == TS_BF16 ? 2 : 4;
+  tsv::SampleArgs sa{};
+  if (!aligned16(p->logits, p->ld, esize) || p->vocab > tsv::kRowMaxVocab ||
+      !tsv::sample_splits(p->vocab, esize, &sa.splits, &sa.chunk))
+    return fail(TS_ERR_INVALID_ARG, "sampling needs 16-byte aligned rows and vocab <= %lld",
+                (long long)tsv::kRowMaxVocab);
+  if ((st = take_workspace(rows, 1, p->vocab, workspace, ws_bytes, &sa.ws)) != TS_OK) return st;
+  if (sa.splits > sa.ws.cand_splits)
+    return fail(TS_ERR_INVALID_ARG, "vocab %lld needs more row chunks than the workspace holds",
+                (long long)p->vocab);
+  sa.x = p->logits;
+  sa.bf16 = p->dtype == TS_BF16;
+  sa.ld = p->ld;
+  sa.V = p->vocab;
+  sa.rows = rows;
+  sa.R = 1;
+  sa.D = 0;
+  sa.temperature = p->temperature;
+  sa.top_k = p->top_k;
+  sa.top_p = p->top_p;
+  sa.min_p = p->min_p;
+  sa.joint = p->filter_order == TS_FILTER_JOINT;
+  sa.thr_single = 1.f;
+  sa.thr_acc = 1.f;
+  sa.sample_n = p->n_per_req;
+  sa.seed = p->seed;
+  sa.offset = p->offset;
+  sa.uniforms = p->uniforms;
+  sa.accepted_tokens = p->tokens;
+  sa.accept_length = sa.ws.slen;
+  sa.logprobs = p->logprobs;
+  sa.probs_out = p->probs;
+  sa.ld_probs = p->ld_probs;
+  sa.probs_row = p->probs_row;
+  sa.wait_cycles = g_wait_cycles.load(std::memory_order_relaxed);
+  return launched(tsv::launch_chain(sa, stream), "sampling launch");
 }
 
 ts_status ts_gumbel_max_sample(const void* logits, ts_dtype dt, int64_t batch,

@@ -87,24 +87,40 @@ static __device__ unsigned int g_chain_err;
 namespace {
 
 struct CKnobs {
-  float T, tp;
+  float T, tp, mp;
   int32_t k;
   int kind;
 };
 
 // The request's knobs and the way its rows are served. top_p <= 0 keeps only the argmax,
-// which is the greedy distribution.
+// which is the greedy distribution. min_p (clamped to [0, 1]), the joint order with both
+// top-k and top-p on, and a probability output are served by the general path.
 __device__ __forceinline__ CKnobs cknobs(const SampleArgs& a, int64_t req) {
   CKnobs kn;
   kn.T = a.temperature ? a.temperature[req] : 1.f;
   kn.k = a.top_k ? a.top_k[req] : 0;
   kn.tp = a.top_p ? a.top_p[req] : 1.f;
+  kn.mp = a.min_p ? fminf(fmaxf(a.min_p[req], 0.f), 1.f) : 0.f;
   const bool tk = kn.k > 0 && (int64_t)kn.k < a.V;
   if (!(kn.T >= kGreedyT)) kn.kind = kCGreedy;
   else if (tk) kn.kind = (kn.k <= kSTopK) ? kCTopK : kCGeneral;
   else if (kn.tp < 1.f) kn.kind = (kn.tp > 0.f) ? kCTopP : kCGreedy;
   else kn.kind = kCPlain;
+  if (kn.kind != kCGreedy &&
+      (kn.mp > 0.f || a.probs_out != nullptr || (a.joint && tk && kn.tp < 1.f)))
+    kn.kind = kCGeneral;
   return kn;
+}
+
+// The seed, offset and coin position of a row's draw coin: a chain's request and its
+// position D, or, when sampling, the row's request and its position within it.
+struct CCoin {
+  int64_t sreq;
+  uint32_t pos;
+};
+__device__ __forceinline__ CCoin ccoin(const SampleArgs& a, int64_t req) {
+  if (a.sample_n > 0) return CCoin{req / a.sample_n, (uint32_t)(req % a.sample_n)};
+  return CCoin{req, (uint32_t)a.D};
 }
 
 __device__ __forceinline__ int ctier(const CKnobs& kn) {
@@ -839,14 +855,14 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
           sm.M = v;
           sm.am = (i == INT32_MAX) ? 0 : i;
           sm.S1 = s;
-          const uint64_t seed = a.seed ? (uint64_t)a.seed[req] : 0;
-          const uint64_t off = a.offset ? (uint64_t)a.offset[req] : 0;
+          const CCoin cc = ccoin(a, req);
+          const uint64_t seed = a.seed ? (uint64_t)a.seed[cc.sreq] : 0;
+          const uint64_t off = a.offset ? (uint64_t)a.offset[cc.sreq] : 0;
           const bool coins = kn.kind != kCGreedy;
           sm.uj = (coins && j < D) ? (a.uniforms ? a.uniforms[req * a.R + j]
                                                  : verify_coin(seed, off, (uint32_t)j))
                                    : 0.f;
-          sm.uD = coins ? (a.uniforms ? a.uniforms[req * a.R + D]
-                                      : verify_coin(seed, off, (uint32_t)D))
+          sm.uD = coins ? (a.uniforms ? a.uniforms[req * a.R + D] : verify_coin(seed, off, cc.pos))
                         : 0.f;
           sm.vx = xvalid ? SVec<E>::at(xr, x) : 0.f;
           sm.qx = (a.q && j < D && xvalid) ? a.q[(req * D + j) * a.ld_q + x] : 0.f;
@@ -1009,8 +1025,15 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
     // target-only u < p(x), with draft probabilities u q(x) < p(x).
     const bool qmode = a.q != nullptr;
     const float qx = sm.qx;
+    // Relaxed acceptance (target-only, a threshold in (0, 1); any other value means 1):
+    // p(x) >= threshold_single or u threshold_acc < p(x).
+    const float ts = (a.thr_single > 0.f && a.thr_single < 1.f) ? a.thr_single : 1.f;
+    const float ta = (a.thr_acc > 0.f && a.thr_acc < 1.f) ? a.thr_acc : 1.f;
+    const bool relaxed = !qmode && (ts < 1.f || ta < 1.f);
     auto accept = [&](double Z, double wx) -> int32_t {
       if (j >= D) return 0;
+      if (relaxed)
+        return (wx >= (double)ts * Z || (double)uj * (double)ta * Z < wx) ? 1 : 0;
       return (qmode ? (double)uj * (double)qx * Z < wx : (double)uj * Z < wx) ? 1 : 0;
     };
     // With draft probabilities the residual draw of a rejected row needs the draft row:
@@ -1172,10 +1195,38 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
             n, gitem, 1ull, (uint64_t)k, [](uint64_t) { return (uint64_t)1; }, lowv, sm.sc);
       uint64_t Z = gmass(C);
       if (kn.tp < 1.f) {
-        const double want = ceil((double)kn.tp * (double)Z);
-        const uint64_t P = (want > (double)Z) ? Z : (uint64_t)want;
-        C = sel::radix_adaptive<kCC, true, CBar>(n, gitem, C, P, wcomp, lowv, sm.sc);
+        // top-k first: the nucleus of the top-k set; joint: the nucleus of the whole row,
+        // intersected with the top-k set (the larger threshold)
+        const bool jt = a.joint && tk;
+        const uint64_t Zref = jt ? gmass(1ull) : Z;
+        const double want = ceil((double)kn.tp * (double)Zref);
+        const uint64_t P = (want > (double)Zref) ? Zref : (uint64_t)want;
+        const uint64_t Cp =
+            sel::radix_adaptive<kCC, true, CBar>(n, gitem, jt ? 1ull : C, P, wcomp, lowv, sm.sc);
+        C = max(C, Cp);
         Z = gmass(C);
+      }
+      if (kn.mp > 0.f) {
+        // min_p: of the kept tokens, those with x - M >= T ln(min_p); the passing values
+        // form a top segment, so the smallest passing key bounds them (the argmax passes)
+        const float thr = kn.T * logf(kn.mp);
+        uint32_t kmin = 0xFFFFFFFFu;
+        for (int i = tid; i < n; i += kCC) {
+          const float v = SVec<E>::at(xr, i);
+          if (v - M >= thr) kmin = min(kmin, fkey(v));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+        if (lane == 0) sm.redi[warp] = (int32_t)kmin;
+        cbar();
+        uint32_t km = 0xFFFFFFFFu;
+        for (int w2 = 0; w2 < kCW; ++w2) km = min(km, (uint32_t)sm.redi[w2]);
+        cbar();
+        const uint64_t Cm = comp_key(min(km, fkey(M)), kIdxMax);
+        if (Cm > C) {
+          C = Cm;
+          Z = gmass(C);
+        }
       }
       uint64_t wx = 0;
       if (xvalid && comp_key(fkey(vx), (uint32_t)x) >= C) wx = wfn(vx);
@@ -1489,6 +1540,61 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
 // elementwise in fp32 and summed in 2^-40 fixed point, and the draw is the smallest token
 // id whose inclusive prefix mass exceeds u_D times the total (a zero residual draws from
 // p''). One CTA per request; it writes accepted_tokens[b, j*] and its logprob.
+// p''_i of a finished row from its record: the kept set (by kind: the argmax; tokens at
+// or above the composite C; every token; or the sixteenths above gh plus those in
+// gl..gh at or above C) and the weight 2^((v - M) log2(e) / T) in 2^-40 units over the
+// kept mass Zk.
+struct KeptRow {
+  float M, sl2, s16, invZ;
+  uint64_t C;
+  int32_t am, gh, gl, kind;
+
+  __device__ __forceinline__ void load(const RowRes* rp, float T) {
+    M = __ldcg(&rp->M);
+    am = __ldcg(&rp->am);
+    kind = __ldcg(&rp->kind);
+    C = __ldcg(&rp->C);
+    const uint64_t Zk = __ldcg(&rp->Zk);
+    gh = __ldcg(&rp->gh);
+    gl = __ldcg(&rp->gl);
+    sl2 = kind != 0 ? __fdiv_rn(kLog2e, T) : 0.f;
+    s16 = sl2 * 16.f;
+    invZ = (float)(1.0 / (double)(Zk ? Zk : 1ull));
+  }
+  __device__ __forceinline__ int six_i(float v) const {
+    float t = __fmaf_rd(v, s16, 12582912.f);
+    t = fminf(fmaxf(t, 8388608.f), 16777216.f);
+    return __float_as_int(t) - 0x4B400000;
+  }
+  __device__ __forceinline__ float prob(float v, int64_t i) const {
+    if (kind == 0) return (i == am) ? 1.f : 0.f;
+    if (v == -INFINITY) return 0.f;
+    bool kept = kind == 2;
+    if (kind == 1) kept = comp_key(fkey(v), (uint32_t)i) >= C;
+    if (kind == 3) {
+      const int g = six_i(v);
+      kept = g > gh || (g >= gl && comp_key(fkey(v), (uint32_t)i) >= C);
+    }
+    if (!kept) return 0.f;
+    return __ull2float_rn(fixw(ex2((v - M) * sl2))) * invZ;
+  }
+};
+
+// Single-step sampling with a probability output: row r's kept distribution p'' to its
+// destination row (blockIdx.x the row, blockIdx.y a slice of `per` tokens). Rows the
+// chain kernel did not finish are left unwritten.
+template <typename E>
+__global__ void __launch_bounds__(256) k_chain_probs(SampleArgs a, int64_t per) {
+  const int64_t row = blockIdx.x;
+  if (__ldcg(&a.accept_length[row]) != 1) return;
+  KeptRow kr;
+  kr.load(a.ws.rowres + row, cknobs(a, row).T);
+  const E* xr = reinterpret_cast<const E*>(a.x) + row * a.ld;
+  float* dst = a.probs_out + (a.probs_row ? a.probs_row[row] : row) * a.ld_probs;
+  const int64_t i0 = (int64_t)blockIdx.y * per, i1 = min(a.V, i0 + per);
+  for (int64_t i = i0 + threadIdx.x; i < i1; i += 256) dst[i] = kr.prob(SVec<E>::at(xr, i), i);
+}
+
 template <typename E>
 __global__ void __launch_bounds__(256) k_chain_resid(SampleArgs a) {
   __shared__ uint64_t tot[8];
@@ -1507,32 +1613,12 @@ __global__ void __launch_bounds__(256) k_chain_resid(SampleArgs a) {
   const E* xr = reinterpret_cast<const E*>(a.x) + row * a.ld;
   int32_t tok = am;
   if (kind != 0) {
-    const CKnobs kn = cknobs(a, b);
-    const float sl2 = __fdiv_rn(kLog2e, kn.T);
-    const float s16 = sl2 * 16.f;
-    const uint64_t C = __ldcg(&rp->C), Zk = __ldcg(&rp->Zk);
-    const int32_t gh = __ldcg(&rp->gh), gl = __ldcg(&rp->gl);
-    const float invZ = (float)(1.0 / (double)(Zk ? Zk : 1ull));
+    KeptRow kr;
+    kr.load(rp, cknobs(a, b).T);
     const float* qr = a.q + (b * D + js) * a.ld_q;
     const int64_t V = a.V;
-    auto six_i = [&](float v) -> int {
-      float t = __fmaf_rd(v, s16, 12582912.f);
-      t = fminf(fmaxf(t, 8388608.f), 16777216.f);
-      return __float_as_int(t) - 0x4B400000;
-    };
     // p''_i, and the residual weight of token i in fixed point
-    auto pw = [&](int64_t i) -> float {
-      const float v = SVec<E>::at(xr, i);
-      if (v == -INFINITY) return 0.f;
-      bool kept = kind == 2;
-      if (kind == 1) kept = comp_key(fkey(v), (uint32_t)i) >= C;
-      if (kind == 3) {
-        const int g = six_i(v);
-        kept = g > gh || (g >= gl && comp_key(fkey(v), (uint32_t)i) >= C);
-      }
-      if (!kept) return 0.f;
-      return __ull2float_rn(fixw(ex2((v - M) * sl2))) * invZ;
-    };
+    auto pw = [&](int64_t i) -> float { return kr.prob(SVec<E>::at(xr, i), i); };
     auto rw = [&](int64_t i, bool from_p) -> uint64_t {
       const float p = pw(i);
       const float r = from_p ? p : fmaxf(p - qr[i], 0.f);
@@ -1618,6 +1704,12 @@ cudaError_t launch_chain_t(const SampleArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   k_chain<E><<<grid, kCThreads, dyn, s>>>(a);
   e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (a.probs_out) {
+    const int64_t per = 8192;
+    k_chain_probs<E><<<dim3((unsigned)a.rows, (unsigned)((a.V + per - 1) / per)), 256, 0, s>>>(a, per);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess || !a.q) return e;
   k_chain_resid<E><<<(unsigned)(a.rows / a.R), 256, 0, s>>>(a);
   return cudaGetLastError();

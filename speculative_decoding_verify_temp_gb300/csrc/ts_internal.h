@@ -68,6 +68,7 @@ struct Workspace {
                       // of rows served by its general path ([2]) and row claims ([3])
   uint32_t* order;    // [rows] the chain kernel's rows in claim order (cost tiers)
   uint32_t* creq;     // [batch] the chain kernel's per-request finished-row counts
+  int32_t* slen;      // [batch] single-step sampling: the chain kernel's accept lengths
   uint64_t* cand;     // [rows * cand_splits * kSTopK] per-row range masses of the row
                       // kernel (vocab > 0 only)
   int64_t cand_splits;
@@ -189,6 +190,17 @@ struct SampleArgs {
   uint64_t wait_cycles;  // chain kernel: SM clock cycles a stage wait may take
   const float* q;        // chain kernel: draft probabilities [B*D, ld_q] fp32, or NULL
   int64_t ld_q;
+  // chain kernel, the next rows
+  const float* min_p;    // per request (per row when sampling), or NULL
+  int32_t joint;         // top-p measured on the whole row's mass (single-step sampling)
+  float thr_single;      // relaxed acceptance (1: plain rejection sampling)
+  float thr_acc;
+  int32_t sample_n;      // 0: chain verification; > 0: single-step sampling of rows in
+                         // requests of sample_n rows (R = 1, D = 0; knobs per row, seed and
+                         // offset per request, coin row % sample_n)
+  float* probs_out;      // sampling: the kept distribution of each row, or NULL
+  int64_t ld_probs;
+  const int64_t* probs_row;  // destination row of each row's distribution, or NULL
 };
 
 // The row kernel in its renorm mode (fp32 probability rows, 16-byte aligned).

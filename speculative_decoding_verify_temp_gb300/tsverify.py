@@ -50,6 +50,39 @@ class ChainArgs(ctypes.Structure):
         ("accept_length", ctypes.c_void_p),
         ("accept_index", ctypes.c_void_p),
         ("logprobs", ctypes.c_void_p),
+        ("min_p", ctypes.c_void_p),
+        ("threshold_single", ctypes.c_float),
+        ("threshold_acc", ctypes.c_float),
+    ]
+
+
+TS_FILTER_TOP_K_FIRST = 0
+TS_FILTER_JOINT = 1
+
+
+class SampleArgs(ctypes.Structure):
+    """ts_sample_args of include/ts_verify.h."""
+    _fields_ = [
+        ("logits", ctypes.c_void_p),
+        ("dtype", ctypes.c_int32),
+        ("n_per_req", ctypes.c_int32),
+        ("batch", ctypes.c_int64),
+        ("vocab", ctypes.c_int64),
+        ("ld", ctypes.c_int64),
+        ("temperature", ctypes.c_void_p),
+        ("top_k", ctypes.c_void_p),
+        ("top_p", ctypes.c_void_p),
+        ("min_p", ctypes.c_void_p),
+        ("filter_order", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32),
+        ("seed", ctypes.c_void_p),
+        ("offset", ctypes.c_void_p),
+        ("uniforms", ctypes.c_void_p),
+        ("tokens", ctypes.c_void_p),
+        ("logprobs", ctypes.c_void_p),
+        ("probs", ctypes.c_void_p),
+        ("ld_probs", ctypes.c_int64),
+        ("probs_row", ctypes.c_void_p),
     ]
 
 
@@ -88,6 +121,8 @@ def load():
     L.ts_gather_logprobs.argtypes = [P, ctypes.c_int, i32, i64, i64, i64, P, P, P,
                                      ctypes.c_size_t, P]
     L.ts_gather_logprobs.restype = st
+    L.ts_sample_from_logits.argtypes = [ctypes.POINTER(SampleArgs), P, ctypes.c_size_t, P]
+    L.ts_sample_from_logits.restype = st
     _lib = L
     return L
 
@@ -194,7 +229,8 @@ def chain_spec_sampling(target, target_is_logits: bool, D: int, draft_tokens, *,
                         draft_probs=None, temperature=None, top_k=None, top_p=None,
                         seed=None, offset=None, uniforms=None, workspace=None,
                         accept_index: bool = True, logprobs: bool = True, outputs=None,
-                        stream=None):
+                        stream=None, min_p=None, threshold_single: float = 1.0,
+                        threshold_acc: float = 1.0):
     rows, V, ld = _rows(target)
     R = D + 1
     B = rows // R
@@ -221,9 +257,47 @@ def chain_spec_sampling(target, target_is_logits: bool, D: int, draft_tokens, *,
     a.accept_length = alen.data_ptr()
     a.accept_index = None if aidx is None else aidx.data_ptr()
     a.logprobs = None if lp is None else lp.data_ptr()
+    a.min_p = None if min_p is None else min_p.data_ptr()
+    a.threshold_single = float(threshold_single)
+    a.threshold_acc = float(threshold_acc)
     _check("ts_chain_spec_sampling", load().ts_chain_spec_sampling(
         ctypes.byref(a), _p(workspace), workspace.numel(), _stream(stream)))
     return dict(accepted_tokens=acc, accept_length=alen, accept_index=aidx, logprobs=lp)
+
+
+def sample_from_logits(logits, n_per_req: int = 1, *, temperature=None, top_k=None, top_p=None,
+                       min_p=None, joint: bool = False, seed=None, offset=None, uniforms=None,
+                       workspace=None, logprobs: bool = False, probs=None, probs_row=None,
+                       out=None, stream=None):
+    """Single-step sampling of each row. probs: True for a new [rows, V] fp32 tensor of
+    the kept distributions, or a 2-D fp32 tensor that probs_row (int64 [rows]) indexes."""
+    rows, V, ld = _rows(logits)
+    B = rows // n_per_req
+    dev = logits.device
+    if workspace is None:
+        workspace = make_workspace(rows, 1, V, dev, stream)
+    tok = out if out is not None else torch.empty((rows,), dtype=torch.int32, device=dev)
+    lp = torch.empty((rows,), dtype=torch.float32, device=dev) if logprobs else None
+    if probs is True:
+        probs = torch.empty((rows, V), dtype=torch.float32, device=dev)
+    a = SampleArgs()
+    a.logits = logits.data_ptr()
+    a.dtype = _dtype(logits)
+    a.n_per_req = n_per_req
+    a.batch, a.vocab, a.ld = B, V, ld
+    for name, t in (("temperature", temperature), ("top_k", top_k), ("top_p", top_p),
+                    ("min_p", min_p), ("seed", seed), ("offset", offset),
+                    ("uniforms", uniforms), ("probs_row", probs_row)):
+        setattr(a, name, None if t is None else t.data_ptr())
+    a.filter_order = TS_FILTER_JOINT if joint else TS_FILTER_TOP_K_FIRST
+    a.tokens = tok.data_ptr()
+    a.logprobs = None if lp is None else lp.data_ptr()
+    if probs is not None:
+        a.probs = probs.data_ptr()
+        a.ld_probs = probs.stride(0)
+    _check("ts_sample_from_logits", load().ts_sample_from_logits(
+        ctypes.byref(a), _p(workspace), workspace.numel(), _stream(stream)))
+    return dict(tokens=tok, logprobs=lp, probs=probs)
 
 
 def gumbel_max_sample(logits, n_per_req: int, temperature, seed, offset, workspace=None,

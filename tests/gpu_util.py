@@ -70,13 +70,15 @@ def _slices(n, parts):
     return [(i, min(n, i + step)) for i in range(0, n, step)]
 
 
-def oracle_all(fn, rows, bf16, R, args=(), per_request=None, static=None, procs=None):
+def oracle_all(fn, rows, bf16, R, args=(), per_request=None, static=None, procs=None,
+               per_row=None):
     """oracle.<fn>(x, *args, **kw) over every request of a launch, the requests split over
     the host cores (the method is per request: each request's coins come from its own seed
     and offset, so the slices are independent). rows: the launch's [B*R, V] values as bf16
     bits (bf16=True) or fp32. args: positional arguments, each (array, "row" | "req" |
     None) - sliced by rows, by requests, or passed whole; per_request: keyword arrays of
-    one entry per request (None allowed); static: keyword arguments passed as they are.
+    one entry per request (None allowed); per_row: keyword arrays of one entry per row;
+    static: keyword arguments passed as they are.
     Dict results (the chain calls) and tuple results are concatenated."""
     B = rows.shape[0] // R
     procs = procs or max(1, min(os.cpu_count() or 1, 32))
@@ -87,6 +89,8 @@ def oracle_all(fn, rows, bf16, R, args=(), per_request=None, static=None, procs=
         for arr, by in args:
             a.append(arr[b0 * R:b1 * R] if by == "row" else arr[b0:b1] if by == "req" else arr)
         kw = {k: (None if v is None else v[b0:b1]) for k, v in per_request.items()}
+        kw.update({k: (None if v is None else v[b0 * R:b1 * R])
+                   for k, v in (per_row or {}).items()})
         kw.update(static or {})
         tasks.append((fn, np.ascontiguousarray(rows[b0 * R:b1 * R]), bf16, tuple(a), kw))
     with multiprocessing.get_context("spawn").Pool(len(tasks)) as pool:
