@@ -77,6 +77,10 @@ def _load():
                                                  P]
         L.orc_sample_from_logits.argtypes = [P, i64, i32, i64, i64, P, P, P, P, ctypes.c_int,
                                              P, P, P, P, P, P, P]
+        L.orc_verify_chain_greedy_ragged.argtypes = [P, i64, i32, i64, i64, P, P, P, P, P, P]
+        L.orc_chain_spec_sampling_ragged.argtypes = [P, ctypes.c_int, i64, i32, i64, i64, P, P,
+                                                     P, P, P, f32, f32, P, i64, P, P, P, P, P,
+                                                     P, P, P, P]
         _lib = L
     return _lib
 
@@ -212,6 +216,56 @@ def chain_spec_sampling(target, target_is_logits: bool, D: int, draft_tokens, *,
             _ptr(_i32(top_k)), _ptr(_f32(top_p)), _ptr(_f32(min_p)), float(threshold_single),
             float(threshold_acc), _ptr(q), V, _ptr(dt), _ptr(_i64(seed)), _ptr(_i64(offset)),
             _ptr(uni), _ptr(acc), _ptr(alen), _ptr(aidx), _ptr(lp), _ptr(marg))
+    return dict(accepted_tokens=acc, accept_length=alen, accept_index=aidx, logprobs=lp,
+                margin=marg)
+
+
+def verify_chain_greedy_ragged(logits, D: int, qo_indptr, draft_tokens) -> dict:
+    """Greedy verification of packed rows: request b owns rows qo_indptr[b] ..
+    qo_indptr[b+1] - 1; drafts [B, D] padded; outputs padded to [B, D+1]."""
+    x = _f32(logits)
+    V = x.shape[1]
+    qo = np.ascontiguousarray(qo_indptr, dtype=np.int32)
+    B = qo.shape[0] - 1
+    R = D + 1
+    dt = np.ascontiguousarray(_i32(draft_tokens).reshape(B, max(D, 0)))
+    acc = np.zeros((B, R), np.int32)
+    alen = np.zeros(B, np.int32)
+    aidx = np.zeros((B, R), np.int32)
+    lp = np.zeros((B, R), np.float64)
+    _load().orc_verify_chain_greedy_ragged(_ptr(x), B, D, V, V, _ptr(qo), _ptr(dt), _ptr(acc),
+                                           _ptr(alen), _ptr(aidx), _ptr(lp))
+    return dict(accepted_tokens=acc, accept_length=alen, accept_index=aidx, logprobs=lp)
+
+
+def chain_spec_sampling_ragged(target, target_is_logits: bool, D: int, qo_indptr,
+                               draft_tokens, *, draft_probs=None, temperature=None, top_k=None,
+                               top_p=None, min_p=None, threshold_single: float = 1.0,
+                               threshold_acc: float = 1.0, seed=None, offset=None,
+                               uniforms=None) -> dict:
+    """Chain sampling of packed rows (request b owns rows qo_indptr[b] ..); knobs, seeds
+    and offsets per request; drafts [B, D], draft probs [B*D, V] and uniforms [B, D+1]
+    padded; outputs padded to [B, D+1]."""
+    x = _f32(target)
+    V = x.shape[1]
+    qo = np.ascontiguousarray(qo_indptr, dtype=np.int32)
+    B = qo.shape[0] - 1
+    R = D + 1
+    dt = np.ascontiguousarray(_i32(draft_tokens).reshape(B, max(D, 0)))
+    q = None if draft_probs is None else _f32(draft_probs).reshape(B * D, V)
+    if uniforms is None and (seed is None or offset is None):
+        raise ValueError("either uniforms or seed and offset are required")
+    acc = np.zeros((B, R), np.int32)
+    alen = np.zeros(B, np.int32)
+    aidx = np.zeros((B, R), np.int32)
+    lp = np.zeros((B, R), np.float64)
+    marg = np.zeros(B, np.float64)
+    _load().orc_chain_spec_sampling_ragged(
+        _ptr(x), int(target_is_logits), B, D, V, V, _ptr(qo), _ptr(_f32(temperature)),
+        _ptr(_i32(top_k)), _ptr(_f32(top_p)), _ptr(_f32(min_p)), float(threshold_single),
+        float(threshold_acc), _ptr(q), V, _ptr(dt), _ptr(_i64(seed)), _ptr(_i64(offset)),
+        _ptr(None if uniforms is None else _f32(uniforms).reshape(B, R)), _ptr(acc),
+        _ptr(alen), _ptr(aidx), _ptr(lp), _ptr(marg))
     return dict(accepted_tokens=acc, accept_length=alen, accept_index=aidx, logprobs=lp,
                 margin=marg)
 

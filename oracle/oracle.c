@@ -410,6 +410,89 @@ void orc_chain_spec_sampling_ex(const float* target, int target_is_logits, int64
 }
 
 /*
+ * Ragged verification (TensorRT-LLM SpecMetadata.verify_lens / qo_indptr; ragged_helpers
+ * scatter_ragged_to_padded, count_accepted_ragged, fill_padded_rows_onehot, and the
+ * accept ceiling min(num_accepted, verify_lens)): request b owns the packed target rows
+ * qo_indptr[b] .. qo_indptr[b+1] - 1, L_b of them, and verifies only its own window: its
+ * first D_b = L_b - 1 drafts, exactly as a request with D = D_b drafts (the pages pad the
+ * rows to a rectangle, fill the padding rows one-hot and cap the count at L_b so that no
+ * token past the window is committed; here the window is verified directly). Drafts,
+ * draft probabilities and coins keep their padded layouts ([B, D], [B*D, ld_draft],
+ * [B, D+1]: the final draw's coin is entry D_b), the outputs are padded to [B, D+1]
+ * (-1, -1, 0 past the emitted tokens) and accept_index holds packed row numbers
+ * qo_indptr[b] + j. A window outside [1, D+1] rows is left unverified (accept_length 0).
+ */
+static void ragged_pad(int64_t b, int32_t D, int32_t Db, int64_t first, const int32_t* acc,
+                       int32_t alen, const int32_t* idx, const double* lp,
+                       int32_t* accepted_tokens, int32_t* accept_length, int32_t* accept_index,
+                       double* logprobs) {
+  const int64_t R = (int64_t)D + 1;
+  for (int64_t j = 0; j < R; ++j) {
+    int in = j <= Db && alen > 0;
+    accepted_tokens[b * R + j] = in ? acc[j] : -1;
+    if (accept_index)
+      accept_index[b * R + j] = (in && idx[j] >= 0) ? (int32_t)(first + idx[j]) : -1;
+    if (logprobs) logprobs[b * R + j] = in ? lp[j] : 0.0;
+  }
+  accept_length[b] = alen;
+}
+
+void orc_verify_chain_greedy_ragged(const float* logits, int64_t B, int32_t D, int64_t V,
+                                    int64_t ld, const int32_t* qo_indptr,
+                                    const int32_t* draft_tokens, int32_t* accepted_tokens,
+                                    int32_t* accept_length, int32_t* accept_index,
+                                    double* logprobs) {
+  int32_t acc[ORC_MAX_R], idx[ORC_MAX_R];
+  double lp[ORC_MAX_R];
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t first = qo_indptr[b];
+    const int64_t L = (int64_t)qo_indptr[b + 1] - first;
+    int32_t alen = 0;
+    if (L >= 1 && L <= (int64_t)D + 1) {
+      const int32_t Db = (int32_t)L - 1;
+      orc_verify_chain_greedy(logits + first * ld, 1, Db, V, ld, draft_tokens + b * D, acc,
+                              &alen, idx, lp);
+    }
+    ragged_pad(b, D, (int32_t)L - 1, first, acc, alen, idx, lp, accepted_tokens, accept_length,
+               accept_index, logprobs);
+  }
+}
+
+void orc_chain_spec_sampling_ragged(const float* target, int target_is_logits, int64_t B,
+                                    int32_t D, int64_t V, int64_t ld, const int32_t* qo_indptr,
+                                    const float* temperature, const int32_t* top_k,
+                                    const float* top_p, const float* min_p,
+                                    float threshold_single, float threshold_acc,
+                                    const float* draft_probs, int64_t ld_draft,
+                                    const int32_t* draft_tokens, const int64_t* seed,
+                                    const int64_t* offset, const float* uniforms,
+                                    int32_t* accepted_tokens, int32_t* accept_length,
+                                    int32_t* accept_index, double* logprobs,
+                                    double* margin_out) {
+  int32_t acc[ORC_MAX_R], idx[ORC_MAX_R];
+  double lp[ORC_MAX_R];
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t first = qo_indptr[b];
+    const int64_t L = (int64_t)qo_indptr[b + 1] - first;
+    int32_t alen = 0;
+    double m = INFINITY;
+    if (L >= 1 && L <= (int64_t)D + 1) {
+      const int32_t Db = (int32_t)L - 1;
+      orc_chain_spec_sampling_ex(
+          target + first * ld, target_is_logits, 1, Db, V, ld,
+          temperature ? temperature + b : NULL, top_k ? top_k + b : NULL,
+          top_p ? top_p + b : NULL, min_p ? min_p + b : NULL, threshold_single, threshold_acc,
+          draft_probs ? draft_probs + b * D * ld_draft : NULL, ld_draft, draft_tokens + b * D,
+          seed ? seed + b : NULL, offset ? offset + b : NULL,
+          uniforms ? uniforms + b * ((int64_t)D + 1) : NULL, acc, &alen, idx, lp, &m);
+    }
+    ragged_pad(b, D, (int32_t)L - 1, first, acc, alen, idx, lp, accepted_tokens, accept_length,
+               accept_index, logprobs);
+    if (margin_out) margin_out[b] = m;
+  }
+}
+
+/*
  * Single-step sampling from logits (TokenSpeed sample(): softmax with temperature,
  * then top_k_top_p_sampling_from_probs(..., filter_apply_order="joint", seed, offset);
  * TensorRT-LLM advanced_sample_draft / advanced_sample_draft_block:

@@ -42,6 +42,9 @@ extern "C" {
  * pages name a greedy temperature threshold without giving its value. */
 #define ORC_GREEDY_T 1e-5f
 
+/* Rows of a request at most (the library's limit on D is 64). */
+#define ORC_MAX_R 65
+
 /* ---- Philox4x32-10 and its streams --------------------------------------- */
 void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
 float orc_u01(uint32_t x);
@@ -92,6 +95,22 @@ void orc_chain_spec_sampling_ex(const float* target, int target_is_logits, int64
                                 const int64_t* offset, const float* uniforms,
                                 int32_t* accepted_tokens, int32_t* accept_length,
                                 int32_t* accept_index, double* logprobs, double* margin_out);
+void orc_verify_chain_greedy_ragged(const float* logits, int64_t B, int32_t D, int64_t V,
+                                    int64_t ld, const int32_t* qo_indptr,
+                                    const int32_t* draft_tokens, int32_t* accepted_tokens,
+                                    int32_t* accept_length, int32_t* accept_index,
+                                    double* logprobs);
+void orc_chain_spec_sampling_ragged(const float* target, int target_is_logits, int64_t B,
+                                    int32_t D, int64_t V, int64_t ld, const int32_t* qo_indptr,
+                                    const float* temperature, const int32_t* top_k,
+                                    const float* top_p, const float* min_p,
+                                    float threshold_single, float threshold_acc,
+                                    const float* draft_probs, int64_t ld_draft,
+                                    const int32_t* draft_tokens, const int64_t* seed,
+                                    const int64_t* offset, const float* uniforms,
+                                    int32_t* accepted_tokens, int32_t* accept_length,
+                                    int32_t* accept_index, double* logprobs,
+                                    double* margin_out);
 void orc_sample_from_logits(const float* logits, int64_t B, int32_t n_per_req, int64_t V,
                             int64_t ld, const float* temperature, const int32_t* top_k,
                             const float* top_p, const float* min_p, int joint,
