@@ -134,6 +134,23 @@ ts_status ts_verify_chain_greedy(const void* target_logits, ts_dtype dt, int64_t
                                  float* logprobs, void* workspace, size_t ws_bytes,
                                  cudaStream_t stream);
 
+/* Greedy verification of a ragged batch [TRT-IF ragged_helpers count_accepted_ragged,
+ * scatter_ragged_to_padded: each request verifies its own window]: as
+ * ts_verify_chain_greedy, with the target rows packed as described for
+ * ts_chain_args.qo_indptr (request b owns rows qo_indptr[b] .. qo_indptr[b+1] - 1, at
+ * most D + 1 of them, and compares its first L_b - 1 drafts), total_rows rows in all,
+ * drafts [batch, D] padded, outputs [batch, D+1] padded, accept_index packed row numbers.
+ * The outputs are cleared on `stream` first (accept_length 0, tokens and indices -1,
+ * logprobs 0), which is what a window that does not fit leaves.
+ * Workspace: ts_workspace_size(batch, D + 1, vocab). */
+ts_status ts_verify_chain_greedy_ragged(const void* target_logits, ts_dtype dt, int64_t batch,
+                                        int32_t D, int64_t vocab, int64_t ld,
+                                        const int32_t* qo_indptr, int64_t total_rows,
+                                        const int32_t* draft_tokens, int32_t* accepted_tokens,
+                                        int32_t* accept_length, int32_t* accept_index,
+                                        float* logprobs, void* workspace, size_t ws_bytes,
+                                        cudaStream_t stream);
+
 /* Arguments of ts_chain_spec_sampling. Layouts as in the comments; NULL where allowed. */
 typedef struct ts_chain_args {
   const void* target;        /* [batch*(D+1), ld]: logits (target_is_logits = 1, dtype
@@ -173,6 +190,18 @@ typedef struct ts_chain_args {
   float threshold_acc;       /* threshold_acc), target-only: accept iff p(x) >= t_single
                                 or u * t_acc < p(x). Values outside (0, 1) mean 1 (plain
                                 rejection sampling); not allowed with draft_probs. */
+  /* Ragged verification (TRT-IF SpecMetadata verify_lens / qo_indptr), or NULL: the
+   * target rows are packed, request b owning rows qo_indptr[b] .. qo_indptr[b+1] - 1
+   * (L_b of them, 1 <= L_b <= D + 1) and verifying its first L_b - 1 drafts exactly as a
+   * request with D = L_b - 1 would; total_rows = qo_indptr[batch] rows in all. Drafts,
+   * draft probabilities and coins keep the padded [batch, D(+1)] layouts (the final
+   * draw's coin is position L_b - 1 of the request's stream, or uniforms[b, L_b - 1]);
+   * outputs are [batch, D+1] with -1 (tokens, indices) and 0 (logprobs) past the
+   * emitted tokens, and accept_index holds packed row numbers qo_indptr[b] + j. A window
+   * outside [1, D + 1] rows or past total_rows leaves its request at accept_length 0.
+   * Logit targets only, 16-byte aligned rows, vocab <= 2^18 (else TS_ERR_INVALID_ARG). */
+  const int32_t* qo_indptr;  /* [batch + 1] device, or NULL */
+  int64_t total_rows;
 } ts_chain_args;
 
 /* Chain speculative sampling [TRT-IF rejection_sampling_one_model; TS-FI verify():

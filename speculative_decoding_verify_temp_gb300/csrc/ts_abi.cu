@@ -117,6 +117,7 @@ size_t workspace_layout(int64_t batch, int32_t R, int64_t vocab, void* base, Wor
   w.order = reinterpret_cast<uint32_t*>(take(rows * 4));
   w.creq = reinterpret_cast<uint32_t*>(take((size_t)batch * 4));
   w.slen = reinterpret_cast<int32_t*>(take(rows * 4));
+  w.rreq = reinterpret_cast<uint32_t*>(take(rows * 4));
   if (vocab > 0) {
     // sized for fp32 rows, which have the most chunks (at most kMaxSplits)
     int64_t chunk = 0;
@@ -271,6 +272,52 @@ ts_status ts_verify_chain_greedy(const void* target_logits, ts_dtype dt, int64_t
   return launched(tsv::launch_rowstat(a, dt == TS_BF16, stream), "greedy verify launch");
 }
 
+ts_status ts_verify_chain_greedy_ragged(const void* target_logits, ts_dtype dt, int64_t batch,
+                                        int32_t D, int64_t vocab, int64_t ld,
+                                        const int32_t* qo_indptr, int64_t total_rows,
+                                        const int32_t* draft_tokens, int32_t* accepted_tokens,
+                                        int32_t* accept_length, int32_t* accept_index,
+                                        float* logprobs, void* workspace, size_t ws_bytes,
+                                        cudaStream_t stream) {
+  ts_status st;
+  if ((st = check_dtype(dt)) != TS_OK) return st;
+  if (D < 0 || D > TS_MAX_DRAFT) return fail(TS_ERR_INVALID_ARG, "D must be in [0, %d]", TS_MAX_DRAFT);
+  if ((st = check_common(batch, vocab, ld)) != TS_OK) return st;
+  const int32_t R = D + 1;
+  if (!target_logits || !qo_indptr || !accepted_tokens || !accept_length || (D > 0 && !draft_tokens))
+    return fail(TS_ERR_INVALID_ARG,
+                "target_logits, qo_indptr, draft_tokens, accepted_tokens and accept_length are required");
+  if (total_rows < 1 || total_rows > batch * (int64_t)R)
+    return fail(TS_ERR_INVALID_ARG, "total_rows must be in [1, batch * (D + 1)]");
+  tsv::RowStatArgs a{};
+  if ((st = take_workspace(batch, R, vocab, workspace, ws_bytes, &a.ws)) != TS_OK) return st;
+  // outputs of a window that does not fit: accept_length 0, tokens and indices -1,
+  // logprobs 0 (the others are overwritten)
+  const size_t outs = (size_t)batch * (size_t)R * sizeof(int32_t);
+  cudaError_t e = cudaMemsetAsync(accept_length, 0, (size_t)batch * sizeof(int32_t), stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(accepted_tokens, 0xFF, outs, stream);
+  if (e == cudaSuccess && accept_index) e = cudaMemsetAsync(accept_index, 0xFF, outs, stream);
+  if (e == cudaSuccess && logprobs) e = cudaMemsetAsync(logprobs, 0, outs, stream);
+  if (e != cudaSuccess) return launched(e, "ragged greedy verify clear");
+  a.x = target_logits;
+  a.ld = ld;
+  a.V = vocab;
+  a.rows = total_rows;
+  choose_splits(a.rows, vocab, 2048, &a.splits, &a.split_len);
+  a.vec = aligned16(target_logits, ld, dt == TS_BF16 ? 2 : 4);
+  a.want_lse = logprobs != nullptr;
+  a.kind = 0;
+  a.D = D;
+  a.draft_tokens = draft_tokens;
+  a.accepted_tokens = accepted_tokens;
+  a.accept_length = accept_length;
+  a.accept_index = accept_index;
+  a.logprobs = logprobs;
+  a.qo = qo_indptr;
+  a.nreq = batch;
+  return launched(tsv::launch_rowstat(a, dt == TS_BF16, stream), "ragged greedy verify launch");
+}
+
 ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t ws_bytes,
                                  cudaStream_t stream) {
   if (!p) return fail(TS_ERR_INVALID_ARG, "args is NULL");
@@ -289,9 +336,13 @@ ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t
   const bool relaxed = thr_s < 1.f || thr_a < 1.f;
   if (relaxed && p->draft_probs)
     return fail(TS_ERR_INVALID_ARG, "relaxed acceptance thresholds are target-only");
-  const bool next_knobs = relaxed || p->min_p != nullptr;
+  const bool ragged = p->qo_indptr != nullptr;
+  if (ragged && (p->total_rows < 1 || p->total_rows > p->batch * (int64_t)R))
+    return fail(TS_ERR_INVALID_ARG, "total_rows must be in [1, batch * (D + 1)]");
+  const bool next_knobs = relaxed || p->min_p != nullptr || ragged;
   if (next_knobs && !p->target_is_logits)
-    return fail(TS_ERR_INVALID_ARG, "min_p and relaxed thresholds need logit targets");
+    return fail(TS_ERR_INVALID_ARG,
+                "min_p, relaxed thresholds and ragged batches need logit targets");
   if (!p->target_is_logits) {
     if (p->target_dtype != TS_F32)
       return fail(TS_ERR_UNSUPPORTED_DTYPE, "probability targets must be fp32");
@@ -370,11 +421,17 @@ ts_status ts_chain_spec_sampling(const ts_chain_args* p, void* workspace, size_t
     sa.min_p = p->min_p;
     sa.thr_single = thr_s;
     sa.thr_acc = thr_a;
+    sa.nreq = p->batch;
+    if (ragged) {
+      sa.qo = p->qo_indptr;
+      sa.rows = p->total_rows;
+    }
     return launched(tsv::launch_chain(sa, stream), "row-streaming chain launch");
   }
   if (next_knobs)
     return fail(TS_ERR_INVALID_ARG,
-                "min_p and relaxed thresholds need 16-byte aligned rows and vocab <= %lld",
+                "min_p, relaxed thresholds and ragged batches need 16-byte aligned rows and "
+                "vocab <= %lld",
                 (long long)tsv::kRowMaxVocab);
   if (p->draft_probs)
     return fail(TS_ERR_INVALID_ARG,
@@ -459,6 +516,7 @@ ts_status ts_sample_from_logits(const ts_sample_args* p, void* workspace, size_t
   sa.ld_probs = p->ld_probs;
   sa.probs_row = p->probs_row;
   sa.wait_cycles = g_wait_cycles.load(std::memory_order_relaxed);
+  sa.nreq = rows;
   return launched(tsv::launch_chain(sa, stream), "sampling launch");
 }
 

@@ -113,14 +113,15 @@ __device__ __forceinline__ CKnobs cknobs(const SampleArgs& a, int64_t req) {
 }
 
 // The seed, offset and coin position of a row's draw coin: a chain's request and its
-// position D, or, when sampling, the row's request and its position within it.
+// position D (the request's own draft count), or, when sampling, the row's request and
+// its position within it.
 struct CCoin {
   int64_t sreq;
   uint32_t pos;
 };
-__device__ __forceinline__ CCoin ccoin(const SampleArgs& a, int64_t req) {
+__device__ __forceinline__ CCoin ccoin(const SampleArgs& a, int64_t req, int32_t D) {
   if (a.sample_n > 0) return CCoin{req / a.sample_n, (uint32_t)(req % a.sample_n)};
-  return CCoin{req, (uint32_t)a.D};
+  return CCoin{req, (uint32_t)D};
 }
 
 __device__ __forceinline__ int ctier(const CKnobs& kn) {
@@ -260,15 +261,30 @@ __device__ __forceinline__ uint32_t warp_kth_key(const uint32_t (&key)[E], int k
 // reserved per CTA)
 static_assert(2 * (kCNSt * kCStageBytes + sizeof(CSmem) + 1024) <= 233472, "two CTAs an SM");
 
+// The packed rows of request b: [first, first + count); count 0 for a ragged window that
+// does not fit (outside the rows, or more than R rows), which is left unverified.
+struct CWin {
+  int64_t first;
+  int32_t count;
+};
+__device__ __forceinline__ CWin cwin(const SampleArgs& a, int64_t b) {
+  if (!a.qo) return CWin{b * a.R, a.R};
+  const int64_t f = a.qo[b], e = a.qo[b + 1];
+  if (f < 0 || e > a.rows || e - f < 1 || e - f > a.R) return CWin{0, 0};
+  return CWin{f, (int32_t)(e - f)};
+}
+
 // Orders the rows by cost tier (stable within a tier) and clears the per-launch state. A
-// request's rows share its knobs, so the order is built over requests: request b at
-// position p of the order owns the claim positions p R .. p R + R - 1. Each entry holds
-// the row and, in bits 30-31, its number of passes minus one.
+// request's rows share its knobs, so the order is built over requests: the rows of a
+// request take consecutive claim positions, after the rows of the requests before it in
+// its tier. Each entry holds the row and, in bits 30-31, its number of passes minus one;
+// positions past the last scheduled row hold kNoRow. A ragged batch also records the
+// request of every packed row.
 __global__ void __launch_bounds__(1024) k_chain_plan(SampleArgs a) {
   __shared__ uint32_t cnt[4];
   __shared__ uint32_t wc[32][4];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t B = a.rows / a.R;
+  const int64_t B = a.nreq;
   if (tid < 4) cnt[tid] = 0u;
   if (tid == 0) {
     a.ws.work[0] = 0u;  // top-k candidates collected (all rows)
@@ -276,54 +292,64 @@ __global__ void __launch_bounds__(1024) k_chain_plan(SampleArgs a) {
     a.ws.work[2] = 0u;  // rows the general path served
     a.ws.work[3] = 0u;  // row claims
   }
-  uint32_t c0 = 0u, c1 = 0u, c2 = 0u, c3 = 0u;
+  uint32_t c[4] = {0u, 0u, 0u, 0u};
   for (int64_t b = tid; b < B; b += 1024) {
     a.ws.creq[b] = 0u;
     a.accept_length[b] = 0;
     const int t = ctier(cknobs(a, b));
-    c0 += (t == 0);
-    c1 += (t == 1);
-    c2 += (t == 2);
-    c3 += (t == 3);
+    const int32_t n = cwin(a, b).count;
+    c[t] += (uint32_t)n;
+    if (n == 0)  // a ragged window that does not fit: its outputs read as unused
+      for (int32_t jj = 0; jj < a.R; ++jj) {
+        a.accepted_tokens[b * a.R + jj] = -1;
+        if (a.accept_index) a.accept_index[b * a.R + jj] = -1;
+        if (a.logprobs) a.logprobs[b * a.R + jj] = 0.f;
+      }
   }
   __syncthreads();
-  if (c0) atomicAdd(&cnt[0], c0);
-  if (c1) atomicAdd(&cnt[1], c1);
-  if (c2) atomicAdd(&cnt[2], c2);
-  if (c3) atomicAdd(&cnt[3], c3);
+  for (int q = 0; q < 4; ++q)
+    if (c[q]) atomicAdd(&cnt[q], c[q]);
   __syncthreads();
-  uint32_t r0 = 0u, r1 = cnt[0], r2 = cnt[0] + cnt[1], r3 = cnt[0] + cnt[1] + cnt[2];
-  const uint32_t lt = (1u << lane) - 1u;
+  uint32_t r[4] = {0u, cnt[0], cnt[0] + cnt[1], cnt[0] + cnt[1] + cnt[2]};
+  const uint32_t total = r[3] + cnt[3];
   for (int64_t bb = 0; bb < B; bb += 1024) {
     const int64_t b = bb + tid;
     int t = 4;
     uint32_t np = 0u;
+    CWin wn{0, 0};
     if (b < B) {
       const CKnobs kn = cknobs(a, b);
       t = ctier(kn);
       np = (kn.kind == kCTopP) ? 2u : 0u;  // passes - 1
+      wn = cwin(a, b);
     }
     uint32_t before = 0u;
     for (int q = 0; q < 4; ++q) {
-      const uint32_t m = __ballot_sync(0xffffffffu, t == q);
-      if (lane == 0) wc[warp][q] = (uint32_t)__popc(m);
-      if (t == q) before = (uint32_t)__popc(m & lt);
+      const uint32_t v = (t == q) ? (uint32_t)wn.count : 0u;
+      uint32_t inc = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (lane == 31) wc[warp][q] = inc;
+      if (t == q) before = inc - v;
     }
     __syncthreads();
     if (t < 4) {
-      uint32_t pos = (t == 0 ? r0 : t == 1 ? r1 : t == 2 ? r2 : r3) + before;
+      uint32_t pos = r[t] + before;
       for (int w = 0; w < warp; ++w) pos += wc[w][t];
-      for (int32_t jj = 0; jj < a.R; ++jj)
-        a.ws.order[(int64_t)pos * a.R + jj] = (uint32_t)(b * a.R + jj) | (np << 30);
+      for (int32_t jj = 0; jj < wn.count; ++jj) {
+        const int64_t row = wn.first + jj;
+        if ((int64_t)pos + jj < a.rows) a.ws.order[(int64_t)pos + jj] = (uint32_t)row | (np << 30);
+        if (a.qo) a.ws.rreq[row] = (uint32_t)b;
+      }
     }
-    for (int w = 0; w < 32; ++w) {
-      r0 += wc[w][0];
-      r1 += wc[w][1];
-      r2 += wc[w][2];
-      r3 += wc[w][3];
-    }
+    for (int w = 0; w < 32; ++w)
+      for (int q = 0; q < 4; ++q) r[q] += wc[w][q];
     __syncthreads();
   }
+  for (int64_t p = (int64_t)total + tid; p < a.rows; p += 1024) a.ws.order[p] = kNoRow;
 }
 
 template <typename E>
@@ -450,13 +476,19 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
     cbar();
     if (ab || row < 0 || row >= a.rows) break;
 
-    const int64_t req = row / a.R;
-    const int32_t j = (int32_t)(row % a.R);
+    // the row's request, its position j in the request's window of rows (first row
+    // rbase) and the request's drafts D (a ragged window verifies count - 1 of them);
+    // the padded layouts (drafts, draft probabilities, coins, outputs) hold DP = a.D
+    const int64_t req = a.qo ? (int64_t)__ldcg(&a.ws.rreq[row]) : row / a.R;
+    const CWin win = cwin(a, req);
+    const int64_t rbase = win.first;
+    const int32_t j = (int32_t)(row - rbase);
+    const int32_t D = win.count - 1;
+    const int32_t DP = a.D;
     const CKnobs kn = cknobs(a, req);
     const E* xr = reinterpret_cast<const E*>(a.x) + row * a.ld;
     const uint4* rp = reinterpret_cast<const uint4*>(xr);
-    const int32_t D = a.D;
-    const int32_t x = (j < D) ? a.draft_tokens[req * D + j] : -1;
+    const int32_t x = (j < D) ? a.draft_tokens[req * DP + j] : -1;
     const bool xvalid = x >= 0 && (int64_t)x < V;
     const float sl2 = (kn.kind == kCGreedy) ? 0.f : __fdiv_rn(kLog2e, kn.T);
     const float s16 = sl2 * 16.f;  // sixteenths of an octave per logit unit
@@ -855,7 +887,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
           sm.M = v;
           sm.am = (i == INT32_MAX) ? 0 : i;
           sm.S1 = s;
-          const CCoin cc = ccoin(a, req);
+          const CCoin cc = ccoin(a, req, D);
           const uint64_t seed = a.seed ? (uint64_t)a.seed[cc.sreq] : 0;
           const uint64_t off = a.offset ? (uint64_t)a.offset[cc.sreq] : 0;
           const bool coins = kn.kind != kCGreedy;
@@ -865,7 +897,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
           sm.uD = coins ? (a.uniforms ? a.uniforms[req * a.R + D] : verify_coin(seed, off, cc.pos))
                         : 0.f;
           sm.vx = xvalid ? SVec<E>::at(xr, x) : 0.f;
-          sm.qx = (a.q && j < D && xvalid) ? a.q[(req * D + j) * a.ld_q + x] : 0.f;
+          sm.qx = (a.q && j < D && xvalid) ? a.q[(req * DP + j) * a.ld_q + x] : 0.f;
         }
       }
       cbar();
@@ -1050,25 +1082,27 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
       a.ws.rowres[row] = rr;
       __threadfence();
       const uint32_t prev = atomicAdd(&a.ws.creq[req], 1u);
-      if (prev != (uint32_t)a.R - 1) return;
+      if (prev != (uint32_t)D) return;
       __threadfence();
       int32_t js = D;
       for (int32_t jj = 0; jj < D; ++jj)
-        if (!__ldcg(&a.ws.rowres[req * a.R + jj].acc)) {
+        if (!__ldcg(&a.ws.rowres[rbase + jj].acc)) {
           js = jj;
           break;
         }
+      // positions of the padded outputs; a ragged window's rows past it read as unused
       for (int32_t jj = 0; jj < a.R; ++jj) {
-        const int64_t rj = req * a.R + jj;
+        const int64_t oj = req * a.R + jj;
+        const int64_t rj = rbase + jj;  // the packed row of position jj (jj <= D)
         int32_t t = -1;
-        if (jj < js) t = a.draft_tokens[req * D + jj];
+        if (jj < js) t = a.draft_tokens[req * DP + jj];
         else if (jj == js) t = __ldcg(&a.ws.rowres[rj].tok);
         if (qmode && jj == js && js < D) {  // the residual kernel writes this position
-          if (a.accept_index) a.accept_index[rj] = (int32_t)rj;
+          if (a.accept_index) a.accept_index[oj] = (int32_t)rj;
           continue;
         }
-        a.accepted_tokens[rj] = t;
-        if (a.accept_index) a.accept_index[rj] = (jj <= js) ? (int32_t)rj : -1;
+        a.accepted_tokens[oj] = t;
+        if (a.accept_index) a.accept_index[oj] = (jj <= js) ? (int32_t)rj : -1;
         if (a.logprobs) {
           float lp = 0.f;
           if (jj <= js && t >= 0 && (int64_t)t < V) {
@@ -1076,7 +1110,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
             lp = (SVec<E>::at(xj, t) - __ldcg(&a.ws.rowres[rj].M)) -
                  logf(__ldcg(&a.ws.rowres[rj].S));
           }
-          a.logprobs[rj] = lp;
+          a.logprobs[oj] = lp;
         }
       }
       a.accept_length[req] = js + 1;
@@ -1601,11 +1635,12 @@ __global__ void __launch_bounds__(256) k_chain_resid(SampleArgs a) {
   __shared__ int32_t s_tok;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t b = blockIdx.x;
-  const int32_t D = a.D, R = a.R;
+  const CWin win = cwin(a, b);
+  const int32_t D = win.count - 1, DP = a.D, R = a.R;
   const int32_t L = __ldcg(&a.accept_length[b]);
   if (L < 1 || L > D) return;  // every draft accepted (the bonus is drawn), or unfinished
   const int32_t js = L - 1;
-  const int64_t row = b * R + js;
+  const int64_t row = win.first + js;  // the rejected row (packed), output position b R + js
   const RowRes* rp = a.ws.rowres + row;
   const float M = __ldcg(&rp->M);
   const int32_t am = __ldcg(&rp->am);
@@ -1615,7 +1650,7 @@ __global__ void __launch_bounds__(256) k_chain_resid(SampleArgs a) {
   if (kind != 0) {
     KeptRow kr;
     kr.load(rp, cknobs(a, b).T);
-    const float* qr = a.q + (b * D + js) * a.ld_q;
+    const float* qr = a.q + (b * DP + js) * a.ld_q;
     const int64_t V = a.V;
     // p''_i, and the residual weight of token i in fixed point
     auto pw = [&](int64_t i) -> float { return kr.prob(SVec<E>::at(xr, i), i); };
@@ -1677,12 +1712,13 @@ __global__ void __launch_bounds__(256) k_chain_resid(SampleArgs a) {
     }
   }
   if (tid == 0) {
-    a.accepted_tokens[row] = tok;
+    const int64_t oj = b * R + js;
+    a.accepted_tokens[oj] = tok;
     if (a.logprobs) {
       float lp = 0.f;
       if (tok >= 0 && (int64_t)tok < a.V)
         lp = (SVec<E>::at(xr, tok) - M) - logf(__ldcg(&a.ws.rowres[row].S));
-      a.logprobs[row] = lp;
+      a.logprobs[oj] = lp;
     }
   }
 }
@@ -1711,7 +1747,7 @@ cudaError_t launch_chain_t(const SampleArgs& a, cudaStream_t s) {
     e = cudaGetLastError();
   }
   if (e != cudaSuccess || !a.q) return e;
-  k_chain_resid<E><<<(unsigned)(a.rows / a.R), 256, 0, s>>>(a);
+  k_chain_resid<E><<<(unsigned)a.nreq, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

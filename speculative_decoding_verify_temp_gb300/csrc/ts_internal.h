@@ -69,6 +69,7 @@ struct Workspace {
   uint32_t* order;    // [rows] the chain kernel's rows in claim order (cost tiers)
   uint32_t* creq;     // [batch] the chain kernel's per-request finished-row counts
   int32_t* slen;      // [batch] single-step sampling: the chain kernel's accept lengths
+  uint32_t* rreq;     // [rows] ragged verification: the request of each packed row
   uint64_t* cand;     // [rows * cand_splits * kSTopK] per-row range masses of the row
                       // kernel (vocab > 0 only)
   int64_t cand_splits;
@@ -108,6 +109,10 @@ struct RowStatArgs {
   const int32_t* lp_tokens;
   float* lp_out;
   Workspace ws;
+  // greedy verify of a ragged batch: request b owns the packed rows qo[b] .. qo[b+1] - 1
+  // (at most D + 1; rows = their total); NULL: rows b (D+1) ..
+  const int32_t* qo;
+  int64_t nreq;
 };
 
 cudaError_t launch_rowstat(const RowStatArgs& a, int bf16, cudaStream_t s);
@@ -201,6 +206,10 @@ struct SampleArgs {
   float* probs_out;      // sampling: the kept distribution of each row, or NULL
   int64_t ld_probs;
   const int64_t* probs_row;  // destination row of each row's distribution, or NULL
+  // ragged verification: request b owns the packed rows qo[b] .. qo[b + 1] - 1 (at most
+  // R of them); NULL: request b owns rows b R .. b R + R - 1. Outputs stay [nreq, R].
+  const int32_t* qo;
+  int64_t nreq;
 };
 
 // The row kernel in its renorm mode (fp32 probability rows, 16-byte aligned).

@@ -268,25 +268,43 @@ __global__ void __launch_bounds__(kStreamThreads) k_rowstat(RowStatArgs a) {
         a.ws.rowres[row] = RowRes{m, am, s, -1, 0, {0, 0, 0}};
         __threadfence();
         const int32_t R = a.D + 1;
-        const int64_t b = row / R;
-        const uint32_t prev = atomicAdd(&a.ws.reqcnt[b], 1u);
-        if (prev == (uint32_t)R - 1) {
+        // the request's window of rows [first, first + cnt): a ragged batch finds it by
+        // bisection of qo (a window that does not fit is left unverified)
+        int64_t b = row / R, first = b * R;
+        int32_t cnt = R;
+        if (a.qo) {
+          int64_t lo = 0, hi = a.nreq - 1;
+          while (lo < hi) {
+            const int64_t mid = (lo + hi + 1) / 2;
+            if ((int64_t)a.qo[mid] <= row) lo = mid;
+            else hi = mid - 1;
+          }
+          b = lo;
+          first = a.qo[b];
+          const int64_t e = a.qo[b + 1];
+          cnt = (first <= row && row < e && e <= a.rows && e - first <= R) ? (int32_t)(e - first)
+                                                                             : 0;
+        }
+        const int32_t Db = cnt - 1;
+        const uint32_t prev = cnt > 0 ? atomicAdd(&a.ws.reqcnt[b], 1u) : 0u;
+        if (cnt > 0 && prev == (uint32_t)Db) {
           __threadfence();
           a.ws.reqcnt[b] = 0;
-          int32_t js = a.D;
-          for (int32_t j = 0; j < a.D; ++j) {
-            if (a.draft_tokens[b * a.D + j] != __ldcg(&a.ws.rowres[b * R + j].am)) {
+          int32_t js = Db;
+          for (int32_t j = 0; j < Db; ++j) {
+            if (a.draft_tokens[b * a.D + j] != __ldcg(&a.ws.rowres[first + j].am)) {
               js = j;
               break;
             }
           }
           for (int32_t j = 0; j < R; ++j) {
-            const int64_t rj = b * R + j;
+            const int64_t oj = b * R + j;  // the padded output position
+            const int64_t rj = first + j;  // its packed row (j <= js)
             int32_t tok = -1;
             if (j < js) tok = a.draft_tokens[b * a.D + j];
             else if (j == js) tok = __ldcg(&a.ws.rowres[rj].am);
-            a.accepted_tokens[rj] = tok;
-            if (a.accept_index) a.accept_index[rj] = (j <= js) ? (int32_t)rj : -1;
+            a.accepted_tokens[oj] = tok;
+            if (a.accept_index) a.accept_index[oj] = (j <= js) ? (int32_t)rj : -1;
             if (a.logprobs) {
               float lp = 0.f;
               if (j <= js) {
@@ -294,7 +312,7 @@ __global__ void __launch_bounds__(kStreamThreads) k_rowstat(RowStatArgs a) {
                 lp = (Vec<E>::scalar(xj, tok) - __ldcg(&a.ws.rowres[rj].M)) -
                      logf(__ldcg(&a.ws.rowres[rj].S));
               }
-              a.logprobs[rj] = lp;
+              a.logprobs[oj] = lp;
             }
           }
           a.accept_length[b] = js + 1;

@@ -53,6 +53,8 @@ class ChainArgs(ctypes.Structure):
         ("min_p", ctypes.c_void_p),
         ("threshold_single", ctypes.c_float),
         ("threshold_acc", ctypes.c_float),
+        ("qo_indptr", ctypes.c_void_p),
+        ("total_rows", ctypes.c_int64),
     ]
 
 
@@ -122,6 +124,9 @@ def load():
                                      ctypes.c_size_t, P]
     L.ts_gather_logprobs.restype = st
     L.ts_sample_from_logits.argtypes = [ctypes.POINTER(SampleArgs), P, ctypes.c_size_t, P]
+    L.ts_verify_chain_greedy_ragged.argtypes = [P, ctypes.c_int, i64, i32, i64, i64, P, i64, P,
+                                                P, P, P, P, P, ctypes.c_size_t, P]
+    L.ts_verify_chain_greedy_ragged.restype = st
     L.ts_sample_from_logits.restype = st
     _lib = L
     return L
@@ -225,15 +230,36 @@ def verify_chain_greedy(target_logits, D: int, draft_tokens, workspace=None, *,
     return dict(accepted_tokens=acc, accept_length=alen, accept_index=aidx, logprobs=lp)
 
 
+def verify_chain_greedy_ragged(target_logits, D: int, qo_indptr, draft_tokens, workspace=None,
+                               *, accept_index: bool = True, logprobs: bool = True,
+                               outputs=None, stream=None):
+    """Greedy verification of packed rows (request b owns rows qo_indptr[b] ..
+    qo_indptr[b+1] - 1, qo_indptr int32 [B+1] on the device); outputs [B, D+1]."""
+    rows, V, ld = _rows(target_logits)
+    R = D + 1
+    B = qo_indptr.numel() - 1
+    if workspace is None:
+        workspace = make_workspace(B, R, V, target_logits.device, stream)
+    acc, alen, aidx, lp = outputs or _chain_outputs(B, R, target_logits.device, accept_index,
+                                                    logprobs)
+    _check("ts_verify_chain_greedy_ragged", load().ts_verify_chain_greedy_ragged(
+        _p(target_logits), _dtype(target_logits), B, D, V, ld, _p(qo_indptr), rows,
+        _p(draft_tokens), _p(acc), _p(alen), _p(aidx), _p(lp), _p(workspace), workspace.numel(),
+        _stream(stream)))
+    return dict(accepted_tokens=acc, accept_length=alen, accept_index=aidx, logprobs=lp)
+
+
 def chain_spec_sampling(target, target_is_logits: bool, D: int, draft_tokens, *,
                         draft_probs=None, temperature=None, top_k=None, top_p=None,
                         seed=None, offset=None, uniforms=None, workspace=None,
                         accept_index: bool = True, logprobs: bool = True, outputs=None,
                         stream=None, min_p=None, threshold_single: float = 1.0,
-                        threshold_acc: float = 1.0):
+                        threshold_acc: float = 1.0, qo_indptr=None):
+    """Chain sampling of [B*(D+1), V] rows, or, with qo_indptr (int32 [B+1] on the
+    device), of packed rows: request b owns rows qo_indptr[b] .. qo_indptr[b+1] - 1."""
     rows, V, ld = _rows(target)
     R = D + 1
-    B = rows // R
+    B = rows // R if qo_indptr is None else qo_indptr.numel() - 1
     if workspace is None:
         workspace = make_workspace(B, R, V, target.device, stream)
     acc, alen, aidx, lp = outputs or _chain_outputs(B, R, target.device, accept_index, logprobs)
@@ -260,6 +286,9 @@ def chain_spec_sampling(target, target_is_logits: bool, D: int, draft_tokens, *,
     a.min_p = None if min_p is None else min_p.data_ptr()
     a.threshold_single = float(threshold_single)
     a.threshold_acc = float(threshold_acc)
+    if qo_indptr is not None:
+        a.qo_indptr = qo_indptr.data_ptr()
+        a.total_rows = rows
     _check("ts_chain_spec_sampling", load().ts_chain_spec_sampling(
         ctypes.byref(a), _p(workspace), workspace.numel(), _stream(stream)))
     return dict(accepted_tokens=acc, accept_length=alen, accept_index=aidx, logprobs=lp)

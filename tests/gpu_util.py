@@ -24,12 +24,14 @@ def dev(a):
 
 
 def compare_chain(gpu: dict, ref: dict, dtype: str = "f32", max_boundary_frac: float = 0.05,
-                  check_logprobs: bool = True):
+                  check_logprobs: bool = True, row_base=None):
     """Exact token/length/index parity on every request the oracle does not flag as a
     boundary case; logprobs within tolerance on the emitted positions. Returns the
     number of boundary requests. A draw over a flat distribution of V tokens lands
     within 1e-6 of a CDF edge with probability about 2e-6 * V, so the bound on the
-    count of boundary requests is a sanity bound, not part of the parity rule."""
+    count of boundary requests is a sanity bound, not part of the parity rule.
+    row_base: the first (packed) row of each request of a ragged batch; accept_index holds
+    row_base[b] + j (rectangular: b * R + j)."""
     acc = gpu["accepted_tokens"].cpu().numpy()
     alen = gpu["accept_length"].cpu().numpy()
     margin = ref.get("margin")
@@ -45,7 +47,8 @@ def compare_chain(gpu: dict, ref: dict, dtype: str = "f32", max_boundary_frac: f
     assert ((acc >= 0) == (pos < alen[:, None])).all()
     if gpu.get("accept_index") is not None:
         aidx = gpu["accept_index"].cpu().numpy()
-        want = np.where(pos < alen[:, None], np.arange(len(alen))[:, None] * R + pos, -1)
+        base = np.arange(len(alen)) * R if row_base is None else np.asarray(row_base)
+        want = np.where(pos < alen[:, None], base[:, None] + pos, -1)
         np.testing.assert_array_equal(aidx, want)
     if check_logprobs and gpu.get("logprobs") is not None and ref.get("logprobs") is not None:
         lp = gpu["logprobs"].cpu().numpy()
@@ -106,3 +109,40 @@ def oracle_all(fn, rows, bf16, R, args=(), per_request=None, static=None, procs=
         return {k: (None if parts[0][k] is None else np.concatenate([p[k] for p in parts]))
                 for k in parts[0]}
     return tuple(np.concatenate([p[i] for p in parts]) for i in range(len(parts[0])))
+
+
+def _ragged_worker(task):
+    import oracle
+    from speculative_decoding_verify_temp_gb300 import synth
+
+    fn, rows, bf16, D, qo, pre, drafts, kw = task
+    x = synth.f32_from_bf16_bits(rows) if bf16 else rows
+    return getattr(oracle, fn)(x, *pre, D, qo, drafts, **kw)
+
+
+def oracle_ragged_all(fn, rows, bf16, D, qo, args=(), per_request=None, static=None, procs=None):
+    """oracle.<fn> (a ragged call: fn(x, [is_logits,] D, qo_indptr, drafts, **kw)) over every
+    request of a packed launch, requests split over the host cores with their packed rows
+    (qo rebased per slice). args: (is_logits,) or () before D; per_request: keyword
+    arrays of one entry (or row of entries) per request, drafts included under
+    "draft_tokens"; accept_index comes back as packed row numbers of the whole launch."""
+    B = len(qo) - 1
+    procs = procs or max(1, min(os.cpu_count() or 1, 32))
+    per_request = dict(per_request or {})
+    drafts = per_request.pop("draft_tokens")
+    tasks, bases = [], []
+    for b0, b1 in _slices(B, procs):
+        r0, r1 = int(qo[b0]), int(qo[b1])
+        sub_qo = (np.asarray(qo[b0:b1 + 1]) - r0).astype(np.int32)
+        kw = {k: (None if v is None else v[b0:b1]) for k, v in per_request.items()}
+        kw.update(static or {})
+        tasks.append((fn, np.ascontiguousarray(rows[r0:r1]), bf16, D, sub_qo, tuple(args),
+                      np.ascontiguousarray(drafts[b0:b1]), kw))
+        bases.append(r0)
+    with multiprocessing.get_context("spawn").Pool(len(tasks)) as pool:
+        parts = pool.map(_ragged_worker, tasks)
+    for p, r0 in zip(parts, bases):
+        ai = p["accept_index"]
+        p["accept_index"] = np.where(ai >= 0, ai + r0, ai)
+    return {k: (None if parts[0].get(k) is None else np.concatenate([p[k] for p in parts]))
+            for k in parts[0]}
