@@ -500,6 +500,8 @@ def _oracle_task(task):
         return oracle.gumbel_max_sample(x, *args, **kw)
     if kind == "greedy":
         return oracle.verify_chain_greedy(x, *args, **kw)
+    if kind == "sample":
+        return oracle.sample_from_logits(x, *args, **kw)
     return oracle.chain_spec_sampling(x, *args, **kw)
 
 
@@ -531,9 +533,13 @@ def leg_parity(kind, x, is_bits, R, args_req, kw_req, gpu, extra=None):
                       for n, v in extra.items()})
         tasks.append((kind, xa, is_bits, a, k))
     parts = _oracle_pool().map(_oracle_task, tasks)
-    if kind == "gumbel":
-        want = np.concatenate([p[0] for p in parts])
-        marg = np.concatenate([p[1] for p in parts])
+    if kind in ("gumbel", "sample"):
+        if kind == "gumbel":
+            want = np.concatenate([p[0] for p in parts])
+            marg = np.concatenate([p[1] for p in parts])
+        else:
+            want = np.concatenate([p["tokens"] for p in parts])
+            marg = np.concatenate([p["margin"] for p in parts])
         ok = marg > 1e-6
         mism = int((gpu[0] != want)[ok].sum())
         return {"rows": int(len(want)), "mismatches_outside_boundary": mism,
@@ -662,6 +668,68 @@ def run_legs(args, d, logits, device, tv, synth, peak):
                                                     flush=flush)
             rec(name, ms, nr, nr * Vs * 2, **more)
         del gl
+    # single-step sampling of the same logits (2048 rows, joint top-k/top-p order)
+    kn_rows = {k: torch.from_numpy(np.repeat(d[k], R)).to(device)
+               for k in ("temperature", "top_k", "top_p")}
+    name = "sample_joint_R2048_V201088_bf16"
+    if want(name):
+        wss = tv.make_workspace(rows, 1, V, device)
+        stok = torch.empty(rows, dtype=torch.int32, device=device)
+        ms = time_device(lambda: tv.sample_from_logits(logits, R, **kn_rows, joint=True, seed=seed,
+                                                       offset=off, workspace=wss, out=stok),
+                         steps, warm, device)
+        rec(name, ms, rows, rows * V * 2, launches=2)
+        if parity:
+            legs[name]["parity"] = leg_parity(
+                "sample", bits, True, R, [R],
+                {"temperature": Trow_np, "top_k": np.repeat(d["top_k"], R).astype(np.int32),
+                 "top_p": np.repeat(d["top_p"], R).astype(np.float32), "joint": True,
+                 "seed": d["seed"], "offset": d["offset"]}, (host(stok),))
+    # draft-side sampling with the kept distributions stored (min_p on), 2048 rows
+    name = "draft_sample_with_probs_R2048_V201088_bf16"
+    if want(name):
+        wss = tv.make_workspace(rows, 1, V, device)
+        stok = torch.empty(rows, dtype=torch.int32, device=device)
+        pbuf = torch.empty((rows, V), dtype=torch.float32, device=device)
+        mp = torch.full((rows,), 0.01, dtype=torch.float32, device=device)
+        ms = time_device(lambda: tv.sample_from_logits(logits, R, **kn_rows, min_p=mp, seed=seed,
+                                                       offset=off, workspace=wss, out=stok,
+                                                       probs=pbuf),
+                         steps, warm, device)
+        rec(name, ms, rows, rows * V * (2 + 4), launches=3)
+        del pbuf
+    # the verify step with min_p and relaxed acceptance thresholds
+    name = "verify_step_min_p_relaxed_B512_D3_V201088_bf16"
+    if want(name):
+        outs = tv._chain_outputs(B, R, device, False, False)
+        mpr = torch.full((B,), 0.01, dtype=torch.float32, device=device)
+        kw = dict(temperature=torch.from_numpy(d["temperature"]).to(device),
+                  top_k=torch.from_numpy(d["top_k"]).to(device),
+                  top_p=torch.from_numpy(d["top_p"]).to(device), seed=seed, offset=off,
+                  workspace=tv.make_workspace(B, R, V, device), outputs=outs, min_p=mpr,
+                  threshold_single=0.9, threshold_acc=0.5)
+        ms = time_device(lambda: tv.chain_spec_sampling(logits, True, D, drafts, **kw), steps,
+                         warm, device)
+        rec(name, ms, rows, rows * V * 2, launches=2)
+    # ragged verification: windows of 1 to 4 rows of the step's logits
+    name = "verify_ragged_B512_D3_V201088_bf16"
+    if want(name):
+        rng = np.random.default_rng(512)
+        lens = rng.integers(1, D + 2, B)
+        qo_np = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        sel = np.concatenate([np.arange(b * R, b * R + lens[b]) for b in range(B)])
+        packed = logits[torch.from_numpy(sel).to(device)]
+        qo = torch.from_numpy(qo_np).to(device)
+        outs = tv._chain_outputs(B, R, device, False, False)
+        kw = dict(temperature=torch.from_numpy(d["temperature"]).to(device),
+                  top_k=torch.from_numpy(d["top_k"]).to(device),
+                  top_p=torch.from_numpy(d["top_p"]).to(device), seed=seed, offset=off,
+                  workspace=tv.make_workspace(B, R, V, device), outputs=outs, qo_indptr=qo)
+        ms = time_device(lambda: tv.chain_spec_sampling(packed, True, D, drafts, **kw), steps,
+                         warm, device)
+        nrow = int(qo_np[-1])
+        rec(name, ms, nrow, nrow * V * 2, launches=2)
+        del packed
     # softmax with temperature, fp32 probabilities out
     name = "softmax_B512_R4_V201088_bf16"
     if want(name):

@@ -2,17 +2,20 @@
 // flashinfer.py verify(): sampling_argmax for greedy requests; softmax with temperature,
 // fused top-k/top-p renorm and chain_speculative_sampling_target_only for the others).
 //
-// Two launches per call:
+// Two launches per call (three with a probability output, one more with draft
+// probabilities):
 //  - k_chain_plan (one CTA) orders the rows by cost tier (top-p and general rows first,
 //    then large top-k rows, then the other sampled rows, greedy rows last), so that the
 //    step ends on short rows, and clears the per-launch state: the row claim counter, the
 //    per-request row counts and accept_length (0 until a request's chain is written).
-//  - k_chain: persistent CTAs (two an SM) of 8 warps, all of which compute. Thread 0 also
-//    keeps a ring of kCNSt shared-memory stages of 16 KB filled with bulk copies that
-//    complete on mbarriers: after its warp has read stage g it refills the slot of stage
-//    g - 1 (once every warp has released it), claiming rows from the planned order one
-//    row ahead. Each warp copies its four 16-byte vectors of a stage to registers, frees
-//    the slot, and keeps running row state in a loop specialised for the row's kind:
+//    A ragged batch (qo_indptr) schedules each request's own window of packed rows.
+//  - k_chain: persistent CTAs (two an SM) of a producer warp and 7 compute warps. The
+//    producer keeps a ring of kCNSt shared-memory stages of 14 KB filled with bulk copies
+//    that complete on mbarriers, and claims the next row from the planned order when the
+//    current one has kCNSt + 1 stages left to issue (the claim's latency hides behind
+//    them, and a CTA never holds more than its current and next rows). Each compute warp
+//    copies its four 16-byte vectors of a stage to registers, releases the slot, and
+//    keeps running row state in a loop specialised for the row's kind:
 //     - every row: maximum and its first token id (lowest id among equal values), and
 //       the temperature-1 log-sum-exp when logprobs are asked for;
 //     - top-k (k <= kSTopK): a candidate list in shared memory above a threshold: first a
@@ -33,7 +36,14 @@
 //       the elements within them, resolved exactly; then the draw.
 //    Rows the summaries cannot serve (top_k above kSTopK, candidate overflow, a top-p
 //    crossing outside its windows) take a general path: radix selections over the whole
-//    row, read again from memory.
+//    row, read again from memory. So do rows with min_p and no top-k. Top-k rows apply
+//    min_p to their list, and with the joint order measure top_p on the whole row's mass
+//    (one more pass over the row).
+//  - k_chain_resid (draft probabilities): the residual draw of each rejected row.
+//  - k_chain_probs (single-step sampling with a probability output): each row's kept
+//    distribution, rebuilt from the row's record.
+// The same launches serve single-step sampling (TokenSpeed sample(); TensorRT-LLM
+// fused_sample_from_logits_with_probs) as chains of one row and no draft.
 //
 // Weights are 2^((x - M) log2(e) / T) for the row maximum M; masses that decide a
 // selection are sums of floor(w * 2^40); composite keys order tokens by value, then by
@@ -93,8 +103,8 @@ struct CKnobs {
 };
 
 // The request's knobs and the way its rows are served. top_p <= 0 keeps only the argmax,
-// which is the greedy distribution. min_p (clamped to [0, 1]), the joint order with both
-// top-k and top-p on, and a probability output are served by the general path.
+// which is the greedy distribution. min_p (clamped to [0, 1]) on rows without top-k is
+// served by the general path.
 __device__ __forceinline__ CKnobs cknobs(const SampleArgs& a, int64_t req) {
   CKnobs kn;
   kn.T = a.temperature ? a.temperature[req] : 1.f;
@@ -106,9 +116,7 @@ __device__ __forceinline__ CKnobs cknobs(const SampleArgs& a, int64_t req) {
   else if (tk) kn.kind = (kn.k <= kSTopK) ? kCTopK : kCGeneral;
   else if (kn.tp < 1.f) kn.kind = (kn.tp > 0.f) ? kCTopP : kCGreedy;
   else kn.kind = kCPlain;
-  if (kn.kind != kCGreedy &&
-      (kn.mp > 0.f || a.probs_out != nullptr || (a.joint && tk && kn.tp < 1.f)))
-    kn.kind = kCGeneral;
+  if ((kn.kind == kCTopP || kn.kind == kCPlain) && kn.mp > 0.f) kn.kind = kCGeneral;
   return kn;
 }
 
@@ -1176,7 +1184,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
     // the row. Zr is the ranges' total.
     const int64_t e1max = (int64_t)nst * kCW;  // the row's ranges
     auto draw_ranges = [&](uint64_t mine, uint64_t ex, uint64_t Zr, int64_t e0, int64_t e1,
-                           int32_t acc, auto&& wgt) {
+                           int32_t acc, int32_t kset, uint64_t Cf, uint64_t Zf, auto&& wgt) {
       uint64_t t = (uint64_t)((double)uD * (double)Zr);
       if (t >= Zr) t = Zr - 1;
       if (mine > 0 && ex <= t && t < ex + mine) {
@@ -1198,7 +1206,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
         const int64_t es = min((int64_t)(sm.res_u % (uint64_t)e1max), e1max - 1);
         const int64_t v0 = (es / kCW) * (SE / N) + (es % kCW) * (kCVecs * 32);
         const int32_t tok = walk_range(v0, (float)sm.res_d, wgt);
-        if (lane == 0) finish_row(tok >= 0 ? tok : am, acc);
+        if (lane == 0) finish_row(tok >= 0 ? tok : am, acc, kset, Cf, Zf);
       }
     };
 
@@ -1214,9 +1222,15 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
       };
       auto gmass = [&](uint64_t c0) -> uint64_t {
         uint64_t sum = 0;
-        for (int i = tid; i < n; i += kCC) {
-          const uint64_t cc = gitem(i);
-          if (cc >= c0) sum += wcomp(cc);
+        for (int64_t vi = tid; vi < nvall; vi += kCC) {
+          float xv[N];
+          load_vec(vi, xv);
+#pragma unroll
+          for (int q = 0; q < N; ++q) {
+            const int64_t i = vi * N + q;
+            const uint64_t cc = comp_key(fkey(xv[q]), (uint32_t)i);
+            if (i < n && cc >= c0) sum += wfn(xv[q]);
+          }
         }
         uint64_t tot;
         (void)sel::excl_scan<kCC, CBar>(sum, sm.sc, tot);
@@ -1225,7 +1239,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
       const bool tk = k > 0 && (int64_t)k < V;
       uint64_t C = 1;  // every composite key is at least 1
       if (tk)
-        C = sel::radix_adaptive<kCC, false, CBar>(
+        C = sel::radix_adaptive<kCC, false, CBar, 4>(
             n, gitem, 1ull, (uint64_t)k, [](uint64_t) { return (uint64_t)1; }, lowv, sm.sc);
       uint64_t Z = gmass(C);
       if (kn.tp < 1.f) {
@@ -1236,7 +1250,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
         const double want = ceil((double)kn.tp * (double)Zref);
         const uint64_t P = (want > (double)Zref) ? Zref : (uint64_t)want;
         const uint64_t Cp =
-            sel::radix_adaptive<kCC, true, CBar>(n, gitem, jt ? 1ull : C, P, wcomp, lowv, sm.sc);
+            sel::radix_adaptive<kCC, true, CBar, 4>(n, gitem, jt ? 1ull : C, P, wcomp, lowv, sm.sc);
         C = max(C, Cp);
         Z = gmass(C);
       }
@@ -1245,9 +1259,12 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
         // form a top segment, so the smallest passing key bounds them (the argmax passes)
         const float thr = kn.T * logf(kn.mp);
         uint32_t kmin = 0xFFFFFFFFu;
-        for (int i = tid; i < n; i += kCC) {
-          const float v = SVec<E>::at(xr, i);
-          if (v - M >= thr) kmin = min(kmin, fkey(v));
+        for (int64_t vi = tid; vi < nvall; vi += kCC) {
+          float xv[N];
+          load_vec(vi, xv);
+#pragma unroll
+          for (int q = 0; q < N; ++q)
+            if (xv[q] - M >= thr) kmin = min(kmin, fkey(xv[q]));
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
@@ -1278,13 +1295,33 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
         if (t >= Zr) t = Zr - 1;
         const int idx_sh[3] = {16, 8, 0};
         uint64_t gsel = 0;
-        (void)sel::radix<kCC, true, CBar>(
+        (void)sel::radix<kCC, true, CBar, 4>(
             n, gitem, C, t + 1,
             [&](uint64_t cc) { return ((int32_t)comp_token(cc) == x) ? 0ull : wcomp(cc); },
             idx_sh, 3, sm.sc, &gsel);
         tok = (int32_t)comp_token(gsel);
       }
       if (tid == 0) finish_row(tok, acc, 1, C, Z);
+    };
+
+    // Top-k rows with the joint order measure top_p on the whole row's mass (one more
+    // pass over the row, every compute thread); with min_p they keep only the tokens at
+    // or above the value bound thr_v (x - M >= T ln(min_p)).
+    const bool jrow = a.joint && kn.kind == kCTopK && kn.tp < 1.f && !bad;
+    uint64_t Zall = 0;
+    if (jrow) {
+      uint64_t sum = 0;
+      for (int64_t vi = tid; vi < nvall; vi += kCC) {
+        float xv[N];
+        load_vec(vi, xv);
+#pragma unroll
+        for (int q = 0; q < N; ++q) sum += wfn(xv[q]);
+      }
+      (void)sel::excl_scan<kCC, CBar>(sum, sm.sc, Zall);
+    }
+    const float mp_thr = kn.mp > 0.f ? kn.T * logf(kn.mp) : -INFINITY;
+    auto mp_keep = [&](uint64_t cc) -> bool {
+      return !(kn.mp > 0.f) || key_to_value((uint32_t)(cc >> kIdxBits)) - M >= mp_thr;
     };
 
     // ---- finish the row ---------------------------------------------------------------------
@@ -1340,9 +1377,9 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
         if (skip_draw) {
           if (tid == 0) finish_row(-1, acc, 3, C, Zr + wx);
         } else if (Zr == 0) {
-          if (tid == 0) finish_row((wx > 0) ? x : am, acc);
+          if (tid == 0) finish_row((wx > 0) ? x : am, acc, 3, C, Zr + wx);
         } else {
-          draw_ranges(mine, ex, Zr, e0, e1, acc, [&](float v, int64_t gidx) -> float {
+          draw_ranges(mine, ex, Zr, e0, e1, acc, 3, C, Zr + wx, [&](float v, int64_t gidx) -> float {
             if (gidx == (int64_t)x || v == -INFINITY || !kept(v, gidx)) return 0.f;
             return ex2((v - M) * sl2);
           });
@@ -1373,17 +1410,20 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
         }
         const uint64_t Zk = warp_scan_incl(incl);
         // top-p within the top k: rank r kept iff r = 0 or the mass before it is below P
+        // (P a fraction of the top-k mass, or of the whole row's with the joint order);
+        // min_p then keeps the ranks whose value passes its bound
         uint64_t P = Zk;
         if (kn.tp < 1.f) {
-          const double want = ceil((double)kn.tp * (double)Zk);
-          P = (want > (double)Zk) ? Zk : (want > 0.0 ? (uint64_t)want : 0ull);
+          const uint64_t Zref = jrow ? Zall : Zk;
+          const double want = ceil((double)kn.tp * (double)Zref);
+          P = (want > (double)Zref) ? Zref : (want > 0.0 ? (uint64_t)want : 0ull);
         }
         uint64_t Z = 0, wx = 0;
         bool kept[kCSmallE];
 #pragma unroll
         for (int e = 0; e < kCSmallE; ++e) {
           const int i = e * 32 + lane;
-          kept[e] = i < nl && i < k && (i == 0 || incl[e] - w[e] < P);
+          kept[e] = i < nl && i < k && (i == 0 || (incl[e] - w[e] < P && mp_keep(v[e])));
           const uint32_t tk = comp_token(v[e]);
           if (kept[e]) {
             Z += w[e];
@@ -1465,10 +1505,35 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
       };
       uint64_t C = Ck, Z = mass_from(Ck);
       if (kn.tp < 1.f) {
-        const double want = ceil((double)kn.tp * (double)Z);
-        const uint64_t P = (want > (double)Z) ? Z : (want > 0.0 ? (uint64_t)want : 0ull);
-        C = sel::radix_adaptive<kCC, true, CBar>(nl, item, Ck, P, wcomp, lowv, sm.sc);
-        Z = mass_from(C);
+        // top-k first: the nucleus of the top-k set; joint: the nucleus of the whole row
+        // (its mass Zall), which cuts inside the top k only if P is within their mass
+        const uint64_t Zref = jrow ? Zall : Z;
+        const double want = ceil((double)kn.tp * (double)Zref);
+        const uint64_t P = (want > (double)Zref) ? Zref : (want > 0.0 ? (uint64_t)want : 0ull);
+        if (P <= Z) {
+          C = sel::radix_adaptive<kCC, true, CBar>(nl, item, Ck, P, wcomp, lowv, sm.sc);
+          Z = mass_from(C);
+        }
+      }
+      if (kn.mp > 0.f) {
+        // min_p: the smallest kept list value that passes the bound (the argmax does)
+        uint32_t kmin = fkey(M);
+        for (int i = tid; i < nl; i += kCC) {
+          const uint64_t cc = sm.w.list[i];
+          if (cc >= C && mp_keep(cc)) kmin = min(kmin, (uint32_t)(cc >> kIdxBits));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+        if (lane == 0) sm.redi[warp] = (int32_t)kmin;
+        cbar();
+        uint32_t km = 0xFFFFFFFFu;
+        for (int w2 = 0; w2 < kCW; ++w2) km = min(km, (uint32_t)sm.redi[w2]);
+        cbar();
+        const uint64_t Cm = comp_key(km, kIdxMax);
+        if (Cm > C) {
+          C = Cm;
+          Z = mass_from(C);
+        }
       }
       uint64_t wx = 0;
       if (xvalid && comp_key(fkey(vx), (uint32_t)x) >= C) wx = wfn(vx);
@@ -1508,10 +1573,11 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
       const double ex = excl_scan_f64_t<kCW, CBar>(mine, sm.dscan, Zr);
       const double wx = xvalid ? (double)ex2((vx - M) * sl2) : 0.0;
       const int32_t acc = accept(Zr + wx, wx);
+      const uint64_t Zfx = (uint64_t)((Zr + wx) * 1099511627776.0);
       if (skip_draw) {
-        if (tid == 0) finish_row(-1, acc, 2, 1ull, (uint64_t)((Zr + wx) * 1099511627776.0));
+        if (tid == 0) finish_row(-1, acc, 2, 1ull, Zfx);
       } else if (!(Zr > 0.0)) {
-        if (tid == 0) finish_row((wx > 0.0) ? x : am, acc);
+        if (tid == 0) finish_row((wx > 0.0) ? x : am, acc, 2, 1ull, Zfx);
       } else {
         const double t = (double)uD * Zr;
         if (tid == 0) sm.owner = -1;
@@ -1557,7 +1623,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
           const int32_t tok = walk_range(v0, (float)sm.res_d, [&](float v, int64_t gidx) -> float {
             return (gidx == (int64_t)x || v == -INFINITY) ? 0.f : ex2((v - em) * sl2);
           });
-          if (lane == 0) finish_row(tok >= 0 ? tok : am, acc);
+          if (lane == 0) finish_row(tok >= 0 ? tok : am, acc, 2, 1ull, Zfx);
         }
       }
     }

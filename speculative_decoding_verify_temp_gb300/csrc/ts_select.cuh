@@ -10,6 +10,7 @@
 namespace tsv {
 namespace sel {
 
+
 // Barrier policies: the whole CTA, or the 256 consumer threads of a warp-specialised CTA
 // (named barrier 1; the producer warp never takes part).
 struct BlockBar {
@@ -113,7 +114,10 @@ __device__ __forceinline__ void find_bin(Scratch& s, uint64_t above, uint64_t ta
 // selected iff it is >= the result. group_max receives the largest item of the final
 // digit group (the crossing item itself once the group holds one item); beyond is set
 // if the target lies past the eligible total (then every eligible item is selected).
-template <int NT, bool MASS, class Bar = BlockBar, class Item, class WFn>
+//
+// kU: items a thread takes at a time, loaded before any of them is counted (items read
+// from global memory then have kU loads in flight).
+template <int NT, bool MASS, class Bar = BlockBar, int kU = 1, class Item, class WFn>
 __device__ uint64_t radix(int n, Item item, uint64_t lo_key, uint64_t target, WFn wfn,
                           const int* shifts, int nsh, Scratch& s, uint64_t* group_max = nullptr,
                           bool* beyond = nullptr) {
@@ -129,12 +133,17 @@ __device__ uint64_t radix(int n, Item item, uint64_t lo_key, uint64_t target, WF
       s.cnt[i] = 0;
     }
     Bar::sync();
-    for (int i = tid; i < n; i += NT) {
-      const uint64_t v = item(i);
-      if (v >= lo_key && (v & mask) == prefix) {
-        const int b = (int)((v >> sh) & 255u);
-        atomicAdd(&s.cnt[b], 1u);
-        if (MASS) add3(&s.m3[0][b], &s.m3[1][b], &s.m3[2][b], wfn(v));
+    for (int i0 = tid * kU; i0 < n; i0 += NT * kU) {
+      uint64_t v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) v[u] = (i0 + u < n) ? item(i0 + u) : 0ull;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        if (i0 + u < n && v[u] >= lo_key && (v[u] & mask) == prefix) {
+          const int b = (int)((v[u] >> sh) & 255u);
+          atomicAdd(&s.cnt[b], 1u);
+          if (MASS) add3(&s.m3[0][b], &s.m3[1][b], &s.m3[2][b], wfn(v[u]));
+        }
       }
     }
     Bar::sync();
@@ -161,10 +170,17 @@ __device__ uint64_t radix(int n, Item item, uint64_t lo_key, uint64_t target, WF
   }
   if (beyond) *beyond = all;
   unsigned long long mn = ~0ull, gx = 0;
-  for (int i = tid; i < n; i += NT) {
-    const uint64_t v = item(i);
-    if (v >= lo_key && (all || (v & mask) >= prefix) && v < mn) mn = v;
-    if (v >= lo_key && !all && (v & mask) == prefix && v > gx) gx = v;
+  for (int i0 = tid * kU; i0 < n; i0 += NT * kU) {
+    uint64_t vv[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) vv[u] = (i0 + u < n) ? item(i0 + u) : 0ull;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const uint64_t v = vv[u];
+      if (i0 + u >= n || v < lo_key) continue;
+      if ((all || (v & mask) >= prefix) && v < mn) mn = v;
+      if (!all && (v & mask) == prefix && v > gx) gx = v;
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -189,17 +205,23 @@ __device__ uint64_t radix(int n, Item item, uint64_t lo_key, uint64_t target, WF
   return r;
 }
 
-// AND and OR of the 32-bit values f(i) over i < n with pred(i), reduced over the block.
-template <int NT, class Bar, class F>
+// AND and OR of the 32-bit values f(i) over i < n with pred(i), reduced over the block
+// (kU items a thread at a time, as in radix).
+template <int NT, class Bar, int kU = 1, class F>
 __device__ __forceinline__ void block_and_or(int n, F f, Scratch& s, uint32_t& and_, uint32_t& or_) {
   constexpr int NW = NT / 32;
   uint32_t a = 0xFFFFFFFFu, o = 0u;
-  for (int i = threadIdx.x; i < n; i += NT) {
-    uint32_t v;
-    if (f(i, v)) {
-      a &= v;
-      o |= v;
-    }
+  for (int i0 = (int)threadIdx.x * kU; i0 < n; i0 += NT * kU) {
+    uint32_t v[kU];
+    bool ok[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) ok[u] = (i0 + u < n) && f(i0 + u, v[u]);
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (ok[u]) {
+        a &= v[u];
+        o |= v[u];
+      }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -267,12 +289,12 @@ __device__ uint32_t select_bound(int n, Key key, uint32_t k, int ndig, Scratch& 
 // digits start below the bits that all eligible items share, down to value bit
 // `lowvbit` (16 when the values are widened bf16, whose low key bits follow from the
 // high ones), then the three id digits.
-template <int NT, bool MASS, class Bar = BlockBar, class Item, class WFn>
+template <int NT, bool MASS, class Bar = BlockBar, int kU = 1, class Item, class WFn>
 __device__ uint64_t radix_adaptive(int n, Item item, uint64_t lo_key, uint64_t target, WFn wfn,
                                    int lowvbit, Scratch& s, uint64_t* group_max = nullptr,
                                    bool* beyond = nullptr) {
   uint32_t ka, ko;
-  block_and_or<NT, Bar>(
+  block_and_or<NT, Bar, kU>(
       n,
       [&](int i, uint32_t& v) {
         const uint64_t c = item(i);
@@ -294,7 +316,7 @@ __device__ uint64_t radix_adaptive(int n, Item item, uint64_t lo_key, uint64_t t
   shifts[ns++] = 16;
   shifts[ns++] = 8;
   shifts[ns++] = 0;
-  return radix<NT, MASS, Bar>(n, item, lo_key, target, wfn, shifts, ns, s, group_max, beyond);
+  return radix<NT, MASS, Bar, kU>(n, item, lo_key, target, wfn, shifts, ns, s, group_max, beyond);
 }
 
 }  // namespace sel
