@@ -36,9 +36,10 @@
 //       the elements within them, resolved exactly; then the draw.
 //    Rows the summaries cannot serve (top_k above kSTopK, candidate overflow, a top-p
 //    crossing outside its windows) take a general path: radix selections over the whole
-//    row, read again from memory. So do rows with min_p and no top-k. Top-k rows apply
-//    min_p to their list, and with the joint order measure top_p on the whole row's mass
-//    (one more pass over the row).
+//    row, read again from memory. Top-k rows apply min_p to their list, and with the
+//    joint order measure top_p on the whole row's mass (one more pass over the row);
+//    other rows with min_p take one more pass that keeps the tokens above its bound
+//    (top-p rows only when that bound lies above their nucleus cut).
 //  - k_chain_resid (draft probabilities): the residual draw of each rejected row.
 //  - k_chain_probs (single-step sampling with a probability output): each row's kept
 //    distribution, rebuilt from the row's record.
@@ -103,8 +104,7 @@ struct CKnobs {
 };
 
 // The request's knobs and the way its rows are served. top_p <= 0 keeps only the argmax,
-// which is the greedy distribution. min_p (clamped to [0, 1]) on rows without top-k is
-// served by the general path.
+// which is the greedy distribution. min_p is clamped to [0, 1].
 __device__ __forceinline__ CKnobs cknobs(const SampleArgs& a, int64_t req) {
   CKnobs kn;
   kn.T = a.temperature ? a.temperature[req] : 1.f;
@@ -116,7 +116,6 @@ __device__ __forceinline__ CKnobs cknobs(const SampleArgs& a, int64_t req) {
   else if (tk) kn.kind = (kn.k <= kSTopK) ? kCTopK : kCGeneral;
   else if (kn.tp < 1.f) kn.kind = (kn.tp > 0.f) ? kCTopP : kCGreedy;
   else kn.kind = kCPlain;
-  if ((kn.kind == kCTopP || kn.kind == kCPlain) && kn.mp > 0.f) kn.kind = kCGeneral;
   return kn;
 }
 
@@ -360,7 +359,49 @@ __global__ void __launch_bounds__(1024) k_chain_plan(SampleArgs a) {
   for (int64_t p = (int64_t)total + tid; p < a.rows; p += 1024) a.ws.order[p] = kNoRow;
 }
 
+// The min_p pass of a row (one warp a range at a time, ranges warp, warp + kCW, ...):
+// range e (stage e / kCW, warp e % kCW of it: kCVecs x 32 vectors) gets the sum of the
+// fixed-point weights of its tokens with x - M >= bound, the draft token x left out.
+// Returns the lane's smallest passing value key (at most fkey(M)). Kept out of line: it
+// runs once for a few rows, and inlined it would raise the register need of the
+// streaming loops.
 template <typename E>
+__device__ __noinline__ uint32_t minp_ranges(const E* xr, int64_t V, int64_t nranges, int SE,
+                                             float M, float bound, float sl2, int32_t x,
+                                             uint64_t* rowslots) {
+  constexpr int N = SVec<E>::N;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint4* rp = reinterpret_cast<const uint4*>(xr);
+  const int64_t nvr = V / N, nvall = (V + N - 1) / N;
+  uint32_t kmin = fkey(M);
+  for (int64_t e = warp; e < nranges; e += kCW) {
+    const int64_t v0 = (e / kCW) * (SE / N) + (e % kCW) * (kCVecs * 32);
+    uint64_t sum = 0;
+    for (int u = 0; u < kCVecs; ++u) {
+      const int64_t vi = v0 + u * 32 + lane;
+      if (vi >= nvall) continue;
+      float xv[N];
+      if (vi < nvr) {
+        SVec<E>::unpack(__ldcg(rp + vi), xv);
+      } else {
+        for (int q = 0; q < N; ++q) xv[q] = (vi * N + q < V) ? SVec<E>::at(xr, vi * N + q) : -INFINITY;
+      }
+#pragma unroll
+      for (int q = 0; q < N; ++q) {
+        if (!(xv[q] - M >= bound)) continue;
+        kmin = min(kmin, fkey(xv[q]));
+        if (vi * N + q != (int64_t)x) sum += fixw(ex2((xv[q] - M) * sl2));
+      }
+    }
+    sum = warp_sum_u64(sum);
+    if (lane == 0) rowslots[e] = sum;
+  }
+  return kmin;
+}
+
+// EXT: the kernel also serves min_p and the joint filter order (a separate
+// instantiation, so that calls without them run the smaller kernel).
+template <typename E, bool EXT>
 __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
   extern __shared__ __align__(128) unsigned char dsm[];
   constexpr int N = SVec<E>::N;
@@ -1210,6 +1251,61 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
       }
     };
 
+    // min_p: a token stays iff x - M >= T ln(min_p) (a value bound; the argmax passes)
+    const bool use_mp = EXT && kn.mp > 0.f;
+    const float mp_thr = use_mp ? kn.T * logf(kn.mp) : -INFINITY;
+    auto mp_keep = [&](uint64_t cc) -> bool {
+      return !use_mp || key_to_value((uint32_t)(cc >> kIdxBits)) - M >= mp_thr;
+    };
+    // The weight of a token in a draw over ranges (the draft token left out): top-p rows
+    // keep the sixteenths above dr_gh and those in dr_gl..dr_gh at or above the composite
+    // dr_C; min_p rows (dr_bound) keep the tokens above the value bound.
+    bool dr_bound = false;
+    uint64_t dr_C = 0;
+    int dr_gh = 0, dr_gl = 0;
+    auto dr_wgt = [&](float v, int64_t gidx) -> float {
+      if (gidx == (int64_t)x || v == -INFINITY) return 0.f;
+      if (dr_bound) {
+        if (!(v - M >= mp_thr)) return 0.f;
+      } else {
+        const int gx = six_i(v);
+        if (!(gx > dr_gh || (gx >= dr_gl && comp_key(fkey(v), (uint32_t)gidx) >= dr_C))) return 0.f;
+      }
+      return ex2((v - M) * sl2);
+    };
+    // min_p without top-k: the kept set is every token with x - M >= T ln(min_p) (top-p
+    // rows take this path when that bound lies above their nucleus cut). One pass over
+    // the row: each warp sums the fixed-point weights of the passing tokens of its ranges
+    // (the draft token left out) into the range slots, and notes the smallest passing
+    // value; then the accept test and the draw over the ranges, as for top-p rows.
+    auto minp_path = [&](auto) {  // generic: instantiated only where called (EXT)
+      const int64_t E_ = (int64_t)nst * kCW;
+      uint32_t kmin = minp_ranges<E>(xr, V, E_, SE, M, mp_thr, sl2, x, rowslots);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+      if (lane == 0) sm.redi[warp] = (int32_t)kmin;
+      cbar();
+      uint32_t km = 0xFFFFFFFFu;
+      for (int w2 = 0; w2 < kCW; ++w2) km = min(km, (uint32_t)sm.redi[w2]);
+      const uint64_t Cm = comp_key(km, kIdxMax);
+      const int64_t per = (E_ + kCC - 1) / kCC;
+      const int64_t e0 = min(E_, (int64_t)tid * per), e1 = min(E_, e0 + per);
+      uint64_t mine = 0;
+      for (int64_t e = e0; e < e1; ++e) mine += __ldcg(rowslots + e);
+      uint64_t Zr;
+      const uint64_t ex = sel::excl_scan<kCC, CBar>(mine, sm.sc, Zr);
+      const uint64_t wx = (xvalid && vx - M >= mp_thr) ? wfn(vx) : 0ull;
+      const int32_t acc = accept((double)(Zr + wx), (double)wx);
+      if (skip_draw) {
+        if (tid == 0) finish_row(-1, acc, 1, Cm, Zr + wx);
+      } else if (Zr == 0) {
+        if (tid == 0) finish_row((wx > 0) ? x : am, acc, 1, Cm, Zr + wx);
+      } else {
+        dr_bound = true;
+        draw_ranges(mine, ex, Zr, e0, e1, acc, 1, Cm, Zr + wx, dr_wgt);
+      }
+    };
+
     // The general path for the rows the streamed summaries cannot serve (top_k above
     // kSTopK, candidate overflow, a top-p crossing outside its windows): radix selections
     // over the whole row, read again from memory for every digit, in the order top-k,
@@ -1245,7 +1341,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
       if (kn.tp < 1.f) {
         // top-k first: the nucleus of the top-k set; joint: the nucleus of the whole row,
         // intersected with the top-k set (the larger threshold)
-        const bool jt = a.joint && tk;
+        const bool jt = EXT && a.joint && tk;
         const uint64_t Zref = jt ? gmass(1ull) : Z;
         const double want = ceil((double)kn.tp * (double)Zref);
         const uint64_t P = (want > (double)Zref) ? Zref : (uint64_t)want;
@@ -1254,7 +1350,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
         C = max(C, Cp);
         Z = gmass(C);
       }
-      if (kn.mp > 0.f) {
+      if (use_mp) {
         // min_p: of the kept tokens, those with x - M >= T ln(min_p); the passing values
         // form a top segment, so the smallest passing key bounds them (the argmax passes)
         const float thr = kn.T * logf(kn.mp);
@@ -1307,7 +1403,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
     // Top-k rows with the joint order measure top_p on the whole row's mass (one more
     // pass over the row, every compute thread); with min_p they keep only the tokens at
     // or above the value bound thr_v (x - M >= T ln(min_p)).
-    const bool jrow = a.joint && kn.kind == kCTopK && kn.tp < 1.f && !bad;
+    const bool jrow = EXT && a.joint && kn.kind == kCTopK && kn.tp < 1.f && !bad;
     uint64_t Zall = 0;
     if (jrow) {
       uint64_t sum = 0;
@@ -1319,12 +1415,9 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
       }
       (void)sel::excl_scan<kCC, CBar>(sum, sm.sc, Zall);
     }
-    const float mp_thr = kn.mp > 0.f ? kn.T * logf(kn.mp) : -INFINITY;
-    auto mp_keep = [&](uint64_t cc) -> bool {
-      return !(kn.mp > 0.f) || key_to_value((uint32_t)(cc >> kIdxBits)) - M >= mp_thr;
-    };
 
     // ---- finish the row ---------------------------------------------------------------------
+    bool go_minp = false;  // set by the kinds that leave the row to the min_p path
     if (kn.kind == kCGreedy) {
       if (tid == 0) finish_row(am, (j < D && x == am) ? 1 : 0);
     } else if (bad || kn.kind == kCGeneral) {
@@ -1353,36 +1446,40 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
       } else {
         const uint64_t C = sel::radix_adaptive<kCC, true, CBar>(
             (int)cnt, [&](int i) { return sm.w.list[i]; }, 1ull, P - A, wcomp, lowv, sm.sc);
-        for (uint32_t i = tid; i < cnt; i += kCC) {
-          const uint64_t cc = sm.w.list[i];
-          const uint32_t gidx = comp_token(cc);
-          if (cc >= C && (int32_t)gidx != x)
-            atomicAdd(reinterpret_cast<unsigned long long*>(
-                          rowslots + (gidx / N) / (kCVecs * 32)),
-                      (unsigned long long)wcomp(cc));
-        }
-        cbar();
-        auto kept = [&](float v, int64_t gidx) -> bool {
-          const int gx = six_i(v);
-          if (gx > ghi) return true;
-          return gx >= gli && comp_key(fkey(v), (uint32_t)gidx) >= C;
-        };
-        uint64_t wx = 0;
-        if (xvalid && kept(vx, x)) wx = wfn(vx);
-        mine = 0;
-        for (int64_t e = e0; e < e1; ++e) mine += __ldcg(rowslots + e);
-        uint64_t Zr;
-        const uint64_t ex = sel::excl_scan<kCC, CBar>(mine, sm.sc, Zr);
-        const int32_t acc = accept((double)(Zr + wx), (double)wx);
-        if (skip_draw) {
-          if (tid == 0) finish_row(-1, acc, 3, C, Zr + wx);
-        } else if (Zr == 0) {
-          if (tid == 0) finish_row((wx > 0) ? x : am, acc, 3, C, Zr + wx);
+        if (use_mp && !mp_keep(C)) {  // min_p's bound lies above the nucleus cut: it decides
+          go_minp = true;
         } else {
-          draw_ranges(mine, ex, Zr, e0, e1, acc, 3, C, Zr + wx, [&](float v, int64_t gidx) -> float {
-            if (gidx == (int64_t)x || v == -INFINITY || !kept(v, gidx)) return 0.f;
-            return ex2((v - M) * sl2);
-          });
+          for (uint32_t i = tid; i < cnt; i += kCC) {
+            const uint64_t cc = sm.w.list[i];
+            const uint32_t gidx = comp_token(cc);
+            if (cc >= C && (int32_t)gidx != x)
+              atomicAdd(reinterpret_cast<unsigned long long*>(
+                            rowslots + (gidx / N) / (kCVecs * 32)),
+                        (unsigned long long)wcomp(cc));
+          }
+          cbar();
+          auto kept = [&](float v, int64_t gidx) -> bool {
+            const int gx = six_i(v);
+            if (gx > ghi) return true;
+            return gx >= gli && comp_key(fkey(v), (uint32_t)gidx) >= C;
+          };
+          uint64_t wx = 0;
+          if (xvalid && kept(vx, x)) wx = wfn(vx);
+          mine = 0;
+          for (int64_t e = e0; e < e1; ++e) mine += __ldcg(rowslots + e);
+          uint64_t Zr;
+          const uint64_t ex = sel::excl_scan<kCC, CBar>(mine, sm.sc, Zr);
+          const int32_t acc = accept((double)(Zr + wx), (double)wx);
+          if (skip_draw) {
+            if (tid == 0) finish_row(-1, acc, 3, C, Zr + wx);
+          } else if (Zr == 0) {
+            if (tid == 0) finish_row((wx > 0) ? x : am, acc, 3, C, Zr + wx);
+          } else {
+            dr_C = C;
+            dr_gh = ghi;
+            dr_gl = gli;
+            draw_ranges(mine, ex, Zr, e0, e1, acc, 3, C, Zr + wx, dr_wgt);
+          }
         }
       }
     } else if (kn.kind == kCTopK && (int)sm.lcnt <= 32 * kCSmallE) {
@@ -1515,7 +1612,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
           Z = mass_from(C);
         }
       }
-      if (kn.mp > 0.f) {
+      if (use_mp) {
         // min_p: the smallest kept list value that passes the bound (the argmax does)
         uint32_t kmin = fkey(M);
         for (int i = tid; i < nl; i += kCC) {
@@ -1555,6 +1652,8 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
         tok = (int32_t)comp_token(gsel);
       }
       if (tid == 0) finish_row(tok, acc, 1, C, Z);
+    } else if (use_mp) {  // kCPlain with min_p
+      go_minp = true;
     } else {  // kCPlain: the warp ranges scaled to the row maximum, in token order
       const int64_t E_ = (int64_t)nst * kCW;
       const int64_t per = (E_ + kCC - 1) / kCC;
@@ -1626,6 +1725,9 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
           if (lane == 0) finish_row(tok >= 0 ? tok : am, acc, 2, 1ull, Zfx);
         }
       }
+    }
+    if constexpr (EXT) {
+      if (go_minp) minp_path(0);
     }
     cbar();  // the row's shared state is free for the next row
   }
@@ -1802,9 +1904,17 @@ cudaError_t launch_chain_t(const SampleArgs& a, cudaStream_t s) {
   const int64_t want = (int64_t)nsm * 2;  // two CTAs an SM
   const unsigned grid = (unsigned)(a.rows < want ? a.rows : want);
   const size_t dyn = (size_t)kCNSt * kCStageBytes + sizeof(CSmem);
-  e = cudaFuncSetAttribute(k_chain<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
-  if (e != cudaSuccess) return e;
-  k_chain<E><<<grid, kCThreads, dyn, s>>>(a);
+  if (a.min_p || a.joint) {
+    e = cudaFuncSetAttribute(k_chain<E, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)dyn);
+    if (e != cudaSuccess) return e;
+    k_chain<E, true><<<grid, kCThreads, dyn, s>>>(a);
+  } else {
+    e = cudaFuncSetAttribute(k_chain<E, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)dyn);
+    if (e != cudaSuccess) return e;
+    k_chain<E, false><<<grid, kCThreads, dyn, s>>>(a);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (a.probs_out) {
