@@ -188,10 +188,18 @@ def set_wait_cycles(cycles: int) -> None:
     _check("ts_set_wait_cycles", load().ts_set_wait_cycles(int(cycles)))
 
 
+def _dense_out(out, rows, V, device):
+    """A [rows, V] contiguous fp32 output (the C ABI writes rows of V floats back to back)."""
+    if out is None:
+        return torch.empty((rows, V), dtype=torch.float32, device=device)
+    if out.dtype != torch.float32 or tuple(out.shape) != (rows, V) or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous fp32 tensor of shape ({rows}, {V})")
+    return out
+
+
 def softmax_temp(logits, temperature=None, out=None, stream=None):
     rows, V, ld = _rows(logits)
-    if out is None:
-        out = torch.empty((rows, V), dtype=torch.float32, device=logits.device)
+    out = _dense_out(out, rows, V, logits.device)
     _check("ts_softmax_temp", load().ts_softmax_temp(
         _p(logits), _dtype(logits), rows, V, ld, _p(temperature), _p(out), _stream(stream)))
     return out
@@ -199,8 +207,7 @@ def softmax_temp(logits, temperature=None, out=None, stream=None):
 
 def topk_topp_renorm(probs, top_k=None, top_p=None, out=None, stream=None):
     rows, V, ld = _rows(probs)
-    if out is None:
-        out = torch.empty((rows, V), dtype=torch.float32, device=probs.device)
+    out = _dense_out(out, rows, V, probs.device)
     _check("ts_topk_topp_renorm", load().ts_topk_topp_renorm(
         _p(probs), rows, V, ld, _p(top_k), _p(top_p), _p(out), _stream(stream)))
     return out
