@@ -722,21 +722,11 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
               }
             }
             if (__any_sync(0xffffffffu, nsel != 0u)) {
-              uint32_t pos = warp_reserve(&sm.lcnt, nsel, lane);
-  #pragma unroll
-              for (int u = 0; u < kCVecs; ++u) {
-                if (!mk[u]) continue;
-                float xv[N];
-                SVec<E>::unpack(rv[u], xv);
-  #pragma unroll
-                for (int q = 0; q < N; ++q)
-                  if (mk[u] & (1u << q)) {
-                    if (pos < (uint32_t)kCCap)
-                      sm.w.list[pos] = comp_key(fkey(xv[q]),
-                                                (uint32_t)(c0 + (vbase + u * 32) * N + q));
-                    ++pos;
-                  }
-              }
+              const uint32_t pos = warp_reserve(&sm.lcnt, nsel, lane);
+              uint32_t m32 = 0;
+#pragma unroll
+              for (int u = 0; u < kCVecs; ++u) m32 |= mk[u] << (u * N);
+              append_candidates<E>(m32, rv, c0, vbase, pos, sm.w.list, (uint32_t)kCCap);
             }
           }
           // k > 128: the list is checked every few stages (and after the last) and compacted
@@ -881,21 +871,11 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
             nsel += (uint32_t)__popc(mk[u]);
           }
           if (__any_sync(0xffffffffu, nsel != 0u)) {
-            uint32_t pos = warp_reserve(&sm.lcnt, nsel, lane);
+            const uint32_t pos = warp_reserve(&sm.lcnt, nsel, lane);
+            uint32_t m32 = 0;
 #pragma unroll
-            for (int u = 0; u < kCVecs; ++u) {
-              if (!mk[u]) continue;
-              float xv[N];
-              SVec<E>::unpack(rv[u], xv);
-#pragma unroll
-              for (int q = 0; q < N; ++q)
-                if (mk[u] & (1u << q)) {
-                  if (pos < (uint32_t)kCCap)
-                    sm.w.list[pos] = comp_key(fkey(xv[q]),
-                                              (uint32_t)(c0 + (vbase + u * 32) * N + q));
-                  ++pos;
-                }
-            }
+            for (int u = 0; u < kCVecs; ++u) m32 |= mk[u] << (u * N);
+            append_candidates<E>(m32, rv, c0, vbase, pos, sm.w.list, (uint32_t)kCCap);
           }
           const uint64_t f = warp_sum_u64(__float2ull_rz(s * kFx));
           if (lane == 0) rowslots[c * kCW + warp] = f;

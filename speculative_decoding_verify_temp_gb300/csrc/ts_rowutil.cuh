@@ -30,6 +30,11 @@ struct SVec<float> {
                  fminf(__uint_as_float(r.z), __uint_as_float(r.w)));
   }
   __device__ __forceinline__ static float at(const float* p, int64_t i) { return p[i]; }
+  // element q (a run-time index) of a vector, by selects (no indexed register access)
+  __device__ __forceinline__ static float elem(const uint4& r, int q) {
+    const uint32_t w = q < 2 ? (q == 0 ? r.x : r.y) : (q == 2 ? r.z : r.w);
+    return __uint_as_float(w);
+  }
 };
 template <>
 struct SVec<uint16_t> {
@@ -66,7 +71,35 @@ struct SVec<uint16_t> {
   __device__ __forceinline__ static float at(const uint16_t* p, int64_t i) {
     return bf16_bits_to_f32(p[i]);
   }
+  // element q (a run-time index) of a vector, by selects (no indexed register access)
+  __device__ __forceinline__ static float elem(const uint4& r, int q) {
+    const uint32_t w = q < 4 ? (q < 2 ? r.x : r.y) : (q < 6 ? r.z : r.w);
+    return __uint_as_float((q & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
 };
+
+// Appends this lane's candidates (bit u * N + q of m32: element q of vector rv[u], token
+// c0 + (vbase + 32 u) N + q) to the list at pos .. as composite keys, one set bit at a
+// time, so that a warp spends one step per candidate of its busiest lane rather than one
+// per element slot. Entries at or past cap are dropped (the count still advances).
+template <typename E, int NV>
+__device__ __forceinline__ void append_candidates(uint32_t m32, const uint4 (&rv)[NV], int c0,
+                                                  int vbase, uint32_t pos, uint64_t* list,
+                                                  uint32_t cap) {
+  constexpr int N = SVec<E>::N;
+  while (m32) {
+    const int b = __ffs(m32) - 1;
+    m32 &= m32 - 1u;
+    const int u = b / N, q = b % N;
+    uint4 r = rv[0];
+#pragma unroll
+    for (int uu = 1; uu < NV; ++uu)
+      if (u == uu) r = rv[uu];
+    if (pos < cap)
+      list[pos] = comp_key(fkey(SVec<E>::elem(r, q)), (uint32_t)(c0 + (vbase + u * 32) * N + q));
+    ++pos;
+  }
+}
 
 __device__ __forceinline__ uint32_t comp_token(uint64_t c) {
   return kIdxMax - (uint32_t)(c & kIdxMax);
