@@ -504,25 +504,19 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
         }
         // the elements at or above the threshold
         const uint32_t tau = sm.tau;
+        uint32_t m32 = 0;
 #pragma unroll
         for (int u = 0; u < kRVecs; ++u) {
           if (!(vmv[u] > -INFINITY) || fkey(vmv[u]) < tau) continue;
-          const int vi = vbase + u * 32;
           float xv[N];
           SVec<E>::unpack(rv[u], xv);
-          uint32_t m = 0;
 #pragma unroll
           for (int q = 0; q < N; ++q)
-            if (fkey(xv[q]) >= tau && xv[q] != -INFINITY) m |= 1u << q;
-          if (!m) continue;
-          uint32_t pos = atomicAdd(&sm.lcnt, (uint32_t)__popc(m));
-#pragma unroll
-          for (int q = 0; q < N; ++q)
-            if (m & (1u << q)) {
-              if (pos < (uint32_t)kRCrossCap)
-                sm.w.cross[pos] = comp_key(fkey(xv[q]), (uint32_t)(c0 + (int64_t)vi * N + q));
-              ++pos;
-            }
+            if (fkey(xv[q]) >= tau && xv[q] != -INFINITY) m32 |= 1u << (u * N + q);
+        }
+        if (__any_sync(0xffffffffu, m32 != 0u)) {
+          const uint32_t pos = warp_reserve(&sm.lcnt, (uint32_t)__popc(m32), lane);
+          append_candidates<E>(m32, rv, (int)c0, vbase, pos, sm.w.cross, (uint32_t)kRCrossCap);
         }
       } else if (RN && kn.kind == kRowPlain) {
         // renorm without knobs: the row's exact mass
@@ -977,21 +971,11 @@ __global__ void __launch_bounds__(kRThreads, 2) k_row(SampleArgs a) {
               nsel += (uint32_t)__popc(mk[u]);
             }
             if (__any_sync(0xffffffffu, nsel != 0)) {
-              uint32_t pos = warp_reserve(&sm.lcnt, nsel, lane);
+              const uint32_t pos = warp_reserve(&sm.lcnt, nsel, lane);
+              uint32_t m32 = 0;
 #pragma unroll
-              for (int u = 0; u < kRVecs; ++u) {
-                if (!mk[u]) continue;
-                float xv[N];
-                SVec<E>::unpack(rv[u], xv);
-#pragma unroll
-                for (int q = 0; q < N; ++q)
-                  if (mk[u] & (1u << q)) {
-                    if (pos < (uint32_t)kRCrossCap)
-                      sm.w.cross[pos] = comp_key(
-                          fkey(xv[q]), (uint32_t)(c0 + (int64_t)(vbase + u * 32) * N + q));
-                    ++pos;
-                  }
-              }
+              for (int u = 0; u < kRVecs; ++u) m32 |= mk[u] << (u * N);
+              append_candidates<E>(m32, rv, (int)c0, vbase, pos, sm.w.cross, (uint32_t)kRCrossCap);
             }
           }
         }
