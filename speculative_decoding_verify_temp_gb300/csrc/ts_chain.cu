@@ -818,7 +818,11 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
               const float v = xv[q];
               const float wv = ex2(fmaf(v, sl2, -ptop));
               zs += wv;
-              const int d = pbi - (six_i(v) >> 4);
+              // the octave below the window top: from the weight's exponent (wv = 2^t, t =
+              // v sl2 - pbi - 1, so d = pbi - floor(v sl2) = 126 - biased exponent; a zero
+              // weight falls in the last bin). An element the fast 2^t puts one octave off
+              // near an octave edge only moves the window the later exact passes check.
+              const int d = 126 - (int)(__float_as_uint(wv) >> 23);
               dmin = min(dmin, d);
               sm.w.hist[min(max(d, 0), kPB - 1) * kCC + tid] += wv;
             }
