@@ -997,17 +997,27 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
           if (!okb) sm.bad = 1;
           sm.gtop = 16 * (sm.pbi - bt) + 15;
           sm.res_d = above * K;  // the mass above the window, 2^-40 units of the maximum
+          // A crossing octave that holds few tokens (each weighs at least half its top
+          // edge, so its mass bounds their number) is collected whole by pass 3, and
+          // pass 2 is skipped: its sixteenths bound the crossing elements instead.
+          sm.gh = 0;
+          sm.gl = 1;  // gl > gh: pass 2 decides the window
+          if (okb && bmass * exp2((double)(bs + 1)) <= 3500.0) {
+            sm.gh = 16 * (sm.pbi - bs) + 15;
+            sm.gl = 16 * (sm.pbi - bs);
+          }
         }
       }
       cbar();
       const bool bad1 = sm.bad != 0;
+      const bool skip2 = sm.gl <= sm.gh;  // the crossing octave is the window of pass 3
       // pass 2 (its stages are consumed in any case)
-      if (!bad1) {
+      if (!bad1 && !skip2) {
 #pragma unroll
         for (int b = 0; b < kPB; ++b) sm.w.hist[b * kCC + tid] = 0.f;
       }
       cbar();
-      if (!bad1) {
+      if (!bad1 && !skip2) {
         stream(KindTag<kCTopP>{}, KindTag<2>{});
       } else {
         for (int c = 0; c < nst; ++c, ++g) {
@@ -1016,8 +1026,8 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
         }
       }
       cbar();
-      bin_totals();
-      if (warp == 0 && !bad1) {
+      if (!skip2) bin_totals();
+      if (warp == 0 && !bad1 && !skip2) {
         // sixteenth f (0: the window's highest) in 2^-40 units of the maximum's weight,
         // after the mass above the window
         const double mf = sm.hb[lane] * 1099511627776.0;
