@@ -1477,20 +1477,24 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
         }
       }
     } else if (kn.kind == kCTopK && (int)sm.lcnt <= 32 * kCSmallE) {
-      // few candidates: one warp finishes the row. Orders come from counting (compact
-      // loops, so that this code, run once a row, stays small).
-      if (warp == 0) {
+      // few candidates: every compute thread ranks one of them by counting (composites
+      // are distinct, so the ranks are a permutation), then one warp finishes the row
+      // (compact loops, so that this code, run once a row, stays small)
+      uint64_t* srt = sm.w.list + kCHalf;  // the candidates by rank (value order)
+      {
         const int nl = (int)sm.lcnt;
-        uint64_t* srt = sm.w.list + kCHalf;        // the candidates by rank (value order)
-        uint64_t* wid = sm.w.list + kCHalf + 128;  // kept: weight by rank in id order
-        uint32_t* kid = reinterpret_cast<uint32_t*>(sm.w.list + kCHalf + 256);  // kept ids
-        for (int i = lane; i < nl; i += 32) {
+        for (int i = tid; i < nl; i += kCC) {
           const uint64_t ci = sm.w.list[i];
           int r = 0;
           for (int jj = 0; jj < nl; ++jj) r += (sm.w.list[jj] > ci) ? 1 : 0;
-          srt[r] = ci;  // composites are distinct: ranks are a permutation
+          srt[r] = ci;
         }
-        __syncwarp();
+      }
+      cbar();
+      if (warp == 0) {
+        const int nl = (int)sm.lcnt;
+        uint64_t* wid = sm.w.list + kCHalf + 128;  // kept: weight by rank in id order
+        uint32_t* kid = reinterpret_cast<uint32_t*>(sm.w.list + kCHalf + 256);  // kept ids
         uint64_t v[kCSmallE], w[kCSmallE], incl[kCSmallE];
 #pragma unroll
         for (int e = 0; e < kCSmallE; ++e) {
