@@ -118,3 +118,58 @@ def test_in_place_renorm_needs_contiguous_rows(lib):
     p = P(4096)
     st = lib.ts_topk_topp_renorm(p, 2, 100, 104, None, None, p, None)
     assert st == 1 and "in-place" in _err(lib)
+
+
+def test_next_entry_points_reject_invalid_arguments_before_launch(lib):
+    from speculative_decoding_verify_temp_gb300.tsverify import ChainArgs, SampleArgs
+    P = ctypes.c_void_p
+
+    def sample_args(**kw):
+        a = SampleArgs()
+        a.logits, a.dtype, a.n_per_req, a.batch, a.vocab, a.ld = 256, 1, 1, 4, 64, 64
+        a.seed = a.offset = a.tokens = 256
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+
+    def call(a):
+        return lib.ts_sample_from_logits(ctypes.byref(a), P(512), 1 << 30, None)
+
+    assert call(sample_args(batch=0)) == 1 and "batch" in _err(lib)  # empty
+    assert call(sample_args(n_per_req=0)) == 1 and "n_per_req" in _err(lib)
+    assert call(sample_args(filter_order=2)) == 1 and "filter_order" in _err(lib)
+    assert call(sample_args(probs=256, ld_probs=10)) == 1 and "ld_probs" in _err(lib)
+    assert call(sample_args(ld=65, vocab=65)) == 1 and "aligned" in _err(lib)  # 130-byte rows
+    assert call(sample_args(seed=None)) == 1 and "seed" in _err(lib)
+    assert call(sample_args(dtype=9)) == 2
+
+    def chain_args(**kw):
+        a = ChainArgs()
+        a.target, a.target_dtype, a.target_is_logits = 256, 1, 1
+        a.batch, a.D, a.vocab, a.ld = 2, 1, 64, 64
+        a.draft_tokens = a.accepted_tokens = a.accept_length = a.seed = a.offset = 256
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+
+    def ccall(a):
+        return lib.ts_chain_spec_sampling(ctypes.byref(a), P(512), 1 << 30, None)
+
+    assert ccall(chain_args(batch=0)) == 1  # empty
+    assert ccall(chain_args(draft_probs=256, ld_draft=64, threshold_acc=0.5)) == 1
+    assert "target-only" in _err(lib)
+    assert ccall(chain_args(target_is_logits=0, target_dtype=0, min_p=256)) == 1
+    assert "logit targets" in _err(lib)
+    assert ccall(chain_args(qo_indptr=256, total_rows=5)) == 1 and "total_rows" in _err(lib)
+    assert ccall(chain_args(qo_indptr=256, total_rows=0)) == 1 and "total_rows" in _err(lib)
+    # ragged greedy: total_rows out of range, missing qo_indptr
+    st = lib.ts_verify_chain_greedy_ragged(P(256), 1, 2, 1, 64, 64, P(256), 5, P(256), P(256),
+                                           P(256), None, None, P(512), 1 << 30, None)
+    assert st == 1 and "total_rows" in _err(lib)
+    st = lib.ts_verify_chain_greedy_ragged(P(256), 1, 2, 1, 64, 64, None, 3, P(256), P(256),
+                                           P(256), None, None, P(512), 1 << 30, None)
+    assert st == 1 and "qo_indptr" in _err(lib)
+    # an empty Gumbel call
+    st = lib.ts_gumbel_max_sample(P(256), 0, 0, 4, 100, 100, P(256), P(256), P(256), P(256),
+                                  P(512), 1 << 30, None)
+    assert st == 1
