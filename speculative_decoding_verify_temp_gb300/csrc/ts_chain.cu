@@ -683,19 +683,37 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
               if (lane == 0 && mykey) atomicMax(&sm.tau, mykey);
               cbar();
             } else {
-              uint32_t* skeys = reinterpret_cast<uint32_t*>(sm.w.list);
+              // the stage's k-th largest key, built bit by bit from the top: the largest C
+              // with at least k of the stage's finite elements at or above it (bf16 keys
+              // carry 16 bits). Each round every compute thread counts its own elements;
+              // one barrier a round sums the warps (two slots, alternating).
+              // the thread's keys (0 for -inf) in its own column of the list area (key i
+              // of thread t at i * kCC + t: no bank conflicts)
+              uint32_t* skeys = reinterpret_cast<uint32_t*>(sm.w.list) + tid;
 #pragma unroll
               for (int u = 0; u < kCVecs; ++u) {
                 float xv[N];
                 SVec<E>::unpack(rv[u], xv);
 #pragma unroll
                 for (int q = 0; q < N; ++q)
-                  skeys[(vbase + u * 32) * N + q] = (xv[q] > -INFINITY) ? fkey(xv[q]) : 0u;
+                  skeys[(u * N + q) * kCC] = (xv[q] > -INFINITY) ? fkey(xv[q]) : 0u;
               }
-              cbar();
-              const uint32_t t0 = sel::select_bound<kCC, CBar>(
-                  nc, [&](int i) { return skeys[i]; }, (uint32_t)k, bf16 ? 2 : 4, sm.sc);
-              if (tid == 0) sm.tau = t0;
+              uint32_t C = 0;
+#pragma unroll 1
+              for (int bit = 31; bit >= lowv; --bit) {
+                const uint32_t cand = C | (1u << bit);
+                uint32_t cnt = 0;
+#pragma unroll 8
+                for (int i = 0; i < kCVecs * N; ++i) cnt += (skeys[i * kCC] >= cand) ? 1u : 0u;
+                cnt = __reduce_add_sync(0xffffffffu, cnt);
+                if (lane == 0) sm.red2[bit & 1][warp] = cnt;
+                cbar();
+                uint64_t tot = 0;
+#pragma unroll
+                for (int w2 = 0; w2 < kCW; ++w2) tot += sm.red2[bit & 1][w2];
+                if (tot >= (uint64_t)k) C = cand;
+              }
+              if (tid == 0) sm.tau = C;
               cbar();
             }
           }
