@@ -85,6 +85,8 @@ constexpr long long kCDrainCycles = 1ll << 32;
 constexpr uint32_t kNoRow = 0xFFFFFFFFu;
 constexpr uint32_t kRowMask = (1u << 30) - 1u;
 constexpr double kCInvFx = 1.0 / 1099511627776.0;  // 2^-40
+constexpr float kFx1 = 17592186044416.f;            // 2^44: top-p pass 1's mass scale
+constexpr double kCInvFx1 = 1.0 / 17592186044416.0;  // 2^-44
 
 enum CKind : int { kCGreedy = 0, kCTopK = 1, kCPlain = 2, kCTopP = 3, kCGeneral = 4 };
 
@@ -621,7 +623,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
       }
       return vk;
     };
-    uint64_t z1 = 0;  // top-p pass 1: the row's mass in 2^-40 units of 2^(pbi + 1)
+    uint64_t z1 = 0;  // top-p pass 1: the row's mass in 2^-44 units of 2^(pbi + 1)
 
     // One pass over the row's stages: the statistics every row keeps, and the kind's own
     // summary. PASS is the top-p pass (1 for every other kind).
@@ -683,10 +685,12 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
               if (lane == 0 && mykey) atomicMax(&sm.tau, mykey);
               cbar();
             } else {
-              // the stage's k-th largest key, built bit by bit from the top: the largest C
-              // with at least k of the stage's finite elements at or above it (bf16 keys
-              // carry 16 bits). Each round every compute thread counts its own elements;
-              // one barrier a round sums the warps (two slots, alternating).
+              // the stage's k-th largest key, built two bits at a time from the top: the
+              // largest C with at least k of the stage's finite elements at or above it
+              // (bf16 keys carry 16 bits). Each round every compute thread counts its own
+              // elements at or above the three candidates C + {1, 2, 3} 2^(bit - 1); one
+              // barrier a round sums the warps (two slots, alternating; each count of a
+              // warp is at most 1024 and of the stage at most 7168, so they pack in 16 bits).
               // the thread's keys (0 for -inf) in its own column of the list area (key i
               // of thread t at i * kCC + t: no bank conflicts)
               uint32_t* skeys = reinterpret_cast<uint32_t*>(sm.w.list) + tid;
@@ -698,20 +702,32 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
                 for (int q = 0; q < N; ++q)
                   skeys[(u * N + q) * kCC] = (xv[q] > -INFINITY) ? fkey(xv[q]) : 0u;
               }
+              static_assert(((32 - lowv) & 1) == 0, "the key bits pair up");
               uint32_t C = 0;
 #pragma unroll 1
-              for (int bit = 31; bit >= lowv; --bit) {
-                const uint32_t cand = C | (1u << bit);
-                uint32_t cnt = 0;
+              for (int bit = 31; bit > lowv; bit -= 2) {
+                const uint32_t c1 = C | (1u << (bit - 1)), c2 = C | (2u << (bit - 1)),
+                               c3 = C | (3u << (bit - 1));
+                uint32_t n12 = 0, n3 = 0;
 #pragma unroll 8
-                for (int i = 0; i < kCVecs * N; ++i) cnt += (skeys[i * kCC] >= cand) ? 1u : 0u;
-                cnt = __reduce_add_sync(0xffffffffu, cnt);
-                if (lane == 0) sm.red2[bit & 1][warp] = cnt;
+                for (int i = 0; i < kCVecs * N; ++i) {
+                  const uint32_t key = skeys[i * kCC];
+                  n12 += ((key >= c1) ? 1u : 0u) + ((key >= c2) ? 0x10000u : 0u);
+                  n3 += (key >= c3) ? 1u : 0u;
+                }
+                n12 = __reduce_add_sync(0xffffffffu, n12);
+                n3 = __reduce_add_sync(0xffffffffu, n3);
+                const int slot = (bit >> 1) & 1;
+                if (lane == 0) sm.red2[slot][warp] = (uint64_t)n12 | ((uint64_t)n3 << 32);
                 cbar();
                 uint64_t tot = 0;
 #pragma unroll
-                for (int w2 = 0; w2 < kCW; ++w2) tot += sm.red2[bit & 1][w2];
-                if (tot >= (uint64_t)k) C = cand;
+                for (int w2 = 0; w2 < kCW; ++w2) tot += sm.red2[slot][w2];
+                const uint32_t t1 = (uint32_t)(tot & 0xFFFFu), t2 = (uint32_t)((tot >> 16) & 0xFFFFu),
+                               t3 = (uint32_t)(tot >> 32);
+                if (t3 >= (uint32_t)k) C = c3;
+                else if (t2 >= (uint32_t)k) C = c2;
+                else if (t1 >= (uint32_t)k) C = c1;
               }
               if (tid == 0) sm.tau = C;
               cbar();
@@ -825,28 +841,37 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
           }
           const int pbi = sm.pbi;
           const float ptop = (float)(pbi + 1);
-          int dmin = 0;  // negative if an element lies above the window
           float zs = 0.f;
 #pragma unroll
           for (int u = 0; u < kCVecs; ++u) {
             float xv[N];
             SVec<E>::unpack(rv[u], xv);
+            // the octave below the window top: from the weight's exponent (wv = 2^t, t =
+            // v sl2 - pbi - 1, so d = pbi - floor(v sl2) = 126 - biased exponent; a zero
+            // weight falls in the last bin). An element the fast 2^t puts one octave off
+            // near an octave edge only moves the window the later exact passes check.
+            // The vector maximum has the vector's smallest d: below 0, an element lies
+            // above the window (the row goes to the general path).
+            const int dv = 126 - (int)(__float_as_uint(ex2(fmaf(vmv[u], sl2, -ptop))) >> 23);
+            if (dv < 0) sm.bad = 1;
+            if (__all_sync(0xffffffffu, dv >= kPB - 1)) {
+              // the warp's vectors lie in the lowest bin, whose mass no crossing uses
+              // (a crossing there sends the row to the general path): the row's mass only
 #pragma unroll
-            for (int q = 0; q < N; ++q) {
-              const float v = xv[q];
-              const float wv = ex2(fmaf(v, sl2, -ptop));
-              zs += wv;
-              // the octave below the window top: from the weight's exponent (wv = 2^t, t =
-              // v sl2 - pbi - 1, so d = pbi - floor(v sl2) = 126 - biased exponent; a zero
-              // weight falls in the last bin). An element the fast 2^t puts one octave off
-              // near an octave edge only moves the window the later exact passes check.
-              const int d = 126 - (int)(__float_as_uint(wv) >> 23);
-              dmin = min(dmin, d);
-              sm.w.hist[min(max(d, 0), kPB - 1) * kCC + tid] += wv;
+              for (int q = 0; q < N; ++q) zs += ex2(fmaf(xv[q], sl2, -ptop));
+            } else {
+#pragma unroll
+              for (int q = 0; q < N; ++q) {
+                const float wv = ex2(fmaf(xv[q], sl2, -ptop));
+                zs += wv;
+                const unsigned d = (unsigned)(126 - (int)(__float_as_uint(wv) >> 23));
+                sm.w.hist[min(d, (unsigned)(kPB - 1)) * kCC + tid] += wv;
+              }
             }
           }
-          if (dmin < 0) sm.bad = 1;
-          z1 += __float2ull_rz(zs * kFx);
+          // at most 32 weights of at most 1 each (else the row is flagged above): the
+          // stage's share in 2^-44 units of the window top, rounded to nearest
+          z1 += __float2ull_rn(zs * kFx1);
         } else if constexpr (KIND == kCTopP && PASS == 2) {
           // pass 2 (the row maximum known): sixteenth bins over the window's two octaves,
           // weights relative to the maximum
@@ -899,7 +924,15 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
             for (int u = 0; u < kCVecs; ++u) m32 |= mk[u] << (u * N);
             append_candidates<E>(m32, rv, c0, vbase, pos, sm.w.list, (uint32_t)kCCap);
           }
-          const uint64_t f = warp_sum_u64(__float2ull_rz(s * kFx));
+          // the warp's sum (each lane's below 2^46: 32 weights of at most 1) by two 32-bit
+          // reductions, of the low 24 bits and of the rest; none where the range keeps nothing
+          const uint64_t fl = __float2ull_rz(s * kFx);
+          uint64_t f = 0ull;
+          if (__any_sync(0xffffffffu, fl != 0ull)) {
+            const uint32_t lo = __reduce_add_sync(0xffffffffu, (uint32_t)(fl & 0xFFFFFFu));
+            const uint32_t hi = __reduce_add_sync(0xffffffffu, (uint32_t)(fl >> 24));
+            f = ((uint64_t)hi << 24) + lo;
+          }
           if (lane == 0) rowslots[c * kCW + warp] = f;
         }
       }
@@ -987,7 +1020,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
       if (warp == 0) {
         uint64_t zt = 0;
         for (int w2 = 0; w2 < kCW; ++w2) zt += sm.red2[0][w2];
-        const double zrel = (double)zt * kCInvFx;  // the row's mass, units of 2^(pbi + 1)
+        const double zrel = (double)zt * kCInvFx1;  // the row's mass, units of 2^(pbi + 1)
         const double mb = sm.hb[lane];
         double incl = mb;
 #pragma unroll
