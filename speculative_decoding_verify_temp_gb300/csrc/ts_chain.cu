@@ -971,17 +971,22 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
           sm.M = v;
           sm.am = (i == INT32_MAX) ? 0 : i;
           sm.S1 = s;
-          const CCoin cc = ccoin(a, req, D);
-          const uint64_t seed = a.seed ? (uint64_t)a.seed[cc.sreq] : 0;
-          const uint64_t off = a.offset ? (uint64_t)a.offset[cc.sreq] : 0;
-          const bool coins = kn.kind != kCGreedy;
-          sm.uj = (coins && j < D) ? (a.uniforms ? a.uniforms[req * a.R + j]
-                                                 : verify_coin(seed, off, (uint32_t)j))
-                                   : 0.f;
-          sm.uD = coins ? (a.uniforms ? a.uniforms[req * a.R + D] : verify_coin(seed, off, cc.pos))
-                        : 0.f;
-          sm.vx = xvalid ? SVec<E>::at(xr, x) : 0.f;
-          sm.qx = (a.q && j < D && xvalid) ? a.q[(req * DP + j) * a.ld_q + x] : 0.f;
+          // greedy rows need neither coins nor the draft token's logit
+          float uj0 = 0.f, uD0 = 0.f, vx0 = 0.f, qx0 = 0.f;
+          if (kn.kind != kCGreedy) {
+            const CCoin cc = ccoin(a, req, D);
+            const uint64_t seed = a.seed ? (uint64_t)a.seed[cc.sreq] : 0;
+            const uint64_t off = a.offset ? (uint64_t)a.offset[cc.sreq] : 0;
+            if (j < D)
+              uj0 = a.uniforms ? a.uniforms[req * a.R + j] : verify_coin(seed, off, (uint32_t)j);
+            uD0 = a.uniforms ? a.uniforms[req * a.R + D] : verify_coin(seed, off, cc.pos);
+            vx0 = xvalid ? SVec<E>::at(xr, x) : 0.f;
+            qx0 = (a.q && j < D && xvalid) ? a.q[(req * DP + j) * a.ld_q + x] : 0.f;
+          }
+          sm.uj = uj0;
+          sm.uD = uD0;
+          sm.vx = vx0;
+          sm.qx = qx0;
         }
       }
       cbar();
@@ -1174,10 +1179,14 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
         rr.gl = sm.gl;
       }
       a.ws.rowres[row] = rr;
-      __threadfence();
-      const uint32_t prev = atomicAdd(&a.ws.creq[req], 1u);
+      // one acquire-release count: publishes this record and, for the last row of the
+      // request, makes the other rows' records visible
+      uint32_t prev;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                   : "=r"(prev)
+                   : "l"(&a.ws.creq[req])
+                   : "memory");
       if (prev != (uint32_t)D) return;
-      __threadfence();
       int32_t js = D;
       for (int32_t jj = 0; jj < D; ++jj)
         if (!__ldcg(&a.ws.rowres[rbase + jj].acc)) {
