@@ -466,12 +466,12 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": traffic,
-                     "kernel": "k_chain<bf16> (the step: a one-CTA planning launch, then it)",
-                     "timed": "the whole step (both launches) with CUDA events",
+                     "kernel": "k_chain<bf16> (the step: a one-CTA planning launch, it, then the one-thread-a-request chain writer)",
+                     "timed": "the whole step (all three launches) with CUDA events",
                      "algorithmic_bytes_per_launch": alg_bytes},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 3 * args.steps,
         "clocks": clocks,
         "legs": legs,
     }
@@ -623,7 +623,7 @@ def run_legs(args, d, logits, device, tv, synth, peak):
                   workspace=tv.make_workspace(B, R, V, device), outputs=outs)
         ms = time_device(lambda: tv.chain_spec_sampling(logits, True, D, drafts, **kw), steps,
                          warm, device)
-        rec(name, ms, rows, rows * V * 2, launches=2)
+        rec(name, ms, rows, rows * V * 2, launches=3)
         if parity:
             legs[name]["parity"] = leg_parity(
                 "chain", bits, True, R, [True, D, d["draft_tokens"]],
@@ -680,7 +680,7 @@ def run_legs(args, d, logits, device, tv, synth, peak):
         ms = time_device(lambda: tv.sample_from_logits(logits, R, **kn_rows, joint=True, seed=seed,
                                                        offset=off, workspace=wss, out=stok),
                          steps, warm, device)
-        rec(name, ms, rows, rows * V * 2, launches=2)
+        rec(name, ms, rows, rows * V * 2, launches=3)
         if parity:
             legs[name]["parity"] = leg_parity(
                 "sample", bits, True, R, [R],
@@ -698,7 +698,7 @@ def run_legs(args, d, logits, device, tv, synth, peak):
                                                        offset=off, workspace=wss, out=stok,
                                                        probs=pbuf),
                          steps, warm, device)
-        rec(name, ms, rows, rows * V * (2 + 4), launches=3)
+        rec(name, ms, rows, rows * V * (2 + 4), launches=4)
         del pbuf
     # the verify step with min_p and relaxed acceptance thresholds
     name = "verify_step_min_p_relaxed_B512_D3_V201088_bf16"
@@ -712,7 +712,7 @@ def run_legs(args, d, logits, device, tv, synth, peak):
                   threshold_single=0.9, threshold_acc=0.5)
         ms = time_device(lambda: tv.chain_spec_sampling(logits, True, D, drafts, **kw), steps,
                          warm, device)
-        rec(name, ms, rows, rows * V * 2, launches=2)
+        rec(name, ms, rows, rows * V * 2, launches=3)
     # ragged verification: windows of 1 to 4 rows of the step's logits
     name = "verify_ragged_B512_D3_V201088_bf16"
     if want(name):
@@ -730,7 +730,7 @@ def run_legs(args, d, logits, device, tv, synth, peak):
         ms = time_device(lambda: tv.chain_spec_sampling(packed, True, D, drafts, **kw), steps,
                          warm, device)
         nrow = int(qo_np[-1])
-        rec(name, ms, nrow, nrow * V * 2, launches=2)
+        rec(name, ms, nrow, nrow * V * 2, launches=3)
         del packed
     # softmax with temperature, fp32 probabilities out
     name = "softmax_B512_R4_V201088_bf16"
@@ -777,7 +777,7 @@ def run_legs(args, d, logits, device, tv, synth, peak):
         ms = time_device(lambda: tv.chain_spec_sampling(cl, True, c["D"], cd, **ca), steps, warm,
                          device)
         crows = c["B"] * (c["D"] + 1)
-        rec(name, ms, crows, crows * c["V"] * 2, launches=2)
+        rec(name, ms, crows, crows * c["V"] * 2, launches=3)
         if parity:
             legs[name]["parity"] = leg_parity(
                 "chain", c["logits_bits"], True, c["D"] + 1, [True, c["D"], c["draft_tokens"]],

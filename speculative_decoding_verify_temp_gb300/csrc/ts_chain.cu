@@ -2,7 +2,7 @@
 // flashinfer.py verify(): sampling_argmax for greedy requests; softmax with temperature,
 // fused top-k/top-p renorm and chain_speculative_sampling_target_only for the others).
 //
-// Two launches per call (three with a probability output, one more with draft
+// Three launches per call (four with a probability output, one more with draft
 // probabilities):
 //  - k_chain_plan (one CTA) orders the rows by cost tier (top-p and general rows first,
 //    then large top-k rows, then the other sampled rows, greedy rows last), so that the
@@ -40,6 +40,9 @@
 //    joint order measure top_p on the whole row's mass (one more pass over the row);
 //    other rows with min_p take one more pass that keeps the tokens above its bound
 //    (top-p rows only when that bound lies above their nucleus cut).
+//  - k_chain_write: the chain of every request whose rows are all recorded (accepted
+//    tokens, accept index, logprobs, accept_length), one thread a request. A row only
+//    stores its record and counts itself, without waiting on the count.
 //  - k_chain_resid (draft probabilities): the residual draw of each rejected row.
 //  - k_chain_probs (single-step sampling with a probability output): each row's kept
 //    distribution, rebuilt from the row's record.
@@ -1170,7 +1173,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
     // With draft probabilities the residual draw of a rejected row needs the draft row:
     // rows before the last record their kept set and leave the draw to k_chain_resid.
     const bool skip_draw = qmode && j < D;
-    // records the row; the last row of its request to be recorded writes the chain
+    // records the row (k_chain_write then writes the chains of complete requests)
     auto finish_row = [&](int32_t tok_f, int32_t acc_f, int32_t kset = 0, uint64_t Cf = 0,
                           uint64_t Zf = 0) {
       RowRes rr{M, am, sm.S1, tok_f, acc_f, {0, 0, 0}, Cf, Zf, 0, 0, kset, 0};
@@ -1179,44 +1182,9 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
         rr.gl = sm.gl;
       }
       a.ws.rowres[row] = rr;
-      // one acquire-release count: publishes this record and, for the last row of the
-      // request, makes the other rows' records visible
-      uint32_t prev;
-      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
-                   : "=r"(prev)
-                   : "l"(&a.ws.creq[req])
-                   : "memory");
-      if (prev != (uint32_t)D) return;
-      int32_t js = D;
-      for (int32_t jj = 0; jj < D; ++jj)
-        if (!__ldcg(&a.ws.rowres[rbase + jj].acc)) {
-          js = jj;
-          break;
-        }
-      // positions of the padded outputs; a ragged window's rows past it read as unused
-      for (int32_t jj = 0; jj < a.R; ++jj) {
-        const int64_t oj = req * a.R + jj;
-        const int64_t rj = rbase + jj;  // the packed row of position jj (jj <= D)
-        int32_t t = -1;
-        if (jj < js) t = a.draft_tokens[req * DP + jj];
-        else if (jj == js) t = __ldcg(&a.ws.rowres[rj].tok);
-        if (qmode && jj == js && js < D) {  // the residual kernel writes this position
-          if (a.accept_index) a.accept_index[oj] = (int32_t)rj;
-          continue;
-        }
-        a.accepted_tokens[oj] = t;
-        if (a.accept_index) a.accept_index[oj] = (jj <= js) ? (int32_t)rj : -1;
-        if (a.logprobs) {
-          float lp = 0.f;
-          if (jj <= js && t >= 0 && (int64_t)t < V) {
-            const E* xj = reinterpret_cast<const E*>(a.x) + rj * a.ld;
-            lp = (SVec<E>::at(xj, t) - __ldcg(&a.ws.rowres[rj].M)) -
-                 logf(__ldcg(&a.ws.rowres[rj].S));
-          }
-          a.logprobs[oj] = lp;
-        }
-      }
-      a.accept_length[req] = js + 1;
+      // the request's count of recorded rows (k_chain_write, the next launch, writes the
+      // chains of the requests whose rows are all recorded)
+      asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(&a.ws.creq[req]) : "memory");
     };
     // Warp 0 walks the 32 vectors from row vector v0 (one a lane) and returns the first
     // element at which the running weight exceeds tf (the last element with weight if
@@ -1793,6 +1761,55 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
 }
 
 
+// The chain of every request whose rows have all recorded their results (TokenSpeed
+// verify(): the accepted draft prefix, then the row's corrected or bonus token): accepted
+// tokens (-1 past the chain), accept index, logprobs and accept_length. A request with a
+// row left unrecorded (a stage wait that gave up) keeps accept_length = 0 from the
+// planning launch; with draft probabilities the rejected position is left to
+// k_chain_resid. One thread a request.
+template <typename E>
+__global__ void __launch_bounds__(256) k_chain_write(SampleArgs a) {
+  const int64_t req = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (req >= a.nreq) return;
+  const CWin win = cwin(a, req);
+  if (win.count < 1 || __ldcg(&a.ws.creq[req]) != (uint32_t)win.count) return;
+  const int64_t rbase = win.first;
+  const int32_t D = win.count - 1;
+  const int32_t DP = a.D;
+  const int64_t V = a.V;
+  const bool qmode = a.q != nullptr;
+  int32_t js = D;
+  for (int32_t jj = 0; jj < D; ++jj)
+    if (!__ldcg(&a.ws.rowres[rbase + jj].acc)) {
+      js = jj;
+      break;
+    }
+  // positions of the padded outputs; a ragged window's rows past it read as unused
+  for (int32_t jj = 0; jj < a.R; ++jj) {
+    const int64_t oj = req * a.R + jj;
+    const int64_t rj = rbase + jj;  // the packed row of position jj (jj <= D)
+    int32_t t = -1;
+    if (jj < js) t = a.draft_tokens[req * DP + jj];
+    else if (jj == js) t = __ldcg(&a.ws.rowres[rj].tok);
+    if (qmode && jj == js && js < D) {  // the residual kernel writes this position
+      if (a.accept_index) a.accept_index[oj] = (int32_t)rj;
+      continue;
+    }
+    a.accepted_tokens[oj] = t;
+    if (a.accept_index) a.accept_index[oj] = (jj <= js) ? (int32_t)rj : -1;
+    if (a.logprobs) {
+      float lp = 0.f;
+      if (jj <= js && t >= 0 && (int64_t)t < V) {
+        const E* xj = reinterpret_cast<const E*>(a.x) + rj * a.ld;
+        lp = (SVec<E>::at(xj, t) - __ldcg(&a.ws.rowres[rj].M)) -
+             logf(__ldcg(&a.ws.rowres[rj].S));
+      }
+      a.logprobs[oj] = lp;
+    }
+  }
+  a.accept_length[req] = js + 1;
+}
+
 // With draft probabilities, the residual draw of every request rejected before its last
 // row (TensorRT-LLM rejection_sampling_one_model: at the first rejection j*, a token from
 // norm(max(p - q, 0))): p''_j* is recomputed from the row's recorded kept set (its
@@ -1973,6 +1990,9 @@ cudaError_t launch_chain_t(const SampleArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     k_chain<E, false><<<grid, kCThreads, dyn, s>>>(a);
   }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k_chain_write<E><<<(unsigned)((a.nreq + 255) / 256), 256, 0, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (a.probs_out) {
