@@ -41,7 +41,7 @@
 //    other rows with min_p take one more pass that keeps the tokens above its bound
 //    (top-p rows only when that bound lies above their nucleus cut).
 //  - k_chain_write: the chain of every request whose rows are all recorded (accepted
-//    tokens, accept index, logprobs, accept_length), one thread a request. A row only
+//    tokens, accept index, logprobs, accept_length), one warp a request. A row only
 //    stores its record and counts itself, without waiting on the count.
 //  - k_chain_resid (draft probabilities): the residual draw of each rejected row.
 //  - k_chain_probs (single-step sampling with a probability output): each row's kept
@@ -1766,10 +1766,11 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
 // tokens (-1 past the chain), accept index, logprobs and accept_length. A request with a
 // row left unrecorded (a stage wait that gave up) keeps accept_length = 0 from the
 // planning launch; with draft probabilities the rejected position is left to
-// k_chain_resid. One thread a request.
+// k_chain_resid. One warp a request: lane j takes position j (and j + 32, ...).
 template <typename E>
 __global__ void __launch_bounds__(256) k_chain_write(SampleArgs a) {
-  const int64_t req = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int64_t req = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (req >= a.nreq) return;
   const CWin win = cwin(a, req);
   if (win.count < 1 || __ldcg(&a.ws.creq[req]) != (uint32_t)win.count) return;
@@ -1778,14 +1779,19 @@ __global__ void __launch_bounds__(256) k_chain_write(SampleArgs a) {
   const int32_t DP = a.D;
   const int64_t V = a.V;
   const bool qmode = a.q != nullptr;
+  // the first rejected position (D if every draft is accepted)
   int32_t js = D;
-  for (int32_t jj = 0; jj < D; ++jj)
-    if (!__ldcg(&a.ws.rowres[rbase + jj].acc)) {
-      js = jj;
+  for (int32_t j0 = 0; j0 < D; j0 += 32) {
+    const int32_t jj = j0 + lane;
+    const bool rej = jj < D && !__ldcg(&a.ws.rowres[rbase + jj].acc);
+    const unsigned m = __ballot_sync(0xffffffffu, rej);
+    if (m) {
+      js = j0 + __ffs(m) - 1;
       break;
     }
+  }
   // positions of the padded outputs; a ragged window's rows past it read as unused
-  for (int32_t jj = 0; jj < a.R; ++jj) {
+  for (int32_t jj = lane; jj < a.R; jj += 32) {
     const int64_t oj = req * a.R + jj;
     const int64_t rj = rbase + jj;  // the packed row of position jj (jj <= D)
     int32_t t = -1;
@@ -1807,7 +1813,7 @@ __global__ void __launch_bounds__(256) k_chain_write(SampleArgs a) {
       a.logprobs[oj] = lp;
     }
   }
-  a.accept_length[req] = js + 1;
+  if (lane == 0) a.accept_length[req] = js + 1;
 }
 
 // With draft probabilities, the residual draw of every request rejected before its last
@@ -1992,7 +1998,7 @@ cudaError_t launch_chain_t(const SampleArgs& a, cudaStream_t s) {
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k_chain_write<E><<<(unsigned)((a.nreq + 255) / 256), 256, 0, s>>>(a);
+  k_chain_write<E><<<(unsigned)((a.nreq * 32 + 255) / 256), 256, 0, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (a.probs_out) {
