@@ -252,23 +252,6 @@ __device__ __noinline__ uint4 ragged_vec(const E* xr, int e0, int n) {
   return make_uint4(wv[0], wv[1], wv[2], wv[3]);
 }
 
-// The largest key C, down to bit lowbit, such that at least k of the warp's keys (E a
-// lane) are >= C: the k-th largest key with its bits below lowbit cleared, or 0 if the
-// warp holds fewer than k keys. Bisection on the bits, one ballot per key and bit.
-template <int E>
-__device__ __forceinline__ uint32_t warp_kth_key(const uint32_t (&key)[E], int k, int lowbit) {
-  uint32_t res = 0u;
-#pragma unroll 1
-  for (int bit = 31; bit >= lowbit; --bit) {
-    const uint32_t cand = res | (1u << bit);
-    int cnt = 0;
-#pragma unroll
-    for (int e = 0; e < E; ++e) cnt += __popc(__ballot_sync(0xffffffffu, key[e] >= cand));
-    if (cnt >= k) res = cand;
-  }
-  return res;
-}
-
 // two CTAs an SM: their rings and state fit the SM's 228 KB of shared memory (1 KB of it
 // reserved per CTA)
 static_assert(2 * (kCNSt * kCStageBytes + sizeof(CSmem) + 1024) <= 233472, "two CTAs an SM");
@@ -675,17 +658,44 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
 
         if constexpr (KIND == kCTopK) {
           if (c == 0) {
-            // a lower bound of the row's k-th value from the first stage. k <= 128: every
-            // warp finds the k-th largest of its own 128 vector maxima by bisection on the
-            // key bits
-            // and the row keeps the largest of these (each is the k-th largest of a subset
-            // of the row); one barrier. Larger k: the stage's k-th largest value.
+            // a lower bound of the row's k-th value from the first stage. k <= 128: the k-th
+            // largest of the stage's 896 vector maxima (distinct elements, so at least k of
+            // the row's elements lie at or above it), built two key bits a round: each
+            // thread counts its four maxima at or above the candidates C + {1, 2, 3}
+            // 2^(bit - 1), one barrier a round sums the warps (two slots, alternating; the
+            // counts are at most 896 and pack in 16 bits). Larger k: the stage's k-th
+            // largest value, the same way over its elements.
             if (k <= kCMerge) {
               uint32_t kv[kCVecs];
 #pragma unroll
               for (int u = 0; u < kCVecs; ++u) kv[u] = (vmv[u] > -INFINITY) ? fkey(vmv[u]) : 0u;
-              const uint32_t mykey = warp_kth_key(kv, k, lowv);
-              if (lane == 0 && mykey) atomicMax(&sm.tau, mykey);
+              static_assert(((32 - lowv) & 1) == 0, "the key bits pair up");
+              uint32_t C = 0;
+#pragma unroll 1
+              for (int bit = 31; bit > lowv; bit -= 2) {
+                const uint32_t c1 = C | (1u << (bit - 1)), c2 = C | (2u << (bit - 1)),
+                               c3 = C | (3u << (bit - 1));
+                uint32_t n12 = 0, n3 = 0;
+#pragma unroll
+                for (int u = 0; u < kCVecs; ++u) {
+                  n12 += ((kv[u] >= c1) ? 1u : 0u) + ((kv[u] >= c2) ? 0x10000u : 0u);
+                  n3 += (kv[u] >= c3) ? 1u : 0u;
+                }
+                n12 = __reduce_add_sync(0xffffffffu, n12);
+                n3 = __reduce_add_sync(0xffffffffu, n3);
+                const int slot = (bit >> 1) & 1;
+                if (lane == 0) sm.red2[slot][warp] = (uint64_t)n12 | ((uint64_t)n3 << 32);
+                cbar();
+                uint64_t tot = 0;
+#pragma unroll
+                for (int w2 = 0; w2 < kCW; ++w2) tot += sm.red2[slot][w2];
+                const uint32_t t1 = (uint32_t)(tot & 0xFFFFu), t2 = (uint32_t)((tot >> 16) & 0xFFFFu),
+                               t3 = (uint32_t)(tot >> 32);
+                if (t3 >= (uint32_t)k) C = c3;
+                else if (t2 >= (uint32_t)k) C = c2;
+                else if (t1 >= (uint32_t)k) C = c1;
+              }
+              if (tid == 0) sm.tau = C;
               cbar();
             } else {
               // the stage's k-th largest key, built two bits at a time from the top: the
