@@ -698,22 +698,28 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
               if (tid == 0) sm.tau = C;
               cbar();
             } else {
-              // the stage's k-th largest key, built two bits at a time from the top: the
-              // largest C with at least k of the stage's finite elements at or above it
-              // (bf16 keys carry 16 bits). Each round every compute thread counts its own
-              // elements at or above the three candidates C + {1, 2, 3} 2^(bit - 1); one
-              // barrier a round sums the warps (two slots, alternating; each count of a
-              // warp is at most 1024 and of the stage at most 7168, so they pack in 16 bits).
-              // the thread's keys (0 for -inf) in its own column of the list area (key i
-              // of thread t at i * kCC + t: no bank conflicts)
+              // the k-th largest of the stage's pair maxima (the larger of each two
+              // neighbouring elements: distinct elements, so at least k of the row's
+              // elements lie at or above it; half the keys of an element-wise bound, and a
+              // little looser), built two bits at a time from the top: the largest C with
+              // at least k pair maxima at or above it (bf16 keys carry 16 bits). Each round
+              // every compute thread counts its own keys at or above the three candidates
+              // C + {1, 2, 3} 2^(bit - 1); one barrier a round sums the warps (two slots,
+              // alternating; a warp's counts are at most 512 and the stage's at most 3584,
+              // so they pack in 16 bits). The thread's keys (0 for -inf) sit in its own
+              // column of the list area (key i of thread t at i * kCC + t: no bank
+              // conflicts).
+              constexpr int NP = N / 2;  // pairs a vector
               uint32_t* skeys = reinterpret_cast<uint32_t*>(sm.w.list) + tid;
 #pragma unroll
               for (int u = 0; u < kCVecs; ++u) {
                 float xv[N];
                 SVec<E>::unpack(rv[u], xv);
 #pragma unroll
-                for (int q = 0; q < N; ++q)
-                  skeys[(u * N + q) * kCC] = (xv[q] > -INFINITY) ? fkey(xv[q]) : 0u;
+                for (int q = 0; q < NP; ++q) {
+                  const float pm = fmaxf(xv[2 * q], xv[2 * q + 1]);
+                  skeys[(u * NP + q) * kCC] = (pm > -INFINITY) ? fkey(pm) : 0u;
+                }
               }
               static_assert(((32 - lowv) & 1) == 0, "the key bits pair up");
               uint32_t C = 0;
@@ -723,7 +729,7 @@ __global__ void __launch_bounds__(kCThreads, 2) k_chain(SampleArgs a) {
                                c3 = C | (3u << (bit - 1));
                 uint32_t n12 = 0, n3 = 0;
 #pragma unroll 8
-                for (int i = 0; i < kCVecs * N; ++i) {
+                for (int i = 0; i < kCVecs * NP; ++i) {
                   const uint32_t key = skeys[i * kCC];
                   n12 += ((key >= c1) ? 1u : 0u) + ((key >= c2) ? 0x10000u : 0u);
                   n3 += (key >= c3) ? 1u : 0u;

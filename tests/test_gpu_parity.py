@@ -577,7 +577,9 @@ def _route_rows(V, dtype, rng):
 @pytest.mark.parametrize("V,dtype", [(32000, "bf16"), (201088, "bf16"), (60000, "f32")])
 @pytest.mark.parametrize("k,p,T", [(1, 1.0, 1.0), (50, 1.0, 0.7), (1000, 0.9, 1.5),
                                    (3000, 1.0, 1.0), (0, 0.95, 1.5), (0, 0.5, 0.3),
-                                   (0, 0.0, 1.0), (7, 0.0, 1.0), (0, 1.0, 1.2)])
+                                   (0, 0.0, 1.0), (7, 0.0, 1.0), (0, 1.0, 1.2),
+                                   (64, 1.0, 1.0), (100, 0.9, 0.8), (128, 1.0, 1.3),
+                                   (129, 0.95, 1.0), (500, 1.0, 0.6)])
 def test_selection_routes(V, dtype, k, p, T):
     rng = np.random.default_rng(V + k + int(100 * p))
     d = _route_rows(V, dtype, rng)
