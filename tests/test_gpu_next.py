@@ -45,7 +45,7 @@ def _rows(rng, rows, V, dtype, ld=None):
 def _knobs(rng, rows, with_min_p):
     T = rng.uniform(0.3, 1.5, rows).astype(np.float32)
     T[rng.random(rows) < 0.2] = 0.0
-    k = rng.choice(np.array([0, 1, 20, 50, 1000, 5000], np.int32), rows).astype(np.int32)
+    k = rng.choice(np.array([0, 1, 20, 50, 100, 300, 1000, 5000], np.int32), rows).astype(np.int32)
     p = rng.choice(np.array([1.0, 0.95, 0.9, 0.5], np.float32), rows).astype(np.float32)
     mp = None
     if with_min_p:
